@@ -1,0 +1,421 @@
+"""Pins for the fp64 CPU oracle: closed forms, invariants, a textbook reduction
+and brute force on tiny inputs.  Each test states which part of the definition
+(gfx950 'Unified paged attention on gfx950, from the math up', section 1) a
+plausible mistake in the oracle would break.  CPU only."""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_varlen_flash_gb300 import workloads as W
+from tests.helpers import (decode_tag, gather_logical, position_tags, scatter_logical,
+                           token_of_row)
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "micro_examples.json")
+
+
+def _run(w, **over):
+    kw = dict(causal=w.causal, softcap=w.softcap, window=w.window,
+              alibi_slopes=w.alibi_slopes, sinks=w.sinks)
+    kw.update(over)
+    return oracle.forward(w.q, w.k_cache, w.v_cache, w.block_table, w.cu_seqlens_q,
+                          w.seqused_k, w.scale, **kw)
+
+
+def _blank(seqlens_q, seqlens_k, hq=4, hk=2, d=64, b=16, seed=0, **kw):
+    need = sum((k + b - 1) // b for k in seqlens_k)
+    return W.build("pin", hq, hk, d, b, seqlens_q, seqlens_k, need + 3, 1.0 / math.sqrt(d),
+                   seed=seed, values=False, poison=True, bt_pad=1, **kw)
+
+
+def _visible_range(i, ctx, sk, causal, window):
+    hi = i + ctx if causal else sk - 1
+    lo = max(0, i + ctx - window + 1) if window > 0 else 0
+    return lo, hi
+
+
+# --------------------------------------------------------------------------
+# Closed form: constant keys -> O = mean of the visible V rows.
+# Pins the causal / window edges, ctx = S_k - S_q, the paged lookup and the
+# normalisation (a dropped or extra key, a wrong ctx or a wrong block changes
+# the mean of the position tags).
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("causal,window", [(True, 0), (True, 7), (True, 1), (False, 0),
+                                           (True, 200)])
+def test_constant_keys_give_mean_of_visible_values(causal, window):
+    sq = [5, 16, 1, 33]
+    sk = [37, 16, 50, 90]
+    w = _blank(sq, sk, causal=causal, window=window, seed=3)
+    g = torch.Generator().manual_seed(5)
+    w.q = torch.randn(w.total_q, w.hq, w.d, generator=g).to(torch.bfloat16)
+    kl, vl = [], []
+    c = torch.randn(w.hk, w.d, generator=g)
+    for s in range(w.num_seqs):
+        kl.append(c.expand(sk[s], w.hk, w.d).clone())
+        vl.append(position_tags(sk[s], w.hk, w.d))
+    scatter_logical(w, kl, vl)
+    out = _run(w)
+    for tok, (s, i, ctx) in enumerate(token_of_row(w)):
+        lo, hi = _visible_range(i, ctx, sk[s], causal, window)
+        js = np.arange(lo, hi + 1, dtype=np.float64)
+        for h in range(w.hq):
+            o = out[tok, h]
+            assert abs(o[0] - np.mean(js % 256)) < 1e-12
+            assert abs(o[1] - np.mean(js // 256)) < 1e-12
+            assert abs(o[2] - h // w.g) < 1e-12
+            assert abs(o[3] - np.mean((5 * js + 3) % 256)) < 1e-12
+            assert np.all(o[4:] == 0)
+
+
+def test_window_of_one_returns_the_diagonal_value():
+    """W = 1 keeps only key i + ctx, so O = V_{i+ctx} whatever the logits are
+    (the page-literal reading that keeps W + 1 keys would average two rows)."""
+    sq = [4, 9, 1]
+    sk = [20, 9, 33]
+    w = _blank(sq, sk, window=1, seed=4)
+    g = torch.Generator().manual_seed(6)
+    w.q = torch.randn(w.total_q, w.hq, w.d, generator=g).to(torch.bfloat16)
+    kl = [torch.randn(k, w.hk, w.d, generator=g) for k in sk]
+    vl = [position_tags(k, w.hk, w.d) for k in sk]
+    scatter_logical(w, kl, vl)
+    out = _run(w)
+    for tok, (s, i, ctx) in enumerate(token_of_row(w)):
+        for h in range(w.hq):
+            assert decode_tag(out[tok, h]) == (i + ctx, h // w.g)
+            assert abs(out[tok, h, 3] - (5 * (i + ctx) + 3) % 256) < 1e-12
+
+
+# --------------------------------------------------------------------------
+# One dominant key per (row, kv head): O = V_target to far below bf16 ulp.
+# Pins the GQA head map, the token -> sequence map and the paged lookup.
+# --------------------------------------------------------------------------
+def test_dominant_key_selects_its_value_row():
+    sq = [7, 30, 1]
+    sk = [40, 30, 77]
+    w = _blank(sq, sk, hq=8, hk=2, seed=8)
+    w.scale = 1.0
+    q = torch.zeros(w.total_q, w.hq, w.d)
+    kl = [torch.zeros(k, w.hk, w.d) for k in sk]
+    g = torch.Generator().manual_seed(9)
+    targets = {}
+    for tok, (s, i, ctx) in enumerate(token_of_row(w)):
+        q[tok, :, i] = 1.0
+        for hkv in range(w.hk):
+            t = int(torch.randint(0, i + ctx + 1, (1,), generator=g))
+            targets[(tok, hkv)] = t
+            kl[s][t, hkv, i] = 64.0
+    w.q = q.to(torch.bfloat16)
+    scatter_logical(w, kl, [position_tags(k, w.hk, w.d) for k in sk])
+    out = _run(w)
+    for tok, (s, i, ctx) in enumerate(token_of_row(w)):
+        for h in range(w.hq):
+            t = targets[(tok, h // w.g)]
+            assert decode_tag(out[tok, h]) == (t, h // w.g)
+            assert abs(out[tok, h, 0] - (t % 256)) < 1e-9
+
+
+# --------------------------------------------------------------------------
+# Sinks: with K = 0 every logit is 0, so a sink of ln(m n) gives
+# O = mean(V) / (1 + m); +inf gives 0; -inf is the same as no sink.
+# --------------------------------------------------------------------------
+def test_sink_closed_forms():
+    n = 45
+    w = _blank([1], [n], hq=4, hk=1, seed=10)
+    g = torch.Generator().manual_seed(11)
+    w.q = torch.randn(1, w.hq, w.d, generator=g).to(torch.bfloat16)
+    scatter_logical(w, [torch.zeros(n, 1, w.d)], [position_tags(n, 1, w.d)])
+    mean0 = np.mean(np.arange(n) % 256)
+    sinks = torch.tensor([math.log(n * (h + 1)) for h in range(w.hq)], dtype=torch.float64)
+    out = _run(w, sinks=sinks)
+    for h in range(w.hq):
+        assert abs(out[0, h, 0] - mean0 / (h + 2)) < 1e-12
+    inf = _run(w, sinks=torch.full((w.hq,), math.inf, dtype=torch.float64))
+    assert np.all(inf == 0.0)
+    ninf = _run(w, sinks=torch.full((w.hq,), -math.inf, dtype=torch.float64))
+    assert np.array_equal(ninf, _run(w, sinks=None))
+
+
+# --------------------------------------------------------------------------
+# Softcap: c -> 0 flattens every logit (O -> mean of visible V); c -> inf is
+# the identity; and a tiny cap applied before ALiBi leaves pure ALiBi weights
+# (if ALiBi came first the tiny cap would flatten it too).
+# --------------------------------------------------------------------------
+def _random_kv(w, seed):
+    g = torch.Generator().manual_seed(seed)
+    w.q = torch.randn(w.total_q, w.hq, w.d, generator=g).to(torch.bfloat16)
+    kl = [torch.randn(k, w.hk, w.d, generator=g) for k in w.seqlens_k]
+    vl = [position_tags(k, w.hk, w.d) for k in w.seqlens_k]
+    scatter_logical(w, kl, vl)
+
+
+def test_softcap_limits():
+    sq, sk = [6, 3], [40, 70]
+    w = _blank(sq, sk, seed=12)
+    _random_kv(w, 13)
+    tiny = _run(w, softcap=1e-9)
+    for tok, (s, i, ctx) in enumerate(token_of_row(w)):
+        js = np.arange(0, i + ctx + 1)
+        for h in range(w.hq):
+            assert abs(tiny[tok, h, 0] - np.mean(js % 256)) < 1e-6
+    big = _run(w, softcap=1e12)
+    base = _run(w, softcap=0.0)
+    assert np.max(np.abs(big - base)) < 1e-10
+
+
+def _geometric_mean_index(lo, n, a):
+    """Mean of j over j = lo .. lo+n-1 under weights e^{a j} (closed form of a
+    geometric series)."""
+    r = math.exp(a)
+    return lo + r / (1 - r) - n * r ** n / (1 - r ** n)
+
+
+@pytest.mark.parametrize("window", [0, 9])
+def test_alibi_closed_form_and_order_after_softcap(window):
+    sq, sk = [3, 1], [60, 25]
+    w = _blank(sq, sk, hq=4, hk=2, window=window, seed=14)
+    slopes = torch.tensor([0.5, 0.25, 0.125, 0.0625], dtype=torch.float64)
+    g = torch.Generator().manual_seed(15)
+    w.q = torch.randn(w.total_q, w.hq, w.d, generator=g).to(torch.bfloat16)
+    vl = [position_tags(k, w.hk, w.d) for k in sk]
+    # K = 0: logits are exactly slope * (j - ctx).
+    scatter_logical(w, [torch.zeros(k, w.hk, w.d) for k in sk], vl)
+    out0 = _run(w, alibi_slopes=slopes)
+    # Random K but a vanishing cap applied first: the same ALiBi-only weights.
+    scatter_logical(w, [torch.randn(k, w.hk, w.d, generator=g) for k in sk], vl)
+    out1 = _run(w, alibi_slopes=slopes, softcap=1e-9)
+    for tok, (s, i, ctx) in enumerate(token_of_row(w)):
+        lo, hi = _visible_range(i, ctx, sk[s], True, window)
+        for h in range(w.hq):
+            want = _geometric_mean_index(lo, hi - lo + 1, float(slopes[h]))
+            assert abs(out0[tok, h, 0] - want) < 1e-9
+            assert abs(out1[tok, h, 0] - want) < 1e-6
+
+
+# --------------------------------------------------------------------------
+# Invariants.
+# --------------------------------------------------------------------------
+def _flagged_random(seed, **kw):
+    w = W.random_small(seed, num_seqs=4, hq=8, hk=2, d=64, b=16, sq=(1, 30),
+                       ctx=(0, 60), **kw)
+    return w
+
+
+def test_weights_sum_to_one_and_reproduce_the_output():
+    w = _flagged_random(20, softcap=5.0, window=17, sinks=True, alibi=True)
+    for tok in range(0, w.total_q, 7):
+        for h in (0, 3, 7):
+            wt, o = oracle.row_weights(w.q, w.k_cache, w.v_cache, w.block_table,
+                                       w.cu_seqlens_q, w.seqused_k, w.scale, tok, h,
+                                       causal=True, softcap=5.0, window=17,
+                                       alibi_slopes=w.alibi_slopes, sinks=w.sinks)
+            assert abs(wt.sum() - 1.0) < 1e-12
+            assert np.all(wt >= 0)
+            s, i, ctx = token_of_row(w)[tok]
+            lo, hi = _visible_range(i, ctx, w.seqlens_k[s], True, 17)
+            assert np.all(wt[:lo] == 0) and np.all(wt[hi + 1:-1] == 0)
+            vl = gather_logical(w, w.v_cache, s)[:, h // w.g].double().numpy()
+            assert np.max(np.abs(wt[:-1] @ vl - o)) < 1e-12
+
+
+def test_block_permutation_leaves_output_unchanged():
+    w = _flagged_random(21, softcap=30.0, sinks=True)
+    base = _run(w)
+    g = torch.Generator().manual_seed(22)
+    perm = torch.randperm(w.num_blocks, generator=g)
+    k2 = torch.empty_like(w.k_cache)
+    v2 = torch.empty_like(w.v_cache)
+    k2[perm] = w.k_cache
+    v2[perm] = w.v_cache
+    bt = w.block_table.clone()
+    used = bt >= 0
+    bt[used] = perm[bt[used].long()].to(torch.int32)
+    w.k_cache, w.v_cache, w.block_table = k2, v2, bt
+    assert np.array_equal(_run(w), base)
+
+
+def test_chunk_rows_equal_full_prefill_rows():
+    L, m = 70, 23
+    full = _blank([L], [L], seed=23)
+    _random_kv(full, 24)
+    chunk = _blank([m], [L], seed=23)
+    chunk.k_cache, chunk.v_cache, chunk.block_table = full.k_cache, full.v_cache, full.block_table
+    chunk.q = full.q[L - m:].clone()
+    a = _run(full)[L - m:]
+    b = _run(chunk)
+    assert np.array_equal(a, b)
+
+
+def test_gqa_equals_replicated_mha():
+    w = _flagged_random(25, sinks=True, alibi=True, window=11)
+    gqa = _run(w)
+    rep = W.build("rep", w.hq, w.hq, w.d, w.b, w.seqlens_q, w.seqlens_k, w.num_blocks,
+                  w.scale, values=False, poison=False)
+    rep.q = w.q
+    rep.block_table = w.block_table
+    rep.k_cache = w.k_cache.repeat_interleave(w.g, dim=2)
+    rep.v_cache = w.v_cache.repeat_interleave(w.g, dim=2)
+    mha = _run(rep, alibi_slopes=w.alibi_slopes, sinks=w.sinks, window=11)
+    assert np.array_equal(gqa, mha)
+
+
+def test_window_wider_than_context_is_no_window():
+    w = _flagged_random(26)
+    assert np.array_equal(_run(w, window=10 ** 6), _run(w, window=0))
+
+
+# --------------------------------------------------------------------------
+# Textbook reduction: S_q = S_k, one block, identity table -> ordinary causal
+# scaled-dot-product attention, here torch's fp64 math on the CPU.
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("hq,hk,causal", [(2, 2, True), (6, 2, True), (4, 4, False)])
+def test_reduces_to_textbook_sdpa(hq, hk, causal):
+    S, d = 48, 64
+    w = W.build("sdpa", hq, hk, d, S, [S], [S], 1, 1.0 / math.sqrt(d), seed=27,
+                causal=causal, poison=False, block_ids=torch.tensor([0]))
+    out = _run(w)
+    q = w.q.double().permute(1, 0, 2)                    # [hq, S, d]
+    k = w.k_cache[0].double().permute(1, 0, 2)           # [hk, S, d]
+    v = w.v_cache[0].double().permute(1, 0, 2)
+    k = k.repeat_interleave(hq // hk, dim=0)
+    v = v.repeat_interleave(hq // hk, dim=0)
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        q, k, v, is_causal=causal, scale=w.scale).permute(1, 0, 2).numpy()
+    assert np.max(np.abs(out - ref)) < 1e-12
+
+
+# --------------------------------------------------------------------------
+# Brute force with a different algorithm: the streaming (m, l, o) recurrence
+# over random key tiles (gfx1151 ALGORITHM.md section 3) and random split
+# points merged by re-basing to the global max (gfx950 ALGORITHM.md section 5)
+# reach the same rows as the oracle's direct evaluation.
+# --------------------------------------------------------------------------
+def _streamed_row(logits, vrows, sink, rng):
+    n = len(logits)
+    cuts = sorted(set(rng.integers(0, n + 1, size=rng.integers(0, 4)).tolist()) | {0, n})
+    parts = []
+    for a, b in zip(cuts[:-1], cuts[1:]):
+        m, l, o = -np.inf, 0.0, np.zeros(vrows.shape[1])
+        t = a
+        while t < b:
+            e = min(b, t + int(rng.integers(1, 9)))
+            s_t = logits[t:e]
+            m_new = max(m, np.max(s_t)) if e > t else m
+            if m_new == -np.inf:
+                t = e
+                continue
+            alpha = math.exp(m - m_new) if m > -np.inf else 0.0
+            p = np.exp(s_t - m_new)
+            l = alpha * l + p.sum()
+            o = alpha * o + p @ vrows[t:e]
+            m = m_new
+            t = e
+        parts.append((m, l, o))
+    M = max([p[0] for p in parts] + [sink])
+    if M == -np.inf:
+        return np.zeros(vrows.shape[1])
+    L = sum(math.exp(p[0] - M) * p[1] for p in parts if p[0] > -np.inf)
+    O = sum(math.exp(p[0] - M) * p[2] for p in parts if p[0] > -np.inf)
+    if sink > -np.inf:
+        L += math.exp(sink - M)
+    return O / L if L > 0 else np.zeros(vrows.shape[1])
+
+
+@pytest.mark.parametrize("seed", [30, 31, 32])
+def test_streaming_and_split_merge_agree_with_direct_rows(seed):
+    w = _flagged_random(seed, softcap=8.0, window=13, sinks=True, alibi=True)
+    out = _run(w)
+    rng = np.random.default_rng(seed)
+    for tok, (s, i, ctx) in enumerate(token_of_row(w)):
+        K = gather_logical(w, w.k_cache, s).double().numpy()
+        V = gather_logical(w, w.v_cache, s).double().numpy()
+        for h in range(w.hq):
+            hk = h // w.g
+            x = w.scale * (K[:, hk] @ w.q[tok, h].double().numpy())
+            x = 8.0 * np.tanh(x / 8.0)
+            x = x + float(w.alibi_slopes[h]) * (np.arange(len(x)) - ctx)
+            lo, hi = _visible_range(i, ctx, len(x), True, 13)
+            logits = x[lo:hi + 1]
+            row = _streamed_row(logits, V[lo:hi + 1, hk], float(w.sinks[h]), rng)
+            assert np.max(np.abs(row - out[tok, h])) < 1e-12
+
+
+# --------------------------------------------------------------------------
+# Hand-derived worked examples (tests/golden/micro_examples.json).
+# --------------------------------------------------------------------------
+def golden_cases():
+    with open(GOLDEN) as f:
+        return json.load(f)["cases"]
+
+
+def golden_workload(case):
+    sq, sk = case["seqlens_q"], case["seqlens_k"]
+    w = W.build(case["name"], case["hq"], case["hk"], case["d"], case["b"], sq, sk,
+                sum((k + case["b"] - 1) // case["b"] for k in sk) + 2, case["scale"],
+                seed=0, values=False, poison=True, causal=case["causal"],
+                softcap=case["softcap"], window=case["window"])
+    q = torch.zeros(w.total_q, w.hq, w.d)
+    for tok, h, dim, val in case["q"]:
+        q[tok, h, dim] = val
+    kl = [torch.zeros(k, w.hk, w.d) for k in sk]
+    vl = [torch.zeros(k, w.hk, w.d) for k in sk]
+    for s, j, hk, dim, val in case["k"]:
+        kl[s][j, hk, dim] = val
+    for s, j, hk, dim, val in case["v"]:
+        vl[s][j, hk, dim] = val
+    w.q = q.to(torch.bfloat16)
+    scatter_logical(w, kl, vl)
+    if case["sinks"] is not None:
+        w.sinks = torch.tensor(case["sinks"], dtype=torch.float64)
+    if case["alibi"] is not None:
+        w.alibi_slopes = torch.tensor(case["alibi"], dtype=torch.float64)
+    expected = np.zeros((w.total_q, w.hq, w.d))
+    for tok, h, dim, val in case["expected"]:
+        expected[tok, h, dim] = val
+    return w, expected
+
+
+@pytest.mark.parametrize("case", golden_cases(), ids=lambda c: c["name"])
+def test_golden_micro_examples(case):
+    w, expected = golden_workload(case)
+    assert np.max(np.abs(_run(w) - expected)) < 1e-12
+
+
+# --------------------------------------------------------------------------
+# Malformed inputs and degenerate shapes.
+# --------------------------------------------------------------------------
+def test_rejects_context_shorter_than_chunk_and_bad_blocks():
+    w = _blank([5], [5], seed=40)
+    w.seqused_k = torch.tensor([4], dtype=torch.int32)
+    with pytest.raises(oracle.OracleError) as e:
+        _run(w)
+    assert e.value.code == -2
+    w = _blank([5], [5], seed=40)
+    w.block_table[0, 0] = w.num_blocks
+    with pytest.raises(oracle.OracleError) as e:
+        _run(w)
+    assert e.value.code == -3
+
+
+def test_empty_sequences_and_zero_context():
+    w = _blank([0, 3, 0], [0, 3, 9], seed=41)
+    _random_kv(w, 42)
+    out = _run(w)
+    assert out.shape == (3, w.hq, w.d)
+    assert np.all(np.isfinite(out))
+    # First row of a self-attention sequence sees only key 0: O = V_0.
+    V0 = gather_logical(w, w.v_cache, 1)[0].double().numpy()
+    for h in range(w.hq):
+        assert np.max(np.abs(out[0, h] - V0[h // w.g])) < 1e-12
+
+
+def test_sampled_rows_match_full_forward():
+    w = _flagged_random(43, softcap=20.0, sinks=True, window=25)
+    full = _run(w)
+    ids = W.sample_rows(w, 40, seed=1)
+    part = oracle.forward_workload(w, row_ids=ids)
+    flat = full.reshape(-1, w.d)
+    assert np.array_equal(part, flat[ids.numpy()])
