@@ -1,0 +1,436 @@
+#!/usr/bin/env python
+"""Benchmark of the unified paged varlen attention forward pass on GB300.
+
+One step = one forward call (every stage of the path: work decomposition,
+paged K/V gather, scores, score transforms, online softmax, P.V, split
+partials and their combine) over one batch of synthetic input already
+resident in HBM.  The headline workload is the decode batch (64 sequences,
+S_q = 1, S_k ~ U{512..8192}, H 32/8, d = 128, b = 16, 40,000-block pool); the
+metric is the K/V bytes the path must read per second.  The same JSON line
+also carries the prefill workloads' TFLOPS (``per_config``), the roofline
+object of the dominant kernel, the host-buffer end-to-end number, the CPU
+oracle baseline and the SM clocks sampled during the timed region.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+N > 1 runs under torchrun: every rank processes its own batch (weak scaling,
+no collective on the data path); value = bytes of all ranks / max time.
+``--impl reference`` times the fp64 CPU oracle on the same workload and
+metric (the host cores' baseline, not a GPU implementation).
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "prefill TFLOPS and decode KV-read GB/s on 1×GB300, as % of roofline"
+HEADLINE = "decode"
+SECONDARY = ["chunked", "long_prefill", "wide_mha_alibi"]
+L2_FLUSH_BYTES = 256 << 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+KERNEL_SOURCES = {
+    "split_kernel": ["ua_split.cu", "ua_ptx.cuh", "ua_common.cuh"],
+    "prefill_kernel": ["ua_prefill.cu", "ua_ptx.cuh", "ua_common.cuh", "ua_tc.cuh"],
+}
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def dist_info():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash(kernel):
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES[kernel]:
+        p = os.path.join(ROOT, "paged_varlen_flash_gb300", "csrc", name)
+        if os.path.exists(p):
+            with open(p, "rb") as f:
+                h.update(f.read())
+    return h.hexdigest()
+
+
+def recorded_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernel's source changed since the counters were taken."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f).get(kernel)
+    except Exception:
+        return None
+    if not rec or rec.get("workload") != workload:
+        return None
+    if rec.get("source_sha256") != kernel_source_hash(kernel):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi in the background."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=2)
+
+    def summary(self, t0, t1):
+        rows = [s for t, s in self.samples if t0 - 0.3 <= t <= t1 + 0.3]
+        if not rows and self.samples:
+            mid = 0.5 * (t0 + t1)
+            rows = [min(self.samples, key=lambda x: abs(x[0] - mid))[1]]
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            parts = [p.strip() for p in r.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def workload_units(w):
+    """(algorithmic bytes, algorithmic flops) of one forward pass of w."""
+    kv = w.kv_bytes_read()
+    qo = 2 * w.total_q * w.hq * w.d * 2
+    meta = sum((k + w.b - 1) // w.b for k in w.seqlens_k) * 4 + (2 * w.num_seqs + 1) * 4
+    flops = 4.0 * w.d * w.hq * w.visible_pairs()
+    return kv + qo + meta, flops
+
+
+def time_ours(w, steps, warmup, flush, torch, ua):
+    prob = ua.Problem.for_workload(w)
+    out = torch.empty_like(w.q)
+    stream = torch.cuda.current_stream()
+    flush_buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=w.q.device)
+    for _ in range(warmup):
+        prob.forward_workload(w, out=out)
+    torch.cuda.synchronize()
+    assert prob.check_device_error() == 0
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for evs in ev:   # torch creates CUDA events lazily: record once so each handle exists
+        for x in evs:
+            x.record(stream)
+    launches = 0
+    torch.cuda.synchronize()
+    t0 = time.time()
+    for i in range(steps):
+        if flush:
+            flush_buf.zero_()
+        s, e, ks, ke = ev[i]
+        prob.set_profile_events(ks, ke)
+        s.record(stream)
+        prob.forward_workload(w, out=out)
+        e.record(stream)
+        launches += prob.last_launch_count()
+    torch.cuda.synchronize()
+    t1 = time.time()
+    prob.set_profile_events(None, None)
+    step_ms = [s.elapsed_time(e) for s, e, _, _ in ev]
+    kern_ms = [ks.elapsed_time(ke) for _, _, ks, ke in ev]
+    path = prob.last_path()
+    err = prob.check_device_error()
+    prob.close()
+    return dict(step_ms=step_ms, kernel_ms=kern_ms, launches=launches, path=path,
+                t0=t0, t1=t1, device_error=err)
+
+
+def time_e2e(w, steps, warmup, torch, ua):
+    """The host-buffer entry point: per-step inputs copied in from pinned host
+    memory and the output copied back, all inside the timed call."""
+    prob = ua.Problem.for_workload(w)
+    flags = ua.flags_of(w.causal, w.softcap, w.alibi_slopes is not None, w.window,
+                        w.sinks is not None)
+    q_h = w.q.cpu().pin_memory()
+    bt_h = w.block_table.cpu().pin_memory()
+    cu_h = w.cu_seqlens_q.cpu().pin_memory()
+    su_h = w.seqused_k.cpu().pin_memory()
+    sk_h = w.sinks.cpu().pin_memory() if w.sinks is not None else None
+    al_h = w.alibi_slopes.cpu().pin_memory() if w.alibi_slopes is not None else None
+    out_h = torch.empty_like(q_h).pin_memory()
+    args = (prob.handle, q_h, w.k_cache, w.v_cache, bt_h, cu_h, su_h, w.num_seqs, w.total_q,
+            w.max_seqlen_q, w.max_seqlen_k, flags, sk_h, al_h, out_h)
+    for _ in range(warmup):
+        assert ua.ua_forward_host(*args) == 0
+    stream = torch.cuda.current_stream()
+    times = []
+    for _ in range(steps):
+        s = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        assert ua.ua_forward_host(*args) == 0   # returns after the stream drained
+        e.record(stream)
+        e.synchronize()
+        times.append(s.elapsed_time(e))
+    h2d = sum(t.numel() * t.element_size() for t in (q_h, cu_h, su_h))
+    h2d += w.num_seqs * w.max_blocks_per_seq * 4
+    for t in (sk_h, al_h):
+        if t is not None:
+            h2d += t.numel() * t.element_size()
+    d2h = out_h.numel() * out_h.element_size()
+    prob.close()
+    return statistics.mean(times), h2d, d2h
+
+
+def cpu_baseline_decode(w_host, budget_s=12.0):
+    """The fp64 oracle on the host cores over a bounded sample of the decode
+    batch: whole (sequence, kv head) groups, all g query heads of each, so the
+    K/V bytes it must read are counted exactly as for the GPU."""
+    import numpy as np
+    import oracle
+    threads = oracle.default_threads()
+    order = list(range(w_host.num_seqs))
+    done_bytes, done_time, seqs = 0, 0.0, 0
+    g = w_host.hq // w_host.hk
+    cu = [0]
+    for s in w_host.seqlens_q:
+        cu.append(cu[-1] + s)
+    while done_time < budget_s and seqs < len(order):
+        s = order[seqs]
+        rows = [tok * w_host.hq + h for tok in range(cu[s], cu[s + 1]) for h in range(w_host.hq)]
+        t = time.perf_counter()
+        oracle.forward_workload(w_host, row_ids=np.array(rows, dtype=np.int64), nthreads=threads)
+        done_time += time.perf_counter() - t
+        done_bytes += w_host.seqlens_k[s] * w_host.hk * w_host.d * 2 * 2
+        seqs += 1
+    return dict(value=done_bytes / done_time / 1e9, unit="GB/s", cores=threads, kind="oracle",
+                sample="%d of %d sequences of the decode batch (all %d query heads, g=%d), "
+                       "%.1f s" % (seqs, w_host.num_seqs, w_host.hq, g, done_time))
+
+
+def run_ours(args):
+    import torch
+    import paged_varlen_flash_gb300 as ua
+    from paged_varlen_flash_gb300 import build as ua_build
+    from paged_varlen_flash_gb300 import workloads as W
+
+    rank, world, local = dist_info()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    if rank == 0:
+        ua_build.build()
+    if world > 1:
+        dist.barrier()
+    ua.load_library()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    peaks, peak_src = load_peaks()
+
+    w = W.make(HEADLINE, device=dev)
+    nbytes, _ = workload_units(w)
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.2)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    res = time_ours(w, args.steps, args.warmup, flush=False, torch=torch, ua=ua)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    total_ms = sum(res["step_ms"])
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = nbytes * world / (ms_per_step * 1e-3) / 1e9
+    kern_ms = statistics.mean(res["kernel_ms"])
+    achieved = nbytes / (kern_ms * 1e-3) / 1e9
+    clocks = sampler.summary(res["t0"], res["t1"])
+
+    # e2e through the host-buffer entry point
+    e2e_ms, h2d, d2h = time_e2e(w, max(3, min(args.steps, 20)), 2, torch, ua)
+
+    # prefill / chunked workloads: TFLOPS of the same entry point
+    per_config = {}
+    if not args.headline_only:
+        for name in SECONDARY:
+            ws = W.make(name, device=dev)
+            b_s, f_s = workload_units(ws)
+            r = time_ours(ws, max(3, min(args.steps, 10)), max(3, args.warmup), flush=True,
+                          torch=torch, ua=ua)
+            ms = statistics.mean(r["step_ms"])
+            km = statistics.mean(r["kernel_ms"])
+            per_config[name] = {
+                "ms_per_step": round(ms, 4), "tflops": round(f_s / (ms * 1e-3) / 1e12, 2),
+                "kernel_tflops": round(f_s / (km * 1e-3) / 1e12, 2),
+                "frac_of_bf16_peak": round(f_s / (km * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
+                "path": r["path"], "launches_per_step": r["launches"] // max(1, len(r["step_ms"])),
+                "flops": f_s, "bytes": b_s, "device_error": r["device_error"]}
+            del ws
+            torch.cuda.empty_cache()
+    sampler.stop()
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_decode(w.to("cpu"))
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) bf16 values, seeded lengths and block tables)",
+            "config": {
+                "workload": "decode: 64 seqs, S_q=1, S_k~U[512,8192], H_q/H_k=32/8, d=128, "
+                            "b=16, 40000-block pool, causal",
+                "num_seqs": w.num_seqs, "total_kv_tokens": int(sum(w.seqlens_k)),
+                "algorithmic_bytes_per_step": nbytes, "path": res["path"],
+                "l2": "inputs larger than L2 (1.1 GB of K/V per step), no flush",
+                "parallelism": "replicas" if world > 1 else "single GPU"},
+            "roofline": {"bound": "hbm", "kernel": "split_kernel", "achieved": round(achieved, 1),
+                         "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(achieved / peaks["hbm_gbs"], 4),
+                         "traffic": recorded_traffic("split_kernel", HEADLINE),
+                         "peak_source": peak_src, "kernel_ms": round(kern_ms, 5)},
+            "e2e": {"value": round(nbytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": round(e2e_ms, 4)},
+            "gpu_launches": res["launches"],
+            "clocks": clocks,
+            "cpu_baseline": cpu,
+            "per_config": per_config,
+            "device_error": res["device_error"],
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def run_reference(args):
+    """The fp64 CPU oracle as the reference arm, on the same workload/metric."""
+    rank, world, _ = dist_info()
+    if rank != 0:
+        return
+    import numpy as np
+    import oracle
+    from paged_varlen_flash_gb300 import workloads as W
+    w = W.make(HEADLINE, device="cpu")
+    threads = oracle.default_threads()
+    # Each step: a bounded sample of whole sequences (all heads), ~1-2 s.
+    g = w.hq // w.hk
+    rng = np.random.default_rng(0)
+    seqs = rng.choice(w.num_seqs, size=4, replace=False)
+    cu = np.concatenate([[0], np.cumsum(w.seqlens_q)])
+    rows = np.array([tok * w.hq + h for s in seqs for tok in range(cu[s], cu[s + 1])
+                     for h in range(w.hq)], dtype=np.int64)
+    nbytes = int(sum(w.seqlens_k[s] for s in seqs)) * w.hk * w.d * 2 * 2
+    for _ in range(args.warmup):
+        oracle.forward_workload(w, row_ids=rows, nthreads=threads)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.forward_workload(w, row_ids=rows, nthreads=threads)
+    el = time.perf_counter() - t
+    ms = el * 1e3 / args.steps
+    value = nbytes / (ms * 1e-3) / 1e9
+    sample = "4 of 64 decode sequences per step (all %d query heads, g=%d)" % (w.hq, g)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "decode: 64 seqs, S_q=1, S_k~U[512,8192], H_q/H_k=32/8, "
+                               "d=128, b=16, 40000-block pool, causal",
+                   "sample_bytes_per_step": nbytes},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--headline-only", action="store_true",
+                    help="skip the prefill / chunked workloads")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        log("warmup raised to 3")
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

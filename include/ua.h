@@ -1,0 +1,199 @@
+/*
+ * ua.h -- C ABI of the unified paged varlen attention forward library
+ * (libua.so, sm_103a).
+ *
+ * One forward call serves decode (S_q = 1), prefill (S_q = S_k) and chunked
+ * prefill (1 < S_q < S_k) over a block-table-mapped bf16 KV cache.  For each
+ * packed query row i of sequence s and query head h it computes
+ *
+ *     O_i = sum_j softmax(x)_j V_j   over the visible keys j of s,
+ *
+ * with the score transform applied in this fixed order (gfx950 "Unified paged
+ * attention on gfx950, from the math up", section 1 "What unified attention
+ * computes", steps 1-3 and 5-7):
+ *
+ *     x_j  = tau * <Q_i, K_j>                            scale
+ *     x_j  = c * tanh(x_j / c)            UA_FLAG_SOFTCAP
+ *     x_j += slope_h * (j - ctx)          UA_FLAG_ALIBI
+ *     drop j > i + ctx                    UA_FLAG_CAUSAL
+ *     drop j < i + ctx - W + 1            UA_FLAG_WINDOW (requires CAUSAL)
+ *     sink_h joins the denominator        UA_FLAG_SINKS (no value row)
+ *
+ * where ctx = S_k - S_q (the query chunk is the last S_q of the sequence's S_k
+ * keys, and its K/V are already in the cache), GQA maps query head h to KV head
+ * floor(h / g) with g = H_q / H_k (section 0, notation; section 4 on packing the
+ * g heads of one KV head into one tile), and a row with an empty denominator
+ * gets O_i = 0 (gfx1151 ALGORITHM.md section 6).
+ *
+ * Layouts (all row-major, contiguous, device memory owned by the caller):
+ *   q, out        bf16  [total_q, H_q, d]        packed ragged batch
+ *   k_cache,
+ *   v_cache       bf16  [num_blocks, b, H_k, d]  paged cache (section 0)
+ *   block_table   int32 [num_seqs, max_blocks_per_seq]; key j of sequence s
+ *                       lives in block block_table[s][j / b], slot j % b
+ *   cu_seqlens_q  int32 [num_seqs + 1]; sequence s owns rows
+ *                       cu_seqlens_q[s] .. cu_seqlens_q[s+1]-1, cu_seqlens_q[0] = 0
+ *   seqused_k     int32 [num_seqs]; S_k of each sequence
+ *   sinks         fp32  [H_q] natural-log sink logits (UA_FLAG_SINKS only)
+ *   alibi_slopes  fp32  [H_q] (UA_FLAG_ALIBI only)
+ * Block-table entries past ceil(S_k / b) are never read.
+ *
+ * Every call is asynchronous on the given stream and never synchronises the
+ * host.  Errors the host can see are returned as ua_status before anything is
+ * launched; errors only the device can see (bad lengths or block ids inside
+ * the metadata arrays) are recorded in a problem-owned device error word that
+ * ua_check_device_error() reads -- the kernels never trap.
+ */
+#ifndef UA_H_
+#define UA_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum ua_status {
+    UA_OK = 0,
+    UA_ERR_INVALID_ARG = 1,   /* a null or malformed argument; nothing launched */
+    UA_ERR_UNSUPPORTED = 2,   /* valid, but outside what this build implements */
+    UA_ERR_CUDA = 3,          /* a CUDA runtime call failed (see ua_last_cuda_error) */
+    UA_ERR_OUT_OF_MEMORY = 4, /* device workspace allocation failed */
+    UA_ERR_DEVICE = 5         /* the device error word was non-zero */
+} ua_status;
+
+/* Score-transform flags (section 1 of the spec above).  A problem is created
+ * with the set it may use; each call passes a subset of it. */
+enum {
+    UA_FLAG_CAUSAL = 1u << 0,
+    UA_FLAG_SOFTCAP = 1u << 1,
+    UA_FLAG_ALIBI = 1u << 2,
+    UA_FLAG_WINDOW = 1u << 3,
+    UA_FLAG_SINKS = 1u << 4
+};
+
+/* Bits of the device error word. */
+enum {
+    UA_DEVERR_CONTEXT = 1u << 0,  /* seqused_k[s] < S_q(s): rows of s are written as 0 */
+    UA_DEVERR_BLOCK_ID = 1u << 1, /* a block id outside [0, num_blocks): those keys read as 0 */
+    UA_DEVERR_CU_SEQLENS = 1u << 2, /* cu_seqlens_q decreasing or past total_q: s skipped */
+    UA_DEVERR_BOUNDS = 1u << 3,   /* S_q > max_seqlen_q or S_k > max_seqlen_k or
+                                     S_k > max_blocks_per_seq * b: rows of s written as 0
+                                     where addressable */
+    UA_DEVERR_TIMEOUT = 1u << 4   /* a bounded on-chip wait gave up; results unspecified */
+};
+
+enum { UA_DTYPE_BF16 = 0 };
+
+/*
+ * Static description of a problem family (UnifiedAttentionProblem in the
+ * gfx950 spec: one flag per bias/mask term, section 1 last paragraph and
+ * section 6).  Validated by ua_problem_create.
+ */
+typedef struct ua_problem_desc {
+    int32_t num_q_heads;        /* H_q > 0 */
+    int32_t num_kv_heads;       /* H_k > 0, H_q % H_k == 0 */
+    int32_t head_size;          /* d in {64, 128, 256} */
+    int32_t block_size;         /* b in {16, 32, 64} */
+    int64_t num_blocks;         /* physical blocks in each cache, > 0 */
+    int32_t max_num_seqs;       /* upper bound on num_seqs per call, > 0 */
+    int32_t max_blocks_per_seq; /* row stride of block_table, > 0 */
+    int64_t max_total_q;        /* upper bound on total_q per call, > 0 */
+    int32_t dtype;              /* UA_DTYPE_BF16 */
+    uint32_t flags;             /* UA_FLAG_* the calls may use */
+    float scale;                /* tau > 0 (usually 1/sqrt(d)) */
+    float softcap;              /* c > 0 when UA_FLAG_SOFTCAP, else ignored */
+    int32_t window;             /* W >= 1 when UA_FLAG_WINDOW, else ignored */
+} ua_problem_desc;
+
+typedef struct ua_problem ua_problem;
+
+/*
+ * Validate *desc and create a problem bound to the current CUDA device.  The
+ * problem owns a device workspace (split-KV partials of fp32 (m, l, o), the
+ * device error word) that is allocated here, once; ua_forward allocates
+ * nothing.  Returns UA_ERR_INVALID_ARG for malformed fields (e.g. H_q % H_k !=
+ * 0, WINDOW without CAUSAL), UA_ERR_UNSUPPORTED for d or b outside the sets
+ * above or a non-bf16 dtype, UA_ERR_OUT_OF_MEMORY if the workspace cannot be
+ * allocated.  *out is set only on UA_OK; free it with ua_destroy.
+ */
+ua_status ua_problem_create(const ua_problem_desc *desc, ua_problem **out);
+
+/*
+ * Forward pass, enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ * stream), without host synchronisation.
+ *
+ * num_seqs <= max_num_seqs; total_q = cu_seqlens_q[num_seqs] <= max_total_q;
+ * max_seqlen_q / max_seqlen_k are host-side upper bounds on S_q(s) / S_k(s)
+ * used to size the launch (the device checks them and reports
+ * UA_DEVERR_BOUNDS).  `flags` must be a subset of the problem's flags;
+ * `sinks` / `alibi_slopes` must be non-null exactly when their flag is set.
+ * All array pointers are device pointers with the layouts above, `out` must
+ * not alias any input, and q / out / caches must be 16-byte aligned.  `out` is
+ * fully written for every row of every well-formed sequence.
+ *
+ * Returns UA_ERR_INVALID_ARG (nothing launched) on a contract violation the
+ * host can see, UA_ERR_CUDA if a launch fails.
+ */
+ua_status ua_forward(ua_problem *p, const void *q, const void *k_cache, const void *v_cache,
+                     const int32_t *block_table, const int32_t *cu_seqlens_q,
+                     const int32_t *seqused_k, int32_t num_seqs, int64_t total_q,
+                     int32_t max_seqlen_q, int32_t max_seqlen_k, uint32_t flags,
+                     const float *sinks, const float *alibi_slopes, void *out,
+                     void *stream);
+
+/*
+ * Same computation with the per-step inputs and the output in HOST memory:
+ * q_host, block_table_host, cu_seqlens_q_host, seqused_k_host, sinks_host and
+ * alibi_host are copied to problem-owned device staging buffers (allocated on
+ * first use, sized by the problem's maxima), the forward runs on `stream`, the
+ * result is copied into out_host, and the call returns after `stream` has
+ * drained.  The caches stay device-resident (k_cache / v_cache are device
+ * pointers).  Pinned host memory makes the copies asynchronous DMA.
+ */
+ua_status ua_forward_host(ua_problem *p, const void *q_host, const void *k_cache,
+                          const void *v_cache, const int32_t *block_table_host,
+                          const int32_t *cu_seqlens_q_host, const int32_t *seqused_k_host,
+                          int32_t num_seqs, int64_t total_q, int32_t max_seqlen_q,
+                          int32_t max_seqlen_k, uint32_t flags, const float *sinks_host,
+                          const float *alibi_host, void *out_host, void *stream);
+
+/*
+ * Synchronise `stream`, return the device error word (UA_DEVERR_* bits) in
+ * *code and clear it.  Returns UA_ERR_DEVICE when *code != 0, UA_OK otherwise.
+ */
+ua_status ua_check_device_error(ua_problem *p, void *stream, int32_t *code);
+
+/*
+ * Number of kernel launches the most recent ua_forward / ua_forward_host call
+ * enqueued (for launch accounting in benchmarks).
+ */
+int32_t ua_last_launch_count(const ua_problem *p);
+
+/* Human-readable name of the execution path the last forward call took. */
+const char *ua_last_path(const ua_problem *p);
+
+/*
+ * Profiling hook: when both events are non-null, every later forward call
+ * records `ev_begin` on its stream immediately before launching its dominant
+ * kernel (the attention kernel, not the split combine) and `ev_end`
+ * immediately after it, so the caller can time that kernel alone with
+ * cudaEventElapsedTime.  The events (cudaEvent_t) stay owned by the caller;
+ * pass NULL, NULL to switch the hook off.
+ */
+ua_status ua_set_profile_events(ua_problem *p, void *ev_begin, void *ev_end);
+
+/* Free the workspace and the problem.  NULL is a no-op. */
+void ua_destroy(ua_problem *p);
+
+/* Static string for a status code. */
+const char *ua_status_string(ua_status s);
+
+/* Text of the last CUDA error seen by this thread inside the library. */
+const char *ua_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* UA_H_ */

@@ -1,0 +1,16 @@
+"""Unified paged varlen flash attention (forward) for GB300 / sm_103a.
+
+The computation lives in ``libua.so`` (hand-written CUDA behind the C ABI of
+``include/ua.h``).  This package is a thin ctypes binding with the same entry
+point names; it only marshals torch tensors (device memory, streams) into that
+ABI.  There is no fallback: if the library is missing, every entry point raises.
+
+Build the library with ``python -m paged_varlen_flash_gb300.build`` (or
+``__graft_entry__.build()``).
+"""
+from .binding import (  # noqa: F401
+    UA_FLAG_ALIBI, UA_FLAG_CAUSAL, UA_FLAG_SINKS, UA_FLAG_SOFTCAP, UA_FLAG_WINDOW,
+    UA_DEVERR_BLOCK_ID, UA_DEVERR_BOUNDS, UA_DEVERR_CONTEXT, UA_DEVERR_CU_SEQLENS,
+    UA_DEVERR_TIMEOUT, UAError, Problem, flags_of, lib_path, load_library,
+    ua_check_device_error, ua_destroy, ua_forward, ua_forward_host, ua_problem_create,
+    ua_status_string)

@@ -1,0 +1,426 @@
+// ua_api.cu -- the C ABI of include/ua.h: argument validation, the problem-
+// owned workspace, tensor-map encoding, and the host planner that picks the
+// execution path and launch shape for each call (gfx950 "Unified paged
+// attention on gfx950, from the math up", section 6: choose between a path
+// whose query-tile grid already fills the device and a split-KV path plus a
+// reduction when it does not).
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "ua_common.cuh"
+#include "ua_prefill.h"
+#include "ua_split.h"
+
+namespace {
+
+thread_local char g_cuda_err[256] = "";
+
+void note_cuda(cudaError_t e, const char* where) {
+    std::snprintf(g_cuda_err, sizeof g_cuda_err, "%s: %s", where, cudaGetErrorString(e));
+}
+
+constexpr int kMaxSplits = 64;
+constexpr size_t kWorkspaceCap = size_t(128) << 20;  // bytes of split partials
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+// 4-D map over a paged cache [num_blocks, b, H_k, d] (innermost first:
+// d, H_k, b, num_blocks) with a box of 64 head-dim elements (one 128-byte
+// swizzle panel), one KV head and `box_rows` consecutive slots of one block.
+// Addresses are formed by the TMA unit in 64 bits, so caches beyond 2 GiB need
+// no special path (the overflow hazard described in gfx950 section 7.2).
+bool encode_cache_map(CUtensorMap* m, const void* base, const ua_problem_desc& d, int box_rows) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t es = 2;
+    cuuint64_t dims[4] = {(cuuint64_t)d.head_size, (cuuint64_t)d.num_kv_heads,
+                          (cuuint64_t)d.block_size, (cuuint64_t)d.num_blocks};
+    cuuint64_t strides[3] = {es * d.head_size, es * d.head_size * d.num_kv_heads,
+                             es * d.head_size * d.num_kv_heads * d.block_size};
+    cuuint32_t box[4] = {64, 1, (cuuint32_t)box_rows, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
+
+}  // namespace
+
+struct ua_problem {
+    ua_problem_desc desc;
+    int device = 0;
+    int num_sms = 0;
+    int32_t* d_err = nullptr;
+    float* d_ws = nullptr;
+    size_t ws_bytes = 0;
+    // staging buffers of ua_forward_host (allocated on first use)
+    void* st_q = nullptr;
+    void* st_out = nullptr;
+    int32_t* st_bt = nullptr;
+    int32_t* st_cu = nullptr;
+    int32_t* st_su = nullptr;
+    float* st_sinks = nullptr;
+    float* st_alibi = nullptr;
+    // tensor maps of the most recent caches (re-encoded when the pointers change)
+    const void* map_k_ptr = nullptr;
+    const void* map_v_ptr = nullptr;
+    CUtensorMap map_k16, map_v16;       // 16-slot boxes (split path)
+    CUtensorMap map_kp, map_vp;         // prefill-path boxes
+    int map_p_rows = 0;
+    int last_launches = 0;
+    const char* last_path = "none";
+    cudaEvent_t prof_begin = nullptr;
+    cudaEvent_t prof_end = nullptr;
+};
+
+namespace {
+void prof_mark(const ua_problem* p, bool begin, cudaStream_t st) {
+    if (p->prof_begin && p->prof_end) cudaEventRecord(begin ? p->prof_begin : p->prof_end, st);
+}
+}  // namespace
+
+extern "C" {
+
+const char* ua_status_string(ua_status s) {
+    switch (s) {
+        case UA_OK: return "ok";
+        case UA_ERR_INVALID_ARG: return "invalid argument";
+        case UA_ERR_UNSUPPORTED: return "unsupported configuration";
+        case UA_ERR_CUDA: return "CUDA error";
+        case UA_ERR_OUT_OF_MEMORY: return "out of device memory";
+        case UA_ERR_DEVICE: return "device reported an input error";
+    }
+    return "unknown status";
+}
+
+const char* ua_last_cuda_error(void) { return g_cuda_err; }
+
+ua_status ua_problem_create(const ua_problem_desc* d, ua_problem** out) {
+    if (!d || !out) return UA_ERR_INVALID_ARG;
+    *out = nullptr;
+    const uint32_t known = UA_FLAG_CAUSAL | UA_FLAG_SOFTCAP | UA_FLAG_ALIBI | UA_FLAG_WINDOW |
+                           UA_FLAG_SINKS;
+    if (d->num_q_heads <= 0 || d->num_kv_heads <= 0 || d->num_q_heads % d->num_kv_heads != 0)
+        return UA_ERR_INVALID_ARG;
+    if (d->num_blocks <= 0 || d->max_num_seqs <= 0 || d->max_blocks_per_seq <= 0 ||
+        d->max_total_q <= 0 || d->head_size <= 0 || d->block_size <= 0)
+        return UA_ERR_INVALID_ARG;
+    if (d->flags & ~known) return UA_ERR_INVALID_ARG;
+    if (!(d->scale > 0.f) || !std::isfinite(d->scale)) return UA_ERR_INVALID_ARG;
+    if ((d->flags & UA_FLAG_SOFTCAP) && !(d->softcap > 0.f && std::isfinite(d->softcap)))
+        return UA_ERR_INVALID_ARG;
+    if ((d->flags & UA_FLAG_WINDOW) && (d->window < 1 || !(d->flags & UA_FLAG_CAUSAL)))
+        return UA_ERR_INVALID_ARG;
+    if (d->dtype != UA_DTYPE_BF16) return UA_ERR_UNSUPPORTED;
+    if (d->head_size != 64 && d->head_size != 128 && d->head_size != 256) return UA_ERR_UNSUPPORTED;
+    if (d->block_size != 16 && d->block_size != 32 && d->block_size != 64) return UA_ERR_UNSUPPORTED;
+    if (d->num_blocks > (int64_t(1) << 31) - 1) return UA_ERR_UNSUPPORTED;
+
+    ua_problem* p = new (std::nothrow) ua_problem();
+    if (!p) return UA_ERR_OUT_OF_MEMORY;
+    p->desc = *d;
+    cudaError_t e = cudaGetDevice(&p->device);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device);
+    if (e != cudaSuccess) {
+        note_cuda(e, "ua_problem_create");
+        delete p;
+        return UA_ERR_CUDA;
+    }
+    const size_t row_bytes = size_t(d->head_size + 2) * sizeof(float);
+    const size_t want = size_t(d->max_total_q) * d->num_q_heads * row_bytes * 16;
+    p->ws_bytes = std::min(want, kWorkspaceCap);
+    if (cudaMalloc(&p->d_err, sizeof(int32_t)) != cudaSuccess ||
+        cudaMalloc(&p->d_ws, p->ws_bytes) != cudaSuccess) {
+        cudaGetLastError();
+        cudaFree(p->d_err);
+        delete p;
+        return UA_ERR_OUT_OF_MEMORY;
+    }
+    e = cudaMemset(p->d_err, 0, sizeof(int32_t));
+    if (e != cudaSuccess) {
+        note_cuda(e, "ua_problem_create");
+        cudaFree(p->d_err);
+        cudaFree(p->d_ws);
+        delete p;
+        return UA_ERR_CUDA;
+    }
+    *out = p;
+    return UA_OK;
+}
+
+void ua_destroy(ua_problem* p) {
+    if (!p) return;
+    cudaFree(p->d_err);
+    cudaFree(p->d_ws);
+    cudaFree(p->st_q);
+    cudaFree(p->st_out);
+    cudaFree(p->st_bt);
+    cudaFree(p->st_cu);
+    cudaFree(p->st_su);
+    cudaFree(p->st_sinks);
+    cudaFree(p->st_alibi);
+    delete p;
+}
+
+int32_t ua_last_launch_count(const ua_problem* p) { return p ? p->last_launches : 0; }
+
+const char* ua_last_path(const ua_problem* p) { return p ? p->last_path : "none"; }
+
+ua_status ua_set_profile_events(ua_problem* p, void* ev_begin, void* ev_end) {
+    if (!p || ((ev_begin == nullptr) != (ev_end == nullptr))) return UA_ERR_INVALID_ARG;
+    p->prof_begin = reinterpret_cast<cudaEvent_t>(ev_begin);
+    p->prof_end = reinterpret_cast<cudaEvent_t>(ev_end);
+    return UA_OK;
+}
+
+ua_status ua_forward(ua_problem* p, const void* q, const void* k_cache, const void* v_cache,
+                     const int32_t* block_table, const int32_t* cu_seqlens_q,
+                     const int32_t* seqused_k, int32_t num_seqs, int64_t total_q,
+                     int32_t max_seqlen_q, int32_t max_seqlen_k, uint32_t flags,
+                     const float* sinks, const float* alibi_slopes, void* out, void* stream) {
+    if (!p) return UA_ERR_INVALID_ARG;
+    p->last_launches = 0;
+    p->last_path = "none";
+    const ua_problem_desc& d = p->desc;
+    if (num_seqs < 0 || num_seqs > d.max_num_seqs || total_q < 0 || total_q > d.max_total_q)
+        return UA_ERR_INVALID_ARG;
+    if (max_seqlen_q < 0 || max_seqlen_k < 0 || max_seqlen_q > max_seqlen_k ||
+        (int64_t)max_seqlen_k > (int64_t)d.max_blocks_per_seq * d.block_size)
+        return UA_ERR_INVALID_ARG;
+    if ((flags & ~d.flags) != 0) return UA_ERR_INVALID_ARG;
+    if ((flags & UA_FLAG_WINDOW) && !(flags & UA_FLAG_CAUSAL)) return UA_ERR_INVALID_ARG;
+    if (((flags & UA_FLAG_SINKS) != 0) != (sinks != nullptr)) return UA_ERR_INVALID_ARG;
+    if (((flags & UA_FLAG_ALIBI) != 0) != (alibi_slopes != nullptr)) return UA_ERR_INVALID_ARG;
+    if (num_seqs == 0 || total_q == 0) return UA_OK;
+    if (!q || !k_cache || !v_cache || !block_table || !cu_seqlens_q || !seqused_k || !out)
+        return UA_ERR_INVALID_ARG;
+    auto misaligned = [](const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) != 0; };
+    if (misaligned(q) || misaligned(out) || misaligned(k_cache) || misaligned(v_cache))
+        return UA_ERR_INVALID_ARG;
+    if (max_seqlen_k == 0) {
+        // Only empty sequences can be well formed; nothing to compute.
+        max_seqlen_k = 1;
+        if (max_seqlen_q > 1) return UA_ERR_INVALID_ARG;
+    }
+
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const int g = d.num_q_heads / d.num_kv_heads;
+
+    ua::FwdParams fp;
+    std::memset(&fp, 0, sizeof fp);
+    fp.q = static_cast<const __nv_bfloat16*>(q);
+    fp.block_table = block_table;
+    fp.cu_seqlens_q = cu_seqlens_q;
+    fp.seqused_k = seqused_k;
+    fp.sinks = sinks;
+    fp.alibi = alibi_slopes;
+    fp.out = static_cast<__nv_bfloat16*>(out);
+    fp.err = p->d_err;
+    fp.total_q = total_q;
+    fp.num_blocks = d.num_blocks;
+    fp.num_seqs = num_seqs;
+    fp.bt_stride = d.max_blocks_per_seq;
+    fp.max_seqlen_q = max_seqlen_q;
+    fp.max_seqlen_k = max_seqlen_k;
+    fp.hq = d.num_q_heads;
+    fp.hk = d.num_kv_heads;
+    fp.g = g;
+    fp.d = d.head_size;
+    fp.b = d.block_size;
+    fp.flags = flags;
+    fp.scale = d.scale;
+    fp.softcap = d.softcap;
+    fp.window = d.window;
+
+    if (k_cache != p->map_k_ptr || v_cache != p->map_v_ptr) {
+        if (!encode_cache_map(&p->map_k16, k_cache, d, 16) ||
+            !encode_cache_map(&p->map_v16, v_cache, d, 16)) {
+            p->map_k_ptr = p->map_v_ptr = nullptr;
+            std::snprintf(g_cuda_err, sizeof g_cuda_err, "cuTensorMapEncodeTiled failed");
+            return UA_ERR_CUDA;
+        }
+        p->map_k_ptr = k_cache;
+        p->map_v_ptr = v_cache;
+        p->map_p_rows = 0;
+    }
+
+    // ---- path choice ------------------------------------------------------
+    const int64_t rows_per_kv = (int64_t)g * max_seqlen_q;
+    const bool use_tc = ua::prefill_supported(d.head_size) && rows_per_kv > 16;
+    if (use_tc) {
+        ua::PrefillPlan plan;
+        ua::plan_prefill(fp, p->num_sms, &plan);
+        if (p->map_p_rows != plan.kv_box_rows) {
+            if (!encode_cache_map(&p->map_kp, k_cache, d, plan.kv_box_rows) ||
+                !encode_cache_map(&p->map_vp, v_cache, d, plan.kv_box_rows)) {
+                std::snprintf(g_cuda_err, sizeof g_cuda_err, "cuTensorMapEncodeTiled failed");
+                p->map_p_rows = 0;
+                return UA_ERR_CUDA;
+            }
+            p->map_p_rows = plan.kv_box_rows;
+        }
+        fp.splits = 1;
+        fp.chunk = 0;
+        prof_mark(p, true, st);
+        cudaError_t e = ua::launch_prefill(plan, p->map_kp, p->map_vp, fp, st);
+        prof_mark(p, false, st);
+        if (e != cudaSuccess) {
+            note_cuda(e, "prefill kernel launch");
+            return UA_ERR_CUDA;
+        }
+        p->last_launches = plan.launches;
+        p->last_path = "prefill_tc";
+        return UA_OK;
+    }
+
+    int rows = 1;
+    int row_tiles = 1;
+    if (rows_per_kv <= 16) {
+        while (rows < rows_per_kv) rows <<= 1;
+    } else {
+        rows = 16;
+        row_tiles = ceil_div(rows_per_kv, 16);
+    }
+    const int smem = ua::split_smem_bytes(d.head_size, rows);
+    const int cps = std::max(1, std::min(8, (228 * 1024) / (smem + 1024)));
+    const int64_t base = (int64_t)num_seqs * d.num_kv_heads * row_tiles;
+    const int64_t slots = (int64_t)p->num_sms * cps;
+    int splits = (int)std::min<int64_t>(kMaxSplits, std::max<int64_t>(1, (4 * slots + base - 1) / base));
+    splits = std::min(splits, std::max(1, ceil_div(max_seqlen_k, 256)));
+    const size_t per_split = (size_t)total_q * d.num_q_heads * (d.head_size + 2) * sizeof(float);
+    splits = (int)std::min<size_t>((size_t)splits, p->ws_bytes / per_split);
+    if (splits < 1) splits = 1;
+    int chunk = ceil_div(ceil_div(max_seqlen_k, splits), 64) * 64;
+    splits = ceil_div(max_seqlen_k, chunk);
+    if (row_tiles * (int64_t)d.num_kv_heads > 0x7fffffffLL || splits > 65535) return UA_ERR_UNSUPPORTED;
+    fp.splits = splits;
+    fp.chunk = chunk;
+    fp.row_tiles = row_tiles;
+    fp.part_o = p->d_ws;
+    fp.part_ml = p->d_ws + (size_t)total_q * d.num_q_heads * splits * d.head_size;
+
+    prof_mark(p, true, st);
+    cudaError_t e = ua::launch_split(rows, p->map_k16, p->map_v16, fp, st);
+    prof_mark(p, false, st);
+    if (e != cudaSuccess) {
+        note_cuda(e, "split kernel launch");
+        return UA_ERR_CUDA;
+    }
+    p->last_launches = 1;
+    if (splits > 1) {
+        e = ua::launch_combine(fp, st);
+        if (e != cudaSuccess) {
+            note_cuda(e, "combine kernel launch");
+            return UA_ERR_CUDA;
+        }
+        p->last_launches = 2;
+        p->last_path = "split_kv+combine";
+    } else {
+        p->last_path = "split_kv_direct";
+    }
+    return UA_OK;
+}
+
+ua_status ua_forward_host(ua_problem* p, const void* q_host, const void* k_cache,
+                          const void* v_cache, const int32_t* block_table_host,
+                          const int32_t* cu_seqlens_q_host, const int32_t* seqused_k_host,
+                          int32_t num_seqs, int64_t total_q, int32_t max_seqlen_q,
+                          int32_t max_seqlen_k, uint32_t flags, const float* sinks_host,
+                          const float* alibi_host, void* out_host, void* stream) {
+    if (!p) return UA_ERR_INVALID_ARG;
+    const ua_problem_desc& d = p->desc;
+    if (num_seqs < 0 || num_seqs > d.max_num_seqs || total_q < 0 || total_q > d.max_total_q)
+        return UA_ERR_INVALID_ARG;
+    if (num_seqs == 0 || total_q == 0) return UA_OK;
+    if (!q_host || !block_table_host || !cu_seqlens_q_host || !seqused_k_host || !out_host)
+        return UA_ERR_INVALID_ARG;
+    const size_t qbytes_max = (size_t)d.max_total_q * d.num_q_heads * d.head_size * 2;
+    if (!p->st_q) {
+        bool ok = cudaMalloc(&p->st_q, qbytes_max) == cudaSuccess &&
+                  cudaMalloc(&p->st_out, qbytes_max) == cudaSuccess &&
+                  cudaMalloc(&p->st_bt, (size_t)d.max_num_seqs * d.max_blocks_per_seq * 4) == cudaSuccess &&
+                  cudaMalloc(&p->st_cu, (size_t)(d.max_num_seqs + 1) * 4) == cudaSuccess &&
+                  cudaMalloc(&p->st_su, (size_t)d.max_num_seqs * 4) == cudaSuccess &&
+                  cudaMalloc(&p->st_sinks, (size_t)d.num_q_heads * 4) == cudaSuccess &&
+                  cudaMalloc(&p->st_alibi, (size_t)d.num_q_heads * 4) == cudaSuccess;
+        if (!ok) {
+            cudaGetLastError();
+            cudaFree(p->st_q); cudaFree(p->st_out); cudaFree(p->st_bt); cudaFree(p->st_cu);
+            cudaFree(p->st_su); cudaFree(p->st_sinks); cudaFree(p->st_alibi);
+            p->st_q = p->st_out = nullptr;
+            p->st_bt = p->st_cu = p->st_su = nullptr;
+            p->st_sinks = p->st_alibi = nullptr;
+            return UA_ERR_OUT_OF_MEMORY;
+        }
+    }
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const size_t qbytes = (size_t)total_q * d.num_q_heads * d.head_size * 2;
+    cudaError_t e = cudaMemcpyAsync(p->st_q, q_host, qbytes, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(p->st_bt, block_table_host, (size_t)num_seqs * d.max_blocks_per_seq * 4,
+                            cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(p->st_cu, cu_seqlens_q_host, (size_t)(num_seqs + 1) * 4,
+                            cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(p->st_su, seqused_k_host, (size_t)num_seqs * 4, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess && sinks_host)
+        e = cudaMemcpyAsync(p->st_sinks, sinks_host, (size_t)d.num_q_heads * 4, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess && alibi_host)
+        e = cudaMemcpyAsync(p->st_alibi, alibi_host, (size_t)d.num_q_heads * 4, cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess) {
+        note_cuda(e, "ua_forward_host upload");
+        return UA_ERR_CUDA;
+    }
+    ua_status s = ua_forward(p, p->st_q, k_cache, v_cache, p->st_bt, p->st_cu, p->st_su, num_seqs,
+                             total_q, max_seqlen_q, max_seqlen_k, flags,
+                             sinks_host ? p->st_sinks : nullptr, alibi_host ? p->st_alibi : nullptr,
+                             p->st_out, stream);
+    if (s != UA_OK) return s;
+    e = cudaMemcpyAsync(out_host, p->st_out, qbytes, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) {
+        note_cuda(e, "ua_forward_host download");
+        return UA_ERR_CUDA;
+    }
+    return UA_OK;
+}
+
+ua_status ua_check_device_error(ua_problem* p, void* stream, int32_t* code) {
+    if (!p || !code) return UA_ERR_INVALID_ARG;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    int32_t h = 0;
+    cudaError_t e = cudaStreamSynchronize(st);
+    if (e == cudaSuccess) e = cudaMemcpy(&h, p->d_err, sizeof h, cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess) e = cudaMemset(p->d_err, 0, sizeof(int32_t));
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+        note_cuda(e, "ua_check_device_error");
+        return UA_ERR_CUDA;
+    }
+    *code = h;
+    return h ? UA_ERR_DEVICE : UA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,71 @@
+// ua_common.cuh -- parameters shared by the forward kernels and the host
+// planner, and the per-sequence metadata check every kernel applies the same way.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "../../include/ua.h"
+
+namespace ua {
+
+struct FwdParams {
+    const __nv_bfloat16* q;        // [total_q, hq, d]
+    const int32_t* block_table;    // [num_seqs, bt_stride]
+    const int32_t* cu_seqlens_q;   // [num_seqs + 1]
+    const int32_t* seqused_k;      // [num_seqs]
+    const float* sinks;            // [hq] or null
+    const float* alibi;            // [hq] or null
+    __nv_bfloat16* out;            // [total_q, hq, d]
+    float* part_o;                 // [total_q * hq, splits, d] split partials
+    float* part_ml;                // [total_q * hq, splits, 2] (m in log2 units, l)
+    int32_t* err;                  // device error word
+    int64_t total_q;
+    int64_t num_blocks;
+    int32_t num_seqs;
+    int32_t bt_stride;
+    int32_t max_seqlen_q;
+    int32_t max_seqlen_k;
+    int32_t hq, hk, g, d, b;
+    uint32_t flags;
+    float scale;                   // tau
+    float softcap;                 // c
+    int32_t window;                // W
+    int32_t splits;                // split-KV segments per row (1 = direct)
+    int32_t chunk;                 // keys per segment (multiple of 64)
+    int32_t row_tiles;             // row tiles per (sequence, kv head)
+};
+
+// Per-sequence metadata check.  Returns UA_DEVERR_* bits (0 = well formed) and
+// the sequence's S_q, S_k and first packed row.
+__device__ __forceinline__ uint32_t seq_status(const FwdParams& p, int s, int& sq, int& sk,
+                                               int64_t& q0) {
+    const int32_t a = __ldg(p.cu_seqlens_q + s);
+    const int32_t e = __ldg(p.cu_seqlens_q + s + 1);
+    sk = __ldg(p.seqused_k + s);
+    q0 = a;
+    sq = e - a;
+    uint32_t st = 0;
+    if (a < 0 || e < a || (int64_t)e > p.total_q) {
+        st |= UA_DEVERR_CU_SEQLENS;
+        sq = 0;
+        return st;
+    }
+    if (sk < sq) st |= UA_DEVERR_CONTEXT;
+    if (sq > p.max_seqlen_q || sk > p.max_seqlen_k ||
+        (int64_t)sk > (int64_t)p.bt_stride * p.b)
+        st |= UA_DEVERR_BOUNDS;
+    return st;
+}
+
+// Number of split segments sequence s uses (the split kernel and the combine
+// kernel must agree on it).
+__device__ __forceinline__ int seq_segments(const FwdParams& p, uint32_t st, int sk) {
+    if (st != 0 || sk <= 0) return 1;
+    int n = (sk + p.chunk - 1) / p.chunk;
+    return n < p.splits ? n : p.splits;
+}
+
+}  // namespace ua

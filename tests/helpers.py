@@ -33,23 +33,30 @@ def gather_logical(w, cache, s):
     return torch.cat(rows, 0)
 
 
+def tag_values(j, hkv):
+    """The four tag dims of key j (int or array) in kv head hkv: every value is
+    an integer in [1, 256], exact in bf16 and never 0 (so a tiny weight on
+    another key can never survive rounding in place of an exact 0)."""
+    return ((j % 256) + 1, (j // 256) + 1, hkv + 1, ((5 * j + 3) % 256) + 1)
+
+
 def position_tags(sk, hk, d):
-    """V rows that spell out their own key index j and kv head exactly in bf16:
-    dim 0 = j mod 256, dim 1 = j // 256, dim 2 = kv head, dim 3 = (5 j + 3) mod 256,
-    the remaining dims 0."""
+    """V rows that spell out their own key index j and kv head exactly in bf16
+    (dims 0..3 = tag_values(j, kv head)); the remaining dims are 0."""
     v = torch.zeros(sk, hk, d, dtype=torch.float32)
-    j = torch.arange(sk, dtype=torch.float32)
+    j = torch.arange(sk, dtype=torch.int64)
     for h in range(hk):
-        v[:, h, 0] = torch.remainder(j, 256)
-        v[:, h, 1] = torch.div(j, 256, rounding_mode="floor")
-        v[:, h, 2] = h
-        v[:, h, 3] = torch.remainder(5 * j + 3, 256)
+        t = tag_values(j, h)
+        for k in range(4):
+            v[:, h, k] = t[k].float() if torch.is_tensor(t[k]) else float(t[k])
     return v
 
 
 def decode_tag(row):
     """Inverse of ``position_tags`` for one output row: (j, kv_head)."""
-    return int(round(float(row[0]) + 256 * float(row[1]))), int(round(float(row[2])))
+    lo = int(round(float(row[0]))) - 1
+    hi = int(round(float(row[1]))) - 1
+    return lo + 256 * hi, int(round(float(row[2]))) - 1
 
 
 def token_of_row(w):

@@ -13,7 +13,7 @@ import torch
 import oracle
 from paged_varlen_flash_gb300 import workloads as W
 from tests.helpers import (decode_tag, gather_logical, position_tags, scatter_logical,
-                           token_of_row)
+                           tag_values, token_of_row)
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "micro_examples.json")
 
@@ -61,13 +61,12 @@ def test_constant_keys_give_mean_of_visible_values(causal, window):
     out = _run(w)
     for tok, (s, i, ctx) in enumerate(token_of_row(w)):
         lo, hi = _visible_range(i, ctx, sk[s], causal, window)
-        js = np.arange(lo, hi + 1, dtype=np.float64)
+        js = np.arange(lo, hi + 1, dtype=np.int64)
         for h in range(w.hq):
             o = out[tok, h]
-            assert abs(o[0] - np.mean(js % 256)) < 1e-12
-            assert abs(o[1] - np.mean(js // 256)) < 1e-12
-            assert abs(o[2] - h // w.g) < 1e-12
-            assert abs(o[3] - np.mean((5 * js + 3) % 256)) < 1e-12
+            tags = tag_values(js, h // w.g)
+            for k in range(4):
+                assert abs(o[k] - np.mean(tags[k])) < 1e-12
             assert np.all(o[4:] == 0)
 
 
@@ -86,7 +85,7 @@ def test_window_of_one_returns_the_diagonal_value():
     for tok, (s, i, ctx) in enumerate(token_of_row(w)):
         for h in range(w.hq):
             assert decode_tag(out[tok, h]) == (i + ctx, h // w.g)
-            assert abs(out[tok, h, 3] - (5 * (i + ctx) + 3) % 256) < 1e-12
+            assert abs(out[tok, h, 3] - tag_values(i + ctx, h // w.g)[3]) < 1e-12
 
 
 # --------------------------------------------------------------------------
@@ -115,7 +114,7 @@ def test_dominant_key_selects_its_value_row():
         for h in range(w.hq):
             t = targets[(tok, h // w.g)]
             assert decode_tag(out[tok, h]) == (t, h // w.g)
-            assert abs(out[tok, h, 0] - (t % 256)) < 1e-9
+            assert abs(out[tok, h, 0] - tag_values(t, h // w.g)[0]) < 1e-9
 
 
 # --------------------------------------------------------------------------
@@ -128,7 +127,7 @@ def test_sink_closed_forms():
     g = torch.Generator().manual_seed(11)
     w.q = torch.randn(1, w.hq, w.d, generator=g).to(torch.bfloat16)
     scatter_logical(w, [torch.zeros(n, 1, w.d)], [position_tags(n, 1, w.d)])
-    mean0 = np.mean(np.arange(n) % 256)
+    mean0 = np.mean(tag_values(np.arange(n), 0)[0])
     sinks = torch.tensor([math.log(n * (h + 1)) for h in range(w.hq)], dtype=torch.float64)
     out = _run(w, sinks=sinks)
     for h in range(w.hq):
@@ -160,7 +159,7 @@ def test_softcap_limits():
     for tok, (s, i, ctx) in enumerate(token_of_row(w)):
         js = np.arange(0, i + ctx + 1)
         for h in range(w.hq):
-            assert abs(tiny[tok, h, 0] - np.mean(js % 256)) < 1e-6
+            assert abs(tiny[tok, h, 0] - np.mean(tag_values(js, 0)[0])) < 1e-6
     big = _run(w, softcap=1e12)
     base = _run(w, softcap=0.0)
     assert np.max(np.abs(big - base)) < 1e-10
@@ -190,7 +189,7 @@ def test_alibi_closed_form_and_order_after_softcap(window):
     for tok, (s, i, ctx) in enumerate(token_of_row(w)):
         lo, hi = _visible_range(i, ctx, sk[s], True, window)
         for h in range(w.hq):
-            want = _geometric_mean_index(lo, hi - lo + 1, float(slopes[h]))
+            want = _geometric_mean_index(lo, hi - lo + 1, float(slopes[h])) + 1  # tag = j + 1
             assert abs(out0[tok, h, 0] - want) < 1e-9
             assert abs(out1[tok, h, 0] - want) < 1e-6
 

@@ -1,0 +1,275 @@
+"""CUDA path vs the fp64 CPU oracle, through the C ABI (GPU only).
+
+Tolerance (the acceptance bar for bf16 outputs of N(0,1)-scale inputs):
+max-abs error <= 2e-2 and mean-abs error <= 2e-3 against the unrounded fp64
+oracle.  Index work (which key, which block, which head) is checked bit-exactly
+with position-tag values."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_varlen_flash_gb300 as ua
+from paged_varlen_flash_gb300 import workloads as W
+from tests.helpers import (decode_tag, max_mean_abs, position_tags, scatter_logical, tag_values,
+                           token_of_row)
+
+MAX_ABS = 2e-2
+MEAN_ABS = 2e-3
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from paged_varlen_flash_gb300 import build
+    build.build()
+    ua.load_library()
+
+
+def run_gpu(w, problem=None, out=None):
+    wd = w.to("cuda")
+    prob = problem or ua.Problem.for_workload(wd)
+    res = prob.forward_workload(wd, out=out)
+    err = prob.check_device_error()
+    return res.float().cpu(), err, prob
+
+
+def check_close(got, want, max_abs=MAX_ABS, mean_abs=MEAN_ABS):
+    got = np.asarray(got, dtype=np.float64)
+    assert np.all(np.isfinite(got)), "non-finite output"
+    mx, mn = max_mean_abs(got, want)
+    assert mx <= max_abs and mn <= mean_abs, (mx, mn)
+    return mx, mn
+
+
+# ---------------------------------------------------------------------------
+# Small ragged sweeps, every row checked.
+# ---------------------------------------------------------------------------
+SWEEP = [
+    # (d, b, hq, hk, sq range, ctx range, flags)
+    (64, 16, 4, 1, (1, 1), (0, 300), {}),
+    (128, 16, 32, 8, (1, 1), (100, 900), {}),
+    (128, 32, 8, 8, (1, 1), (0, 200), {}),
+    (256, 64, 4, 4, (1, 1), (0, 500), {}),
+    (128, 16, 16, 1, (1, 1), (0, 400), {}),
+    (64, 16, 8, 2, (1, 7), (0, 100), {}),
+    (128, 32, 8, 2, (1, 40), (0, 130), dict(softcap=50.0, window=64, sinks=True)),
+    (128, 16, 8, 2, (1, 3), (0, 700), dict(alibi=True)),
+    (64, 64, 4, 2, (5, 30), (0, 90), dict(causal=False)),
+    (256, 32, 2, 1, (1, 2), (0, 300), dict(sinks=True, softcap=5.0)),
+    (64, 16, 4, 4, (1, 1), (0, 50), dict(window=1)),
+]
+
+
+@pytest.mark.parametrize("case", range(len(SWEEP)))
+def test_small_sweep_matches_oracle(case):
+    d, b, hq, hk, sq, ctx, fl = SWEEP[case]
+    w = W.random_small(100 + case, num_seqs=5, hq=hq, hk=hk, d=d, b=b, sq=sq, ctx=ctx, **fl)
+    want = oracle.forward_workload(w)
+    got, err, _ = run_gpu(w)
+    assert err == 0
+    check_close(got, want)
+
+
+@pytest.mark.parametrize("d,b,g,sq", [(64, 16, 4, 128), (128, 32, 4, 300), (128, 64, 16, 40),
+                                      (256, 64, 1, 128)])
+def test_prefill_shapes_match_oracle(d, b, g, sq):
+    w = W.random_small(200 + d + b + g, num_seqs=3, hq=2 * g, hk=2, d=d, b=b, sq=(sq // 2, sq),
+                       ctx=(0, 100))
+    want = oracle.forward_workload(w)
+    got, err, _ = run_gpu(w)
+    assert err == 0
+    check_close(got, want)
+
+
+# ---------------------------------------------------------------------------
+# The five benchmark workloads.
+# ---------------------------------------------------------------------------
+def test_tiny_config_full():
+    w = W.make("tiny", poison=True)
+    want = oracle.forward_workload(w)
+    got, err, prob = run_gpu(w)
+    assert err == 0
+    check_close(got, want)
+
+
+@pytest.mark.parametrize("name", ["decode", "chunked", "long_prefill", "wide_mha_alibi"])
+def test_config_sampled_rows(name):
+    w = W.make(name, device="cuda", poison=(name != "long_prefill"))
+    prob = ua.Problem.for_workload(w)
+    out = prob.forward_workload(w)
+    assert prob.check_device_error() == 0
+    ids = W.sample_rows(w, 400, seed=7)
+    want = oracle.forward_workload(w.to("cpu"), row_ids=ids)
+    got = out.float().reshape(-1, w.d)[ids.to("cuda")].cpu().numpy()
+    check_close(got, want)
+
+
+def test_long_prefill_shuffled_table_bit_identical():
+    a = W.make("long_prefill", device="cuda")
+    b = W.make("long_prefill_shuffled", device="cuda", values=False)
+    # Same logical K/V behind a shuffled table: move every block to its new home.
+    ids = b.block_table[0].long()
+    b.k_cache = torch.empty_like(a.k_cache)
+    b.v_cache = torch.empty_like(a.v_cache)
+    b.k_cache[ids] = a.k_cache[a.block_table[0].long()]
+    b.v_cache[ids] = a.v_cache[a.block_table[0].long()]
+    b.q = a.q
+    pa = ua.Problem.for_workload(a)
+    oa = pa.forward_workload(a)
+    ob = pa.forward_workload(b)
+    assert pa.check_device_error() == 0
+    assert torch.equal(oa, ob)
+
+
+# ---------------------------------------------------------------------------
+# Bit-exact index work: one dominant key per (row, kv head) makes the output
+# equal to that key's position-tag row.
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("d,b,hq,hk,sq,sk", [(64, 16, 8, 2, [7, 30, 1], [40, 30, 77]),
+                                             (128, 16, 32, 8, [1, 1, 1], [300, 513, 17]),
+                                             (128, 64, 16, 4, [60, 2], [60, 700])])
+def test_position_tags_bit_exact(d, b, hq, hk, sq, sk):
+    need = sum((k + b - 1) // b for k in sk)
+    w = W.build("tags", hq, hk, d, b, sq, sk, need + 7, 1.0, seed=5, values=False, poison=True,
+                bt_pad=2)
+    q = torch.zeros(w.total_q, w.hq, w.d)
+    kl = [torch.zeros(k, w.hk, w.d) for k in sk]
+    g = torch.Generator().manual_seed(3)
+    targets = {}
+    for tok, (s, i, ctx) in enumerate(token_of_row(w)):
+        q[tok, :, i % d] = 1.0
+        for hkv in range(w.hk):
+            t = int(torch.randint(0, i + ctx + 1, (1,), generator=g))
+            # avoid two rows of one sequence sharing a query direction but
+            # wanting different keys
+            targets[(tok, hkv)] = t
+            kl[s][t, hkv, i % d] = 64.0
+    w.q = q.to(torch.bfloat16)
+    scatter_logical(w, kl, [position_tags(k, w.hk, w.d) for k in sk])
+    got, err, _ = run_gpu(w)
+    assert err == 0
+    want = oracle.forward_workload(w)
+    for tok, (s, i, ctx) in enumerate(token_of_row(w)):
+        for h in range(w.hq):
+            exp_tag = decode_tag(want[tok, h])
+            assert decode_tag(got[tok, h].numpy()) == exp_tag
+            row = got[tok, h].numpy()
+            assert tuple(float(x) for x in row[:4]) == tuple(float(x) for x in tag_values(*exp_tag))
+            assert np.all(row[4:] == 0)
+
+
+def test_block_permutation_bit_identical_on_gpu():
+    w = W.random_small(300, num_seqs=4, hq=8, hk=2, d=128, b=16, sq=(1, 20), ctx=(0, 400),
+                       softcap=30.0, sinks=True)
+    a, err, _ = run_gpu(w)
+    g = torch.Generator().manual_seed(1)
+    perm = torch.randperm(w.num_blocks, generator=g)
+    k2 = torch.empty_like(w.k_cache)
+    v2 = torch.empty_like(w.v_cache)
+    k2[perm] = w.k_cache
+    v2[perm] = w.v_cache
+    bt = w.block_table.clone()
+    used = bt >= 0
+    bt[used] = perm[bt[used].long()].to(torch.int32)
+    w.k_cache, w.v_cache, w.block_table = k2, v2, bt
+    b, err2, _ = run_gpu(w)
+    assert err == 0 and err2 == 0
+    assert torch.equal(a, b)
+
+
+# ---------------------------------------------------------------------------
+# Hand-derived worked examples (tests/golden) on the GPU.  bf16 output
+# rounding is relative, so the bound scales with |expected|.
+# ---------------------------------------------------------------------------
+def test_golden_examples_on_gpu():
+    from tests.test_oracle_pins import golden_cases, golden_workload
+    for case in golden_cases():
+        w, expected = golden_workload(case)
+        if w.sinks is not None:
+            w.sinks = w.sinks.float()
+        if w.alibi_slopes is not None:
+            w.alibi_slopes = w.alibi_slopes.float()
+        got, err, _ = run_gpu(w)
+        assert err == 0, case["name"]
+        tol = MAX_ABS * np.maximum(1.0, np.abs(expected))
+        assert np.all(np.abs(got.numpy() - expected) <= tol), case["name"]
+
+
+# ---------------------------------------------------------------------------
+# Errors: host-visible contract violations launch nothing; malformed metadata
+# is reported through the device error word without a trap.
+# ---------------------------------------------------------------------------
+def test_host_contract_violations():
+    w = W.random_small(400, num_seqs=2, d=64, b=16).to("cuda")
+    prob = ua.Problem.for_workload(w)
+    out = torch.empty_like(w.q)
+    args = [w.q, w.k_cache, w.v_cache, w.block_table, w.cu_seqlens_q, w.seqused_k, w.num_seqs,
+            w.total_q, w.max_seqlen_q, w.max_seqlen_k]
+    fl = ua.UA_FLAG_CAUSAL
+    # sinks pointer without the flag, and the flag without a pointer
+    sinks = torch.zeros(w.hq, device="cuda")
+    assert ua.ua_forward(prob.handle, *args, fl, sinks, None, out) == 1
+    assert ua.ua_forward(prob.handle, *args, fl | ua.UA_FLAG_SINKS, None, None, out) == 1
+    # flags outside the problem's set
+    assert ua.ua_forward(prob.handle, *args, fl | ua.UA_FLAG_ALIBI, None, sinks, out) == 1
+    # too many sequences / rows
+    bad = list(args)
+    bad[6] = w.num_seqs + 100
+    assert ua.ua_forward(prob.handle, *bad, fl, None, None, out) == 1
+    # misaligned output
+    flat = torch.empty(out.numel() + 8, dtype=torch.bfloat16, device="cuda")
+    assert ua.ua_forward(prob.handle, *args, fl, None, None, flat[1:]) == 1
+    assert prob.check_device_error() == 0
+
+
+def test_device_reports_bad_block_id_and_short_context():
+    w = W.random_small(401, num_seqs=3, hq=8, hk=2, d=128, b=16, sq=(1, 1), ctx=(40, 60),
+                       poison=False)
+    ref = oracle.forward_workload(w)
+    # Sequence 1 gets an out-of-range block id; sequence 2 claims fewer keys than queries.
+    bad = w.to("cpu")
+    bad.block_table = w.block_table.clone()
+    bad.block_table[1, 0] = w.num_blocks + 5
+    wd = bad.to("cuda")
+    prob = ua.Problem.for_workload(wd)
+    out = prob.forward_workload(wd)
+    code = prob.check_device_error()
+    assert code & ua.UA_DEVERR_BLOCK_ID
+    got = out.float().cpu().numpy()
+    assert np.all(np.isfinite(got))
+    check_close(got[0], ref[0])          # well-formed sequence unaffected
+    check_close(got[2], ref[2])
+    assert prob.check_device_error() == 0  # cleared by the previous read
+
+    # Sequence 1 now claims fewer keys (0) than its query rows (1).
+    short = w.to("cpu")
+    short.block_table = w.block_table.clone()
+    short.seqused_k = w.seqused_k.clone()
+    short.seqused_k[1] = 0
+    wd = short.to("cuda")
+    out = prob.forward_workload(wd)
+    code = prob.check_device_error()
+    assert code & ua.UA_DEVERR_CONTEXT
+    got = out.float().cpu().numpy()
+    assert np.all(got[1] == 0)
+    check_close(got[0], ref[0])
+    check_close(got[2], ref[2])
+
+
+def test_host_buffer_entry_point_matches_device_entry_point():
+    w = W.make("decode", device="cuda")
+    prob = ua.Problem.for_workload(w)
+    dev = prob.forward_workload(w)
+    flags = ua.flags_of(w.causal, w.softcap, False, w.window, False)
+    q_h = w.q.cpu().pin_memory()
+    out_h = torch.empty_like(q_h).pin_memory()
+    st = ua.ua_forward_host(prob.handle, q_h, w.k_cache, w.v_cache, w.block_table.cpu(),
+                            w.cu_seqlens_q.cpu(), w.seqused_k.cpu(), w.num_seqs, w.total_q,
+                            w.max_seqlen_q, w.max_seqlen_k, flags, None, None, out_h)
+    assert st == 0
+    assert prob.check_device_error() == 0
+    assert torch.equal(out_h, dev.cpu())
