@@ -183,6 +183,42 @@ const char *ua_last_path(const ua_problem *p);
  */
 ua_status ua_set_profile_events(ua_problem *p, void *ev_begin, void *ev_end);
 
+/*
+ * ua_forward_noalloc -- the split-KV forward pass without any allocation.
+ * (An addition of this library; the paper has no counterpart.)
+ *
+ * For callers that cannot call cudaMalloc: code that lives inside a memory
+ * arena owning the whole device, code running inside stream capture where an
+ * allocation would break the capture, plugins that are handed only the
+ * tensors of the call, and latency paths that must not enter an allocator.
+ * Such callers cannot use ua_problem_create, which allocates the workspace.
+ *
+ * It takes the problem description by value-pointer (no ua_problem) plus the
+ * same inputs and output as ua_forward, and runs the same split kernel and
+ * combine kernel.  Their fp32 partials live in a 16 MiB array that the
+ * library declares statically in device memory: every GPU that loads
+ * libua.so holds those 16 MiB until the process exits.  Calls whose partials
+ * (total_q * H_q * (d + 2) * 4 bytes per segment) do not fit twice in that
+ * array return UA_ERR_UNSUPPORTED and launch nothing.
+ *
+ * device_error: optional caller-owned device int32 that receives the
+ * UA_DEVERR_* bits (OR-ed in; the caller clears it).  When NULL the bits go to
+ * a word inside the static array, cleared at the start of each call, and are
+ * not reported.
+ *
+ * The first call on a device resolves the array's address (once per device);
+ * make that first call before any stream capture.  All calls on a device share
+ * the array and leave their partials in it: calls whose kernels may overlap on
+ * the GPU race on it and must be ordered by the caller.
+ */
+ua_status ua_forward_noalloc(const ua_problem_desc *desc, const void *q, const void *k_cache,
+                             const void *v_cache, const int32_t *block_table,
+                             const int32_t *cu_seqlens_q, const int32_t *seqused_k,
+                             int32_t num_seqs, int64_t total_q, int32_t max_seqlen_q,
+                             int32_t max_seqlen_k, uint32_t flags, const float *sinks,
+                             const float *alibi_slopes, void *out, int32_t *device_error,
+                             void *stream);
+
 /* Free the workspace and the problem.  NULL is a no-op. */
 void ua_destroy(ua_problem *p);
 

@@ -12,5 +12,6 @@ from .binding import (  # noqa: F401
     UA_FLAG_ALIBI, UA_FLAG_CAUSAL, UA_FLAG_SINKS, UA_FLAG_SOFTCAP, UA_FLAG_WINDOW,
     UA_DEVERR_BLOCK_ID, UA_DEVERR_BOUNDS, UA_DEVERR_CONTEXT, UA_DEVERR_CU_SEQLENS,
     UA_DEVERR_TIMEOUT, UAError, Problem, flags_of, lib_path, load_library,
-    ua_check_device_error, ua_destroy, ua_forward, ua_forward_host, ua_problem_create,
+    ua_check_device_error, ua_destroy, ua_forward, ua_forward_host, ua_forward_noalloc,
+    ua_problem_create,
     ua_status_string)

@@ -169,6 +169,25 @@ def ua_forward_host(problem, q_host, k_cache, v_cache, block_table_host, cu_seql
         _stream(stream))
 
 
+def ua_forward_noalloc(desc, q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k,
+                       num_seqs, total_q, max_seqlen_q, max_seqlen_k, flags, sinks,
+                       alibi_slopes, out, device_error=None, stream=None):
+    """The allocation-free forward (``ProblemDesc`` instead of a problem
+    handle; partials in the library's static device scratch).  Returns the
+    status code without raising."""
+    lib = load_library()
+    fn = lib.ua_forward_noalloc
+    vp = ctypes.c_void_p
+    fn.argtypes = [ctypes.POINTER(ProblemDesc), vp, vp, vp, vp, vp, vp, ctypes.c_int32,
+                   ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_uint32, vp, vp,
+                   vp, vp, vp]
+    fn.restype = ctypes.c_int
+    return fn(ctypes.byref(desc), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+              _ptr(cu_seqlens_q), _ptr(seqused_k), num_seqs, total_q, max_seqlen_q,
+              max_seqlen_k, flags, _ptr(sinks), _ptr(alibi_slopes), _ptr(out),
+              _ptr(device_error), _stream(stream))
+
+
 def ua_check_device_error(problem, stream=None):
     """Synchronise the stream and return (and clear) the device error word."""
     code = ctypes.c_int32(0)
