@@ -267,7 +267,7 @@ ua_status ua_forward(ua_problem* p, const void* q, const void* k_cache, const vo
 
     // ---- path choice ------------------------------------------------------
     const int64_t rows_per_kv = (int64_t)g * max_seqlen_q;
-    const bool use_tc = ua::prefill_supported(d.head_size) && rows_per_kv > 16;
+    const bool use_tc = ua::prefill_shape_ok(fp) && rows_per_kv > 16;
     if (use_tc) {
         ua::PrefillPlan plan;
         ua::plan_prefill(fp, p->num_sms, &plan);

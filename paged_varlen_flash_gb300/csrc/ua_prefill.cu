@@ -1,15 +1,531 @@
-// ua_prefill.cu -- tensor-core prefill path (not built yet for any head size).
+// ua_prefill.cu -- prefill / chunked-prefill attention on the tcgen05 tensor
+// cores of sm_103a.
+//
+// Work unit: one CTA per (tile of 128 packed (position, head) rows of one KV
+// head, sequence).  The g query heads that share a KV head are packed into the
+// tile's rows, so one QK^T MMA serves the whole group (gfx950 "Unified paged
+// attention on gfx950, from the math up", section 4, GQA packing).  The CTA
+// walks its visible KV tiles with the streaming (m, l, o) recurrence of
+// gfx1151 ALGORITHM.md section 3, in base 2 (gfx950 section 2), with the lazy
+// re-anchor threshold of 8 and the loop split into mask-free and masked tiles
+// plus the causal early exit and the sliding-window start tile of
+// attention_dense.py (section 8.1 of the gfx950 page).
+//
+// Roles (6 warps):
+//   warps 0-3  softmax + epilogue: thread r owns row r of the tile, which is
+//              also tensor-memory lane r, so row max and row sum need no
+//              cross-thread reduction;
+//   warp 4     TMA producer: Q tile once (a 3-D box of g heads x 128/g
+//              positions), then K and V tiles through an NS-stage ring, one box
+//              per (paged block, 64-wide head-dim panel), block ids read from
+//              the block table;
+//   warp 5     tensor-memory allocator and MMA issuer: S = Q K^T into one of two
+//              tensor-memory S buffers, then O += P V with P (bf16) staged in
+//              shared memory and V read MN-major straight from its TMA tile.
+//
+// Tensor memory (512 columns): S0 [0, BN), S1 [BN, 2 BN), O [2 BN, 2 BN + D).
+#include <cstdint>
+#include <cstring>
+
+#include "ua_common.cuh"
 #include "ua_prefill.h"
+#include "ua_ptx.cuh"
+#include "ua_tc.cuh"
+#include "ua_tmap.h"
 
 namespace ua {
+namespace {
 
-bool prefill_supported(int) { return false; }
+constexpr float kLazy = 8.0f;
+constexpr int kRows = 128;
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;
 
-void plan_prefill(const FwdParams&, int, PrefillPlan* plan) { *plan = PrefillPlan(); }
+template <int D, int BN, int NS>
+struct PCfg {
+    static constexpr int kPanels = D / 64;
+    static constexpr int kQPanel = kRows * 128;
+    static constexpr int kQBytes = kPanels * kQPanel;
+    static constexpr int kKvPanel = BN * 128;
+    static constexpr int kKvBytes = kPanels * kKvPanel;
+    static constexpr int kPPanels = BN / 64;
+    static constexpr int kPBytes = kPPanels * kRows * 128;
+    static constexpr int kOffQ = 0;
+    static constexpr int kOffK = kOffQ + kQBytes;
+    static constexpr int kOffV = kOffK + NS * kKvBytes;
+    static constexpr int kOffP = kOffV + NS * kKvBytes;
+    static constexpr int kOffBar = kOffP + kPBytes;
+    // q_full, k_full[NS], v_full[NS], kv_empty[NS], s_full[2], p_full, o_done, drain
+    static constexpr int kNumBars = 1 + 3 * NS + 2 + 3;
+    static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+    static constexpr int kSmem = kOffMisc + 16 + 1024;
+    static constexpr int kTmemS = 0;
+    static constexpr int kTmemO = 2 * BN;
+    static_assert(2 * BN + D <= (int)kTmemCols, "tensor memory budget");
+    static_assert(kSmem <= 232448, "shared memory budget");
+};
 
-cudaError_t launch_prefill(const PrefillPlan&, const CUtensorMap&, const CUtensorMap&,
-                           const FwdParams&, cudaStream_t) {
-    return cudaErrorNotSupported;
+struct Bars {
+    uint32_t q_full, k_full0, v_full0, kv_empty0, s_full0, p_full, o_done, drain;
+};
+
+// Wait on an mbarrier phase; gives up (and raises the CTA's abort flag and the
+// device error bit) after about a second, or as soon as another role aborted.
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
+                                              volatile int* abort_flag, int32_t* err) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t start = global_ns();
+    for (;;) {
+        for (int i = 0; i < 128; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (global_ns() - start > kWaitLimitNs) {
+            *abort_flag = 1;
+            atomicOr(err, (int)UA_DEVERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ float tanh_via_exp2(float x) {
+    // tanh(x) = 1 - 2 / (e^{2x} + 1)
+    const float e = fast_exp2(x * (2.0f * kLog2e));
+    return 1.0f - __fdividef(2.0f, e + 1.0f);
+}
+
+template <int D, int BN, int NS>
+__global__ void __launch_bounds__(kThreads, 1)
+prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+               const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+    using C = PCfg<D, BN, NS>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int s = blockIdx.z;
+    const int hkv = blockIdx.y;
+    const int qt = gridDim.x - 1 - blockIdx.x;  // heaviest (latest) tiles first
+    const int g = p.g;
+    const int ppt = kRows / g;                  // positions per tile
+    const int p0 = qt * ppt;
+
+    int sq, sk;
+    int64_t q0;
+    const uint32_t st = seq_status(p, s, sq, sk, q0);
+    if (st && qt == 0 && hkv == 0 && threadIdx.x == 0) atomicOr(p.err, (int)st);
+    if (st & UA_DEVERR_CU_SEQLENS) return;
+    if (p0 >= sq) return;
+    const int p_last = min(p0 + ppt, sq) - 1;
+    if (st) {  // malformed lengths: the tile's rows are written as zeros
+        for (int e = threadIdx.x; e < kRows * (D / 8); e += kThreads) {
+            const int r = e / (D / 8), c = e % (D / 8);
+            const int i = p0 + r / g;
+            if (i > p_last) continue;
+            const int64_t row = (q0 + i) * p.hq + hkv * g + r % g;
+            *reinterpret_cast<uint4*>(p.out + row * D + c * 8) = make_uint4(0, 0, 0, 0);
+        }
+        return;
+    }
+    const int ctx = sk - sq;
+    const bool causal = (p.flags & UA_FLAG_CAUSAL) != 0;
+    const bool window = (p.flags & UA_FLAG_WINDOW) != 0;
+    const int k_end = causal ? min(sk, p_last + ctx + 1) : sk;
+    const int k_beg = window ? max(0, p0 + ctx - p.window + 1) : 0;
+    const int t_begin = k_beg / BN;
+    const int n_tiles = (k_end + BN - 1) / BN - t_begin;
+
+    uint64_t* bar_mem = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+    Bars B;
+    B.q_full = smem_u32(&bar_mem[0]);
+    B.k_full0 = smem_u32(&bar_mem[1]);
+    B.v_full0 = smem_u32(&bar_mem[1 + NS]);
+    B.kv_empty0 = smem_u32(&bar_mem[1 + 2 * NS]);
+    B.s_full0 = smem_u32(&bar_mem[1 + 3 * NS]);
+    B.p_full = smem_u32(&bar_mem[3 + 3 * NS]);
+    B.o_done = smem_u32(&bar_mem[4 + 3 * NS]);
+    B.drain = smem_u32(&bar_mem[5 + 3 * NS]);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
+
+    if (threadIdx.x == 0) {
+        mbar_init(B.q_full, 1);
+        for (int i = 0; i < NS; ++i) {
+            mbar_init(B.k_full0 + 8 * i, 1);
+            mbar_init(B.v_full0 + 8 * i, 1);
+            mbar_init(B.kv_empty0 + 8 * i, 1);
+        }
+        mbar_init(B.s_full0, 1);
+        mbar_init(B.s_full0 + 8, 1);
+        mbar_init(B.p_full, kRows);
+        mbar_init(B.o_done, 1);
+        mbar_init(B.drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 5) {
+        tc::tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    const uint32_t sQ = smem_u32(smem + C::kOffQ);
+    const uint32_t sK = smem_u32(smem + C::kOffK);
+    const uint32_t sV = smem_u32(smem + C::kOffV);
+    const uint32_t sP = smem_u32(smem + C::kOffP);
+
+    if (warp == 4) {
+        // ------------------------------ TMA producer ------------------------------
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_q);
+            tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_v);
+            mbar_arrive_expect_tx(B.q_full, C::kQBytes);
+#pragma unroll
+            for (int pn = 0; pn < C::kPanels; ++pn)
+                tma_load_3d(sQ + pn * C::kQPanel, &tm_q, pn * 64, hkv * g, (int)(q0 + p0), B.q_full);
+            const int b = p.b;
+            const int nblk_seq = (sk + b - 1) / b;
+            const int32_t* bt = p.block_table + (int64_t)s * p.bt_stride;
+            for (int j = 0; j < n_tiles; ++j) {
+                const int stg = j % NS;
+                if (j >= NS && !wait_or_abort(B.kv_empty0 + 8 * stg, ((j / NS) + 1) & 1, abort_flag,
+                                              p.err))
+                    break;
+                const int key0 = (t_begin + j) * BN;
+                const int blk0 = key0 / b;
+                const int nb = min(BN / b, nblk_seq - blk0);
+                const uint32_t bytes = (uint32_t)nb * b * 128 * C::kPanels;
+                const uint32_t kst = sK + stg * C::kKvBytes;
+                const uint32_t vst = sV + stg * C::kKvBytes;
+                mbar_arrive_expect_tx(B.k_full0 + 8 * stg, bytes);
+                for (int bi = 0; bi < nb; ++bi) {
+                    const int32_t id = __ldg(bt + blk0 + bi);
+                    if (id < 0 || (int64_t)id >= p.num_blocks) atomicOr(p.err, (int)UA_DEVERR_BLOCK_ID);
+#pragma unroll
+                    for (int pn = 0; pn < C::kPanels; ++pn)
+                        tma_load_4d(kst + pn * C::kKvPanel + bi * b * 128, &tm_k, pn * 64, hkv, 0, id,
+                                    B.k_full0 + 8 * stg);
+                }
+                mbar_arrive_expect_tx(B.v_full0 + 8 * stg, bytes);
+                for (int bi = 0; bi < nb; ++bi) {
+                    const int32_t id = __ldg(bt + blk0 + bi);
+#pragma unroll
+                    for (int pn = 0; pn < C::kPanels; ++pn)
+                        tma_load_4d(vst + pn * C::kKvPanel + bi * b * 128, &tm_v, pn * 64, hkv, 0, id,
+                                    B.v_full0 + 8 * stg);
+                }
+            }
+            if (*abort_flag) {
+                // Let every copy this thread issued land before the CTA ends.
+                for (int j = max(0, n_tiles - NS); j < n_tiles; ++j) {
+                    const int stg = j % NS;
+                    mbar_wait_bounded(B.k_full0 + 8 * stg, (j / NS) & 1);
+                    mbar_wait_bounded(B.v_full0 + 8 * stg, (j / NS) & 1);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 5) {
+        // ------------------------------ MMA issuer --------------------------------
+        constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(kRows, BN, false, false);
+        constexpr uint32_t idesc_pv = tc::idesc_bf16_f32(kRows, D, false, true);
+        auto wwait = [&](uint32_t bar, uint32_t par) {
+            return __all_sync(0xffffffffu, wait_or_abort(bar, par, abort_flag, p.err));
+        };
+        bool ok = wwait(B.q_full, 0);
+        auto issue_qk = [&](int j) {
+            const int stg = j % NS;
+            const uint32_t kst = sK + stg * C::kKvBytes;
+            const uint32_t dS = tmem + C::kTmemS + (j & 1) * BN;
+#pragma unroll
+            for (int k = 0; k < D / 16; ++k) {
+                const int pn = k >> 2, off = (k & 3) * 32;
+                const uint64_t a = tc::smem_desc_sw128(sQ + pn * C::kQPanel + off, 16, 1024);
+                const uint64_t bdesc = tc::smem_desc_sw128(kst + pn * C::kKvPanel + off, 16, 1024);
+                tc::mma_bf16(dS, a, bdesc, idesc_qk, k > 0 ? 1u : 0u);
+            }
+            tc::commit(B.s_full0 + 8 * (j & 1));
+        };
+        if (ok) ok = wwait(B.k_full0, 0);
+        if (ok) {
+            tc::fence_after_sync();
+            if (lane == 0) issue_qk(0);
+            __syncwarp();
+        }
+        for (int j = 0; ok && j < n_tiles; ++j) {
+            if (j + 1 < n_tiles) {
+                const int st1 = (j + 1) % NS;
+                if (!wwait(B.k_full0 + 8 * st1, ((j + 1) / NS) & 1)) break;
+                tc::fence_after_sync();
+                if (lane == 0) issue_qk(j + 1);
+                __syncwarp();
+            }
+            const int stg = j % NS;
+            if (!wwait(B.p_full, j & 1)) break;
+            if (!wwait(B.v_full0 + 8 * stg, (j / NS) & 1)) break;
+            tc::fence_after_sync();
+            const uint32_t vst = sV + stg * C::kKvBytes;
+            const int key0 = (t_begin + j) * BN;
+            const int nvalid = min(BN, sk - key0);
+            if (nvalid < BN) {
+                // Keys past S_k: whatever those slots hold must not reach O
+                // (0 * NaN is NaN), so their V rows become zeros.
+                uint8_t* vgen = smem + C::kOffV + stg * C::kKvBytes;
+                const int nbytes_row = 128;
+                for (int e = lane; e < (BN - nvalid) * C::kPanels * (nbytes_row / 16); e += 32) {
+                    const int per_panel = (BN - nvalid) * (nbytes_row / 16);
+                    const int pn = e / per_panel;
+                    const int rem = e % per_panel;
+                    const int row = nvalid + rem / (nbytes_row / 16);
+                    const int ch = rem % (nbytes_row / 16);
+                    *reinterpret_cast<uint4*>(vgen + pn * C::kKvPanel + row * 128 + ch * 16) =
+                        make_uint4(0, 0, 0, 0);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+            }
+            if (lane == 0) {
+                const uint32_t dO = tmem + C::kTmemO;
+#pragma unroll
+                for (int k = 0; k < BN / 16; ++k) {
+                    const int pn = k >> 2, off = (k & 3) * 32;
+                    const uint64_t a = tc::smem_desc_sw128(sP + pn * (kRows * 128) + off, 16, 1024);
+                    const uint64_t bdesc = tc::smem_desc_sw128(vst + k * 16 * 128, C::kKvPanel, 1024);
+                    tc::mma_bf16(dO, a, bdesc, idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
+                }
+                tc::commit(B.o_done);
+                tc::commit(B.kv_empty0 + 8 * stg);
+            }
+            __syncwarp();
+        }
+        if (*abort_flag) {
+            // Make sure no MMA of this CTA is still running before the tensor
+            // memory is released.
+            if (lane == 0) tc::commit(B.drain);
+            __syncwarp();
+            mbar_wait_bounded(B.drain, 0);
+        }
+    } else {
+        // ------------------------- softmax + epilogue warps -----------------------
+        const int r = threadIdx.x;  // tile row == tensor-memory lane
+        const int i = p0 + r / g;
+        const int head = hkv * g + r % g;
+        const bool row_valid = i <= p_last;
+        const int hi = causal ? min(i + ctx, sk - 1) : sk - 1;
+        const int lo = window ? max(0, i + ctx - p.window + 1) : 0;
+        const bool softcap = (p.flags & UA_FLAG_SOFTCAP) != 0;
+        const bool alibi = (p.flags & UA_FLAG_ALIBI) != 0;
+        const float sl2 = p.scale * kLog2e;
+        const float slope = alibi ? __ldg(p.alibi + head) : 0.f;
+        const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+        // Keys every row of the tile sees: [kfree_lo, kfree_hi].
+        const int kfree_hi = causal ? min(p0 + ctx, sk - 1) : sk - 1;
+        const int kfree_lo = window ? max(0, p_last + ctx - p.window + 1) : 0;
+
+        float m = -INFINITY;  // running max, log2 units
+        float l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < n_tiles; ++j) {
+            if (!__all_sync(0xffffffffu, wait_or_abort(B.s_full0 + 8 * (j & 1), (j >> 1) & 1,
+                                                       abort_flag, p.err))) {
+                ok = false;
+                break;
+            }
+            tc::fence_after_sync();
+            // Scores of this row for the tile's BN keys (fp32 bits).
+            uint32_t sr[BN / 32][32];
+#pragma unroll
+            for (int c = 0; c < BN / 32; ++c) tc::ld32(trow + C::kTmemS + (j & 1) * BN + c * 32, sr[c]);
+            tc::wait_ld();
+            const int key0 = (t_begin + j) * BN;
+            const bool mask_free = key0 >= kfree_lo && key0 + BN - 1 <= kfree_hi;
+            const bool plain = !softcap && !alibi;
+            // x: plain -> raw score (scaled later inside the exponent's FMA);
+            //    otherwise -> the transformed logit in log2 units.
+            if (!plain) {
+#pragma unroll
+                for (int c = 0; c < BN / 32; ++c)
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        float t = __uint_as_float(sr[c][e]) * p.scale;
+                        if (softcap) t = p.softcap * tanh_via_exp2(t / p.softcap);
+                        if (alibi) t += slope * (float)(key0 + c * 32 + e - ctx);
+                        sr[c][e] = __float_as_uint(t * kLog2e);
+                    }
+            }
+            if (!mask_free) {
+#pragma unroll
+                for (int c = 0; c < BN / 32; ++c)
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const int kj = key0 + c * 32 + e;
+                        if (kj < lo || kj > hi) sr[c][e] = __float_as_uint(-INFINITY);
+                    }
+            }
+            float tmax = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < BN / 32; ++c)
+#pragma unroll
+                for (int e = 0; e < 32; ++e) tmax = fmaxf(tmax, __uint_as_float(sr[c][e]));
+            if (plain) tmax *= sl2;
+            // Lazy re-anchor: move the reference max only when the tile's max
+            // exceeds it by more than 8 (log2), so P stays at most 2^8.
+            float alpha = 1.f;
+            const bool reanchor = tmax > m + kLazy;
+            if (reanchor) {
+                alpha = fast_exp2(m - tmax);
+                m = tmax;
+            }
+            const float m_use = (m == -INFINITY) ? 0.f : m;
+            const float xs = plain ? sl2 : 1.0f;
+            // The previous P.V must be finished before P is overwritten and
+            // before O is rescaled.
+            if (j > 0) {
+                if (!__all_sync(0xffffffffu,
+                                wait_or_abort(B.o_done, (j - 1) & 1, abort_flag, p.err))) {
+                    ok = false;
+                    break;
+                }
+                tc::fence_after_sync();
+                if (__any_sync(0xffffffffu, reanchor)) {
+#pragma unroll 1
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t o[32];
+                        tc::ld32(trow + C::kTmemO + c * 32, o);
+                        tc::wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                        tc::st32(trow + C::kTmemO + c * 32, o);
+                    }
+                    tc::wait_st();
+                }
+            }
+            // P = 2^(x - m) -> bf16 -> shared memory (128-byte swizzled K-major
+            // panels of 64 keys), chunk by chunk.
+            float rsum = 0.f;
+            uint8_t* prow = smem + C::kOffP + r * 128;
+#pragma unroll
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    const float a0 = fast_exp2(fmaf(__uint_as_float(sr[c][e]), xs, -m_use));
+                    const float a1 = fast_exp2(fmaf(__uint_as_float(sr[c][e + 1]), xs, -m_use));
+                    rsum += a0 + a1;
+                    pk[e / 2] = pack_bf16x2(a0, a1);
+                }
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    const int chunk = c * 4 + q4;  // 8-key chunk index within the row
+                    const int pn = chunk >> 3, cc = chunk & 7;
+                    *reinterpret_cast<uint4*>(prow + pn * (kRows * 128) + ((cc ^ (r & 7)) << 4)) =
+                        make_uint4(pk[q4 * 4 + 0], pk[q4 * 4 + 1], pk[q4 * 4 + 2], pk[q4 * 4 + 3]);
+                }
+            }
+            l = l * alpha + rsum;
+            fence_proxy_async_smem();
+            tc::fence_before_sync();
+            mbar_arrive(B.p_full);
+        }
+        // ------------------------------ epilogue ---------------------------------
+        if (ok && __all_sync(0xffffffffu,
+                             wait_or_abort(B.o_done, (n_tiles - 1) & 1, abort_flag, p.err))) {
+            tc::fence_after_sync();
+            float O_scale_num = 1.f;  // extra factor from the sink re-basing
+            float L = l;
+            bool zero = false;
+            if (p.flags & UA_FLAG_SINKS) {
+                const float s2 = __ldg(p.sinks + head) * kLog2e;
+                if (s2 == INFINITY) {
+                    zero = true;
+                } else if (s2 > m) {
+                    const float a = (m == -INFINITY) ? 0.f : fast_exp2(m - s2);
+                    O_scale_num = a;
+                    L = L * a + 1.0f;
+                } else if (s2 != -INFINITY) {
+                    L += fast_exp2(s2 - m);
+                }
+            }
+            const float inv = (!zero && L > 0.f) ? O_scale_num * __frcp_rn(L) : 0.f;
+            __nv_bfloat16* orow = p.out + ((q0 + i) * p.hq + head) * (int64_t)D;
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t o[32];
+                tc::ld32(trow + C::kTmemO + c * 32, o);
+                tc::wait_ld();
+                if (row_valid) {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 8) {
+                        uint4 v;
+                        v.x = pack_bf16x2(__uint_as_float(o[e + 0]) * inv, __uint_as_float(o[e + 1]) * inv);
+                        v.y = pack_bf16x2(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
+                        v.z = pack_bf16x2(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv);
+                        v.w = pack_bf16x2(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv);
+                        *reinterpret_cast<uint4*>(orow + c * 32 + e) = v;
+                    }
+                }
+            }
+        }
+    }
+
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 5) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+template <int D, int BN, int NS>
+cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                     const FwdParams& p, int tiles, cudaStream_t stream) {
+    using C = PCfg<D, BN, NS>;
+    auto kern = prefill_kernel<D, BN, NS>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    if (e != cudaSuccess) return e;
+    dim3 grid((unsigned)tiles, (unsigned)p.hk, (unsigned)p.num_seqs);
+    kern<<<grid, kThreads, C::kSmem, stream>>>(tq, tk, tv, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool prefill_supported(int d) { return d == 64 || d == 128 || d == 256; }
+
+void plan_prefill(const FwdParams& p, int num_sms, PrefillPlan* plan) {
+    (void)num_sms;
+    *plan = PrefillPlan();
+    plan->kv_box_rows = p.b;
+    const int ppt = kRows / p.g;
+    plan->num_tiles = (p.max_seqlen_q + ppt - 1) / ppt;
+    plan->grid = plan->num_tiles * p.hk * p.num_seqs;
+    plan->launches = 1;
+}
+
+bool prefill_shape_ok(const FwdParams& p) {
+    return prefill_supported(p.d) && p.g >= 1 && p.g <= kRows && (kRows % p.g) == 0;
+}
+
+cudaError_t launch_prefill(const PrefillPlan& plan, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                           const FwdParams& p, cudaStream_t stream) {
+    // Q map: [total_q, H_q, d] innermost first; box = one 64-wide panel x g heads
+    // x 128/g positions, i.e. exactly the tile's 128 packed rows.
+    CUtensorMap tq;
+    cuuint64_t dims[3] = {(cuuint64_t)p.d, (cuuint64_t)p.hq, (cuuint64_t)p.total_q};
+    cuuint64_t strides[2] = {2ull * p.d, 2ull * p.d * p.hq};
+    cuuint32_t box[3] = {64, (cuuint32_t)p.g, (cuuint32_t)(kRows / p.g)};
+    if (!encode_bf16_sw128(&tq, p.q, 3, dims, strides, box)) return cudaErrorInvalidValue;
+    if (plan.num_tiles <= 0) return cudaSuccess;
+    switch (p.d) {
+        case 64: return launch_t<64, 128, 4>(tq, tm_k, tm_v, p, plan.num_tiles, stream);
+        case 128: return launch_t<128, 128, 2>(tq, tm_k, tm_v, p, plan.num_tiles, stream);
+        case 256: return launch_t<256, 64, 2>(tq, tm_k, tm_v, p, plan.num_tiles, stream);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace ua

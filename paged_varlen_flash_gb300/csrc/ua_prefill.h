@@ -15,6 +15,10 @@ struct PrefillPlan {
 // True when the tensor-core path is built for head size d.
 bool prefill_supported(int d);
 
+// True when the call's shape fits the tensor-core tile (128 packed rows hold
+// whole GQA groups: g divides 128).
+bool prefill_shape_ok(const FwdParams& p);
+
 // Fill *plan for the call described by p.
 void plan_prefill(const FwdParams& p, int num_sms, PrefillPlan* plan);
 
