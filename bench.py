@@ -370,6 +370,36 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def run_single(args):
+    """One named workload, timed alone (device-resident inputs, L2 flushed
+    between steps); prints bytes/s and FLOP/s of the whole step and of the
+    dominant kernel."""
+    import torch
+    import paged_varlen_flash_gb300 as ua
+    from paged_varlen_flash_gb300 import build as ua_build
+    from paged_varlen_flash_gb300 import workloads as W
+    torch.cuda.set_device(0)
+    ua_build.build()
+    ua.load_library()
+    peaks, peak_src = load_peaks()
+    w = W.make(args.workload, device="cuda")
+    nbytes, flops = workload_units(w)
+    r = time_ours(w, args.steps, args.warmup, flush=True, torch=torch, ua=ua)
+    ms = statistics.mean(r["step_ms"])
+    km = statistics.mean(r["kernel_ms"])
+    print(json.dumps({
+        "workload": args.workload, "path": r["path"], "steps": args.steps,
+        "ms_per_step": round(ms, 5), "kernel_ms": round(km, 5),
+        "gbs": round(nbytes / (ms * 1e-3) / 1e9, 2),
+        "kernel_gbs": round(nbytes / (km * 1e-3) / 1e9, 2),
+        "tflops": round(flops / (ms * 1e-3) / 1e12, 2),
+        "kernel_tflops": round(flops / (km * 1e-3) / 1e12, 2),
+        "frac_hbm": round(nbytes / (km * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+        "frac_bf16": round(flops / (km * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
+        "peak_source": peak_src, "launches": r["launches"], "device_error": r["device_error"],
+        "bytes": nbytes, "flops": flops}), flush=True)
+
+
 def run_reference(args):
     """The fp64 CPU oracle as the reference arm, on the same workload/metric."""
     rank, world, _ = dist_info()
@@ -422,12 +452,19 @@ def main():
     ap.add_argument("--headline-only", action="store_true",
                     help="skip the prefill / chunked workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default=None,
+                    choices=["tiny", "decode", "chunked", "long_prefill", "long_prefill_shuffled",
+                             "wide_mha_alibi"],
+                    help="time only this workload and print its own short JSON line "
+                         "(for profiling); the default is the full headline run")
     args = ap.parse_args()
     if args.warmup < 3:
         log("warmup raised to 3")
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload:
+        run_single(args)
     else:
         run_ours(args)
 

@@ -49,14 +49,16 @@ struct PCfg {
     static constexpr int kKvPanel = BN * 128;
     static constexpr int kKvBytes = kPanels * kKvPanel;
     static constexpr int kPPanels = BN / 64;
-    static constexpr int kPBytes = kPPanels * kRows * 128;
+    static constexpr int kPBuf = kPPanels * kRows * 128;   // one P buffer
+    static constexpr int kPBytes = 2 * kPBuf;                 // double-buffered
     static constexpr int kOffQ = 0;
     static constexpr int kOffK = kOffQ + kQBytes;
     static constexpr int kOffV = kOffK + NS * kKvBytes;
     static constexpr int kOffP = kOffV + NS * kKvBytes;
     static constexpr int kOffBar = kOffP + kPBytes;
-    // q_full, k_full[NS], v_full[NS], kv_empty[NS], s_full[2], p_full, o_done, drain
-    static constexpr int kNumBars = 1 + 3 * NS + 2 + 3;
+    // q_full, k_full[NS], v_full[NS], k_empty[NS], v_empty[NS], s_full[2], p_full[2],
+    // o_done[2], drain
+    static constexpr int kNumBars = 1 + 4 * NS + 2 + 2 + 2 + 1;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kSmem = kOffMisc + 16 + 1024;
     static constexpr int kTmemS = 0;
@@ -66,7 +68,7 @@ struct PCfg {
 };
 
 struct Bars {
-    uint32_t q_full, k_full0, v_full0, kv_empty0, s_full0, p_full, o_done, drain;
+    uint32_t q_full, k_full0, v_full0, k_empty0, v_empty0, s_full0, p_full, o_done, drain;
 };
 
 // Wait on an mbarrier phase; gives up (and raises the CTA's abort flag and the
@@ -87,13 +89,49 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
     }
 }
 
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;"
+        : "=l"(d)
+        : "l"(*reinterpret_cast<uint64_t*>(&a)), "l"(*reinterpret_cast<uint64_t*>(&b)),
+          "l"(*reinterpret_cast<uint64_t*>(&c)));
+    return *reinterpret_cast<float2*>(&d);
+}
+
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;"
+        : "=l"(d)
+        : "l"(*reinterpret_cast<uint64_t*>(&a)), "l"(*reinterpret_cast<uint64_t*>(&b)));
+    return *reinterpret_cast<float2*>(&d);
+}
+
+// 2^a for a pair: the argument rounded to fp16, the hardware fp16x2 base-2
+// exponential, and the two results widened back to fp32.  -inf maps to 0.
+__device__ __forceinline__ float2 exp2_pair_f16(float2 a) {
+    uint32_t h, e;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(a.y), "f"(a.x));
+    asm("ex2.approx.f16x2 %0, %1;" : "=r"(e) : "r"(h));
+    float lo, hi;
+    asm("{\n\t.reg .f16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+        : "=f"(lo), "=f"(hi)
+        : "r"(e));
+    return make_float2(lo, hi);
+}
+
 __device__ __forceinline__ float tanh_via_exp2(float x) {
     // tanh(x) = 1 - 2 / (e^{2x} + 1)
     const float e = fast_exp2(x * (2.0f * kLog2e));
     return 1.0f - __fdividef(2.0f, e + 1.0f);
 }
 
-template <int D, int BN, int NS>
+template <int D, int BN, int NS, bool PLAIN>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
@@ -140,11 +178,17 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     B.q_full = smem_u32(&bar_mem[0]);
     B.k_full0 = smem_u32(&bar_mem[1]);
     B.v_full0 = smem_u32(&bar_mem[1 + NS]);
-    B.kv_empty0 = smem_u32(&bar_mem[1 + 2 * NS]);
-    B.s_full0 = smem_u32(&bar_mem[1 + 3 * NS]);
-    B.p_full = smem_u32(&bar_mem[3 + 3 * NS]);
-    B.o_done = smem_u32(&bar_mem[4 + 3 * NS]);
-    B.drain = smem_u32(&bar_mem[5 + 3 * NS]);
+    // A K stage is free once its QK^T has run, a V stage once its P.V has run,
+    // so the next K tile can be requested a whole softmax earlier than V.
+    B.k_empty0 = smem_u32(&bar_mem[1 + 2 * NS]);
+    B.v_empty0 = smem_u32(&bar_mem[1 + 3 * NS]);
+    B.s_full0 = smem_u32(&bar_mem[1 + 4 * NS]);
+    // Per-parity barriers: softmax warps may run one tile ahead of the MMA
+    // warp, so P-ready and PV-done are tracked separately for even and odd
+    // tiles (a single barrier could see arrivals of two tiles in one phase).
+    B.p_full = smem_u32(&bar_mem[3 + 4 * NS]);
+    B.o_done = smem_u32(&bar_mem[5 + 4 * NS]);
+    B.drain = smem_u32(&bar_mem[7 + 4 * NS]);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
 
@@ -153,12 +197,15 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         for (int i = 0; i < NS; ++i) {
             mbar_init(B.k_full0 + 8 * i, 1);
             mbar_init(B.v_full0 + 8 * i, 1);
-            mbar_init(B.kv_empty0 + 8 * i, 1);
+            mbar_init(B.k_empty0 + 8 * i, 1);
+            mbar_init(B.v_empty0 + 8 * i, 1);
         }
         mbar_init(B.s_full0, 1);
         mbar_init(B.s_full0 + 8, 1);
         mbar_init(B.p_full, kRows);
+        mbar_init(B.p_full + 8, kRows);
         mbar_init(B.o_done, 1);
+        mbar_init(B.o_done + 8, 1);
         mbar_init(B.drain, 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -192,7 +239,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             const int32_t* bt = p.block_table + (int64_t)s * p.bt_stride;
             for (int j = 0; j < n_tiles; ++j) {
                 const int stg = j % NS;
-                if (j >= NS && !wait_or_abort(B.kv_empty0 + 8 * stg, ((j / NS) + 1) & 1, abort_flag,
+                if (j >= NS && !wait_or_abort(B.k_empty0 + 8 * stg, ((j / NS) + 1) & 1, abort_flag,
                                               p.err))
                     break;
                 const int key0 = (t_begin + j) * BN;
@@ -210,6 +257,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                         tma_load_4d(kst + pn * C::kKvPanel + bi * b * 128, &tm_k, pn * 64, hkv, 0, id,
                                     B.k_full0 + 8 * stg);
                 }
+                if (j >= NS && !wait_or_abort(B.v_empty0 + 8 * stg, ((j / NS) + 1) & 1, abort_flag,
+                                              p.err))
+                    break;
                 mbar_arrive_expect_tx(B.v_full0 + 8 * stg, bytes);
                 for (int bi = 0; bi < nb; ++bi) {
                     const int32_t id = __ldg(bt + blk0 + bi);
@@ -249,6 +299,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 tc::mma_bf16(dS, a, bdesc, idesc_qk, k > 0 ? 1u : 0u);
             }
             tc::commit(B.s_full0 + 8 * (j & 1));
+            tc::commit(B.k_empty0 + 8 * stg);
         };
         if (ok) ok = wwait(B.k_full0, 0);
         if (ok) {
@@ -265,7 +316,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 __syncwarp();
             }
             const int stg = j % NS;
-            if (!wwait(B.p_full, j & 1)) break;
+            if (!wwait(B.p_full + 8 * (j & 1), (j >> 1) & 1)) break;
             if (!wwait(B.v_full0 + 8 * stg, (j / NS) & 1)) break;
             tc::fence_after_sync();
             const uint32_t vst = sV + stg * C::kKvBytes;
@@ -293,12 +344,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 #pragma unroll
                 for (int k = 0; k < BN / 16; ++k) {
                     const int pn = k >> 2, off = (k & 3) * 32;
-                    const uint64_t a = tc::smem_desc_sw128(sP + pn * (kRows * 128) + off, 16, 1024);
+                    const uint64_t a = tc::smem_desc_sw128(sP + (j & 1) * C::kPBuf + pn * (kRows * 128) + off,
+                                                           16, 1024);
                     const uint64_t bdesc = tc::smem_desc_sw128(vst + k * 16 * 128, C::kKvPanel, 1024);
                     tc::mma_bf16(dO, a, bdesc, idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
                 }
-                tc::commit(B.o_done);
-                tc::commit(B.kv_empty0 + 8 * stg);
+                tc::commit(B.o_done + 8 * (j & 1));
+                tc::commit(B.v_empty0 + 8 * stg);
             }
             __syncwarp();
         }
@@ -343,10 +395,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             tc::wait_ld();
             const int key0 = (t_begin + j) * BN;
             const bool mask_free = key0 >= kfree_lo && key0 + BN - 1 <= kfree_hi;
-            const bool plain = !softcap && !alibi;
-            // x: plain -> raw score (scaled later inside the exponent's FMA);
+            // x: PLAIN -> raw score (scaled inside the exponent's FMA);
             //    otherwise -> the transformed logit in log2 units.
-            if (!plain) {
+            if constexpr (!PLAIN) {
 #pragma unroll
                 for (int c = 0; c < BN / 32; ++c)
 #pragma unroll
@@ -366,12 +417,21 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                         if (kj < lo || kj > hi) sr[c][e] = __float_as_uint(-INFINITY);
                     }
             }
-            float tmax = -INFINITY;
+            // Row max: eight independent three-input max chains, then combined.
+            float mx[8];
+#pragma unroll
+            for (int a = 0; a < 8; ++a) mx[a] = -INFINITY;
 #pragma unroll
             for (int c = 0; c < BN / 32; ++c)
 #pragma unroll
-                for (int e = 0; e < 32; ++e) tmax = fmaxf(tmax, __uint_as_float(sr[c][e]));
-            if (plain) tmax *= sl2;
+                for (int e = 0; e < 32; e += 16)
+#pragma unroll
+                    for (int a = 0; a < 8; ++a)
+                        mx[a] = fmax3(mx[a], __uint_as_float(sr[c][e + 2 * a]),
+                                      __uint_as_float(sr[c][e + 2 * a + 1]));
+            float tmax = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
+                               fmaxf(mx[6], mx[7]));
+            if constexpr (PLAIN) tmax *= sl2;
             // Lazy re-anchor: move the reference max only when the tile's max
             // exceeds it by more than 8 (log2), so P stays at most 2^8.
             float alpha = 1.f;
@@ -381,42 +441,54 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 m = tmax;
             }
             const float m_use = (m == -INFINITY) ? 0.f : m;
-            const float xs = plain ? sl2 : 1.0f;
-            // The previous P.V must be finished before P is overwritten and
-            // before O is rescaled.
-            if (j > 0) {
-                if (!__all_sync(0xffffffffu,
-                                wait_or_abort(B.o_done, (j - 1) & 1, abort_flag, p.err))) {
+            const float xs = PLAIN ? sl2 : 1.0f;
+            // P buffer (j & 1) was last read by the P.V of tile j - 2.
+            if (j >= 2) {
+                if (!__all_sync(0xffffffffu, wait_or_abort(B.o_done + 8 * (j & 1), ((j - 2) >> 1) & 1,
+                                                           abort_flag, p.err))) {
+                    ok = false;
+                    break;
+                }
+            }
+            // Rescaling O needs the P.V of tile j - 1 to have finished.
+            if (j > 0 && __any_sync(0xffffffffu, reanchor)) {
+                if (!__all_sync(0xffffffffu, wait_or_abort(B.o_done + 8 * ((j - 1) & 1),
+                                                           ((j - 1) >> 1) & 1, abort_flag, p.err))) {
                     ok = false;
                     break;
                 }
                 tc::fence_after_sync();
-                if (__any_sync(0xffffffffu, reanchor)) {
 #pragma unroll 1
-                    for (int c = 0; c < D / 32; ++c) {
-                        uint32_t o[32];
-                        tc::ld32(trow + C::kTmemO + c * 32, o);
-                        tc::wait_ld();
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    tc::ld32(trow + C::kTmemO + c * 32, o);
+                    tc::wait_ld();
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                        tc::st32(trow + C::kTmemO + c * 32, o);
-                    }
-                    tc::wait_st();
+                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                    tc::st32(trow + C::kTmemO + c * 32, o);
                 }
+                tc::wait_st();
             }
-            // P = 2^(x - m) -> bf16 -> shared memory (128-byte swizzled K-major
-            // panels of 64 keys), chunk by chunk.
-            float rsum = 0.f;
-            uint8_t* prow = smem + C::kOffP + r * 128;
+            // P = 2^(x - m): the exponent argument in fp32 (packed pairs), the
+            // power of two on the fp16x2 special-function path (two results per
+            // instruction; fp16's 11-bit significand is finer than the bf16 P
+            // the MMA consumes), then bf16 into shared memory (128-byte
+            // swizzled K-major panels of 64 keys).  Row sums stay fp32.
+            float2 rs[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                            make_float2(0.f, 0.f)};
+            const float2 sc2 = make_float2(xs, xs);
+            const float2 nm2 = make_float2(-m_use, -m_use);
+            uint8_t* prow = smem + C::kOffP + (j & 1) * C::kPBuf + r * 128;
 #pragma unroll
             for (int c = 0; c < BN / 32; ++c) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int e = 0; e < 32; e += 2) {
-                    const float a0 = fast_exp2(fmaf(__uint_as_float(sr[c][e]), xs, -m_use));
-                    const float a1 = fast_exp2(fmaf(__uint_as_float(sr[c][e + 1]), xs, -m_use));
-                    rsum += a0 + a1;
-                    pk[e / 2] = pack_bf16x2(a0, a1);
+                    const float2 a = ffma2(make_float2(__uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1])),
+                                           sc2, nm2);
+                    const float2 pr = exp2_pair_f16(a);
+                    rs[(e >> 1) & 3] = fadd2(rs[(e >> 1) & 3], pr);
+                    pk[e / 2] = pack_bf16x2(pr.x, pr.y);
                 }
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4) {
@@ -426,14 +498,16 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                         make_uint4(pk[q4 * 4 + 0], pk[q4 * 4 + 1], pk[q4 * 4 + 2], pk[q4 * 4 + 3]);
                 }
             }
+            const float2 rs01 = fadd2(rs[0], rs[1]), rs23 = fadd2(rs[2], rs[3]);
+            const float rsum = (rs01.x + rs01.y) + (rs23.x + rs23.y);
             l = l * alpha + rsum;
             fence_proxy_async_smem();
             tc::fence_before_sync();
-            mbar_arrive(B.p_full);
+            mbar_arrive(B.p_full + 8 * (j & 1));
         }
         // ------------------------------ epilogue ---------------------------------
-        if (ok && __all_sync(0xffffffffu,
-                             wait_or_abort(B.o_done, (n_tiles - 1) & 1, abort_flag, p.err))) {
+        if (ok && __all_sync(0xffffffffu, wait_or_abort(B.o_done + 8 * ((n_tiles - 1) & 1),
+                                                        ((n_tiles - 1) >> 1) & 1, abort_flag, p.err))) {
             tc::fence_after_sync();
             float O_scale_num = 1.f;  // extra factor from the sink re-basing
             float L = l;
@@ -484,7 +558,8 @@ template <int D, int BN, int NS>
 cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                      const FwdParams& p, int tiles, cudaStream_t stream) {
     using C = PCfg<D, BN, NS>;
-    auto kern = prefill_kernel<D, BN, NS>;
+    const bool plain = (p.flags & (UA_FLAG_SOFTCAP | UA_FLAG_ALIBI)) == 0;
+    auto kern = plain ? prefill_kernel<D, BN, NS, true> : prefill_kernel<D, BN, NS, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)tiles, (unsigned)p.hk, (unsigned)p.num_seqs);
