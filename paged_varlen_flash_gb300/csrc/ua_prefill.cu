@@ -38,7 +38,10 @@ namespace {
 
 constexpr float kLazy = 8.0f;
 constexpr int kRows = 128;
-constexpr int kThreads = 192;
+constexpr int kSmThreads = 256;             // two softmax warpgroups: column halves of each row
+constexpr int kThreads = kSmThreads + 64;   // + TMA producer warp + MMA warp
+constexpr int kWarpTma = 8;
+constexpr int kWarpMma = 9;
 constexpr uint32_t kTmemCols = 512;
 
 template <int D, int BN, int NS>
@@ -49,8 +52,7 @@ struct PCfg {
     static constexpr int kKvPanel = BN * 128;
     static constexpr int kKvBytes = kPanels * kKvPanel;
     static constexpr int kPPanels = BN / 64;
-    static constexpr int kPBuf = kPPanels * kRows * 128;   // one P buffer
-    static constexpr int kPBytes = 2 * kPBuf;                 // double-buffered
+    static constexpr int kPBytes = kPPanels * kRows * 128;
     static constexpr int kOffQ = 0;
     static constexpr int kOffK = kOffQ + kQBytes;
     static constexpr int kOffV = kOffK + NS * kKvBytes;
@@ -59,7 +61,8 @@ struct PCfg {
     // q_full, k_full[NS], v_full[NS], k_empty[NS], v_empty[NS], s_full[2], p_full[2],
     // o_done[2], drain
     static constexpr int kNumBars = 1 + 4 * NS + 2 + 2 + 2 + 1;
-    static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+    static constexpr int kOffRed = kOffBar + kNumBars * 8;      // [2 parity][2 half][128] fp32
+    static constexpr int kOffMisc = kOffRed + 2 * 2 * kRows * 4;
     static constexpr int kSmem = kOffMisc + 16 + 1024;
     static constexpr int kTmemS = 0;
     static constexpr int kTmemO = 2 * BN;
@@ -123,6 +126,21 @@ __device__ __forceinline__ float2 exp2_pair_f16(float2 a) {
         : "=f"(lo), "=f"(hi)
         : "r"(e));
     return make_float2(lo, hi);
+}
+
+// Named barrier over `count` threads that also returns the AND of `pred`
+// across them.
+__device__ __forceinline__ bool bar_and_sync(int id, int count, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "barrier.cta.red.and.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
 }
 
 __device__ __forceinline__ float tanh_via_exp2(float x) {
@@ -202,15 +220,15 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         }
         mbar_init(B.s_full0, 1);
         mbar_init(B.s_full0 + 8, 1);
-        mbar_init(B.p_full, kRows);
-        mbar_init(B.p_full + 8, kRows);
+        mbar_init(B.p_full, kSmThreads);
+        mbar_init(B.p_full + 8, kSmThreads);
         mbar_init(B.o_done, 1);
         mbar_init(B.o_done + 8, 1);
         mbar_init(B.drain, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 5) {
+    if (warp == kWarpMma) {
         tc::tmem_alloc(smem_u32(tmem_slot), kTmemCols);
         tc::tmem_relinquish();
     }
@@ -224,7 +242,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     const uint32_t sV = smem_u32(smem + C::kOffV);
     const uint32_t sP = smem_u32(smem + C::kOffP);
 
-    if (warp == 4) {
+    if (warp == kWarpTma) {
         // ------------------------------ TMA producer ------------------------------
         if (lane == 0) {
             tma_prefetch_desc(&tm_q);
@@ -279,7 +297,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             }
         }
         __syncwarp();
-    } else if (warp == 5) {
+    } else if (warp == kWarpMma) {
         // ------------------------------ MMA issuer --------------------------------
         constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(kRows, BN, false, false);
         constexpr uint32_t idesc_pv = tc::idesc_bf16_f32(kRows, D, false, true);
@@ -344,8 +362,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 #pragma unroll
                 for (int k = 0; k < BN / 16; ++k) {
                     const int pn = k >> 2, off = (k & 3) * 32;
-                    const uint64_t a = tc::smem_desc_sw128(sP + (j & 1) * C::kPBuf + pn * (kRows * 128) + off,
-                                                           16, 1024);
+                    const uint64_t a = tc::smem_desc_sw128(sP + pn * (kRows * 128) + off, 16, 1024);
                     const uint64_t bdesc = tc::smem_desc_sw128(vst + k * 16 * 128, C::kKvPanel, 1024);
                     tc::mma_bf16(dO, a, bdesc, idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
                 }
@@ -363,7 +380,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         }
     } else {
         // ------------------------- softmax + epilogue warps -----------------------
-        const int r = threadIdx.x;  // tile row == tensor-memory lane
+        // Thread (half, r): row r of the tile (tensor-memory lane r) and the
+        // half of its BN key columns [half * CPT, half * CPT + CPT).  The two
+        // halves agree on the row max through shared memory once per tile.
+        constexpr int CPT = BN / 2;
+        const int r = threadIdx.x & (kRows - 1);
+        const int half = threadIdx.x >> 7;
         const int i = p0 + r / g;
         const int head = hkv * g + r % g;
         const bool row_valid = i <= p_last;
@@ -373,64 +395,71 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         const bool alibi = (p.flags & UA_FLAG_ALIBI) != 0;
         const float sl2 = p.scale * kLog2e;
         const float slope = alibi ? __ldg(p.alibi + head) : 0.f;
-        const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+        const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+        float* red = reinterpret_cast<float*>(smem + C::kOffRed);
         // Keys every row of the tile sees: [kfree_lo, kfree_hi].
         const int kfree_hi = causal ? min(p0 + ctx, sk - 1) : sk - 1;
         const int kfree_lo = window ? max(0, p_last + ctx - p.window + 1) : 0;
 
-        float m = -INFINITY;  // running max, log2 units
-        float l = 0.f;
+        float m = -INFINITY;  // running max, log2 units (identical in both halves)
+        float l = 0.f;        // this half's share of the running denominator
         bool ok = true;
         for (int j = 0; j < n_tiles; ++j) {
-            if (!__all_sync(0xffffffffu, wait_or_abort(B.s_full0 + 8 * (j & 1), (j >> 1) & 1,
-                                                       abort_flag, p.err))) {
+            const bool got = __all_sync(0xffffffffu, wait_or_abort(B.s_full0 + 8 * (j & 1), (j >> 1) & 1,
+                                                                   abort_flag, p.err));
+            uint32_t sr[CPT / 32][32];
+            const int key0 = (t_begin + j) * BN + half * CPT;
+            float pmax = -INFINITY;
+            if (got) {
+                tc::fence_after_sync();
+#pragma unroll
+                for (int c = 0; c < CPT / 32; ++c)
+                    tc::ld32(trow + C::kTmemS + (j & 1) * BN + half * CPT + c * 32, sr[c]);
+                tc::wait_ld();
+                const bool mask_free = key0 >= kfree_lo && key0 + CPT - 1 <= kfree_hi;
+                if constexpr (!PLAIN) {
+#pragma unroll
+                    for (int c = 0; c < CPT / 32; ++c)
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) {
+                            float t = __uint_as_float(sr[c][e]) * p.scale;
+                            if (softcap) t = p.softcap * tanh_via_exp2(t / p.softcap);
+                            if (alibi) t += slope * (float)(key0 + c * 32 + e - ctx);
+                            sr[c][e] = __float_as_uint(t * kLog2e);
+                        }
+                }
+                if (!mask_free) {
+#pragma unroll
+                    for (int c = 0; c < CPT / 32; ++c)
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) {
+                            const int kj = key0 + c * 32 + e;
+                            if (kj < lo || kj > hi) sr[c][e] = __float_as_uint(-INFINITY);
+                        }
+                }
+                // Eight independent three-input max chains, then combined.
+                float mx[8];
+#pragma unroll
+                for (int a = 0; a < 8; ++a) mx[a] = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < CPT / 32; ++c)
+#pragma unroll
+                    for (int e = 0; e < 32; e += 16)
+#pragma unroll
+                        for (int a = 0; a < 8; ++a)
+                            mx[a] = fmax3(mx[a], __uint_as_float(sr[c][e + 2 * a]),
+                                          __uint_as_float(sr[c][e + 2 * a + 1]));
+                pmax = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
+                             fmaxf(mx[6], mx[7]));
+            }
+            red[((j & 1) * 2 + half) * kRows + r] = pmax;
+            // Exchange the partial maxima; the same barrier votes on whether
+            // every softmax thread got its scores (else all leave together).
+            if (!bar_and_sync(1, kSmThreads, got)) {
                 ok = false;
                 break;
             }
-            tc::fence_after_sync();
-            // Scores of this row for the tile's BN keys (fp32 bits).
-            uint32_t sr[BN / 32][32];
-#pragma unroll
-            for (int c = 0; c < BN / 32; ++c) tc::ld32(trow + C::kTmemS + (j & 1) * BN + c * 32, sr[c]);
-            tc::wait_ld();
-            const int key0 = (t_begin + j) * BN;
-            const bool mask_free = key0 >= kfree_lo && key0 + BN - 1 <= kfree_hi;
-            // x: PLAIN -> raw score (scaled inside the exponent's FMA);
-            //    otherwise -> the transformed logit in log2 units.
-            if constexpr (!PLAIN) {
-#pragma unroll
-                for (int c = 0; c < BN / 32; ++c)
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        float t = __uint_as_float(sr[c][e]) * p.scale;
-                        if (softcap) t = p.softcap * tanh_via_exp2(t / p.softcap);
-                        if (alibi) t += slope * (float)(key0 + c * 32 + e - ctx);
-                        sr[c][e] = __float_as_uint(t * kLog2e);
-                    }
-            }
-            if (!mask_free) {
-#pragma unroll
-                for (int c = 0; c < BN / 32; ++c)
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const int kj = key0 + c * 32 + e;
-                        if (kj < lo || kj > hi) sr[c][e] = __float_as_uint(-INFINITY);
-                    }
-            }
-            // Row max: eight independent three-input max chains, then combined.
-            float mx[8];
-#pragma unroll
-            for (int a = 0; a < 8; ++a) mx[a] = -INFINITY;
-#pragma unroll
-            for (int c = 0; c < BN / 32; ++c)
-#pragma unroll
-                for (int e = 0; e < 32; e += 16)
-#pragma unroll
-                    for (int a = 0; a < 8; ++a)
-                        mx[a] = fmax3(mx[a], __uint_as_float(sr[c][e + 2 * a]),
-                                      __uint_as_float(sr[c][e + 2 * a + 1]));
-            float tmax = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
-                               fmaxf(mx[6], mx[7]));
+            float tmax = fmaxf(pmax, red[((j & 1) * 2 + (half ^ 1)) * kRows + r]);
             if constexpr (PLAIN) tmax *= sl2;
             // Lazy re-anchor: move the reference max only when the tile's max
             // exceeds it by more than 8 (log2), so P stays at most 2^8.
@@ -442,104 +471,104 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             }
             const float m_use = (m == -INFINITY) ? 0.f : m;
             const float xs = PLAIN ? sl2 : 1.0f;
-            // P buffer (j & 1) was last read by the P.V of tile j - 2.
-            if (j >= 2) {
-                if (!__all_sync(0xffffffffu, wait_or_abort(B.o_done + 8 * (j & 1), ((j - 2) >> 1) & 1,
-                                                           abort_flag, p.err))) {
-                    ok = false;
-                    break;
-                }
-            }
-            // Rescaling O needs the P.V of tile j - 1 to have finished.
-            if (j > 0 && __any_sync(0xffffffffu, reanchor)) {
-                if (!__all_sync(0xffffffffu, wait_or_abort(B.o_done + 8 * ((j - 1) & 1),
-                                                           ((j - 1) >> 1) & 1, abort_flag, p.err))) {
-                    ok = false;
-                    break;
-                }
-                tc::fence_after_sync();
-#pragma unroll 1
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t o[32];
-                    tc::ld32(trow + C::kTmemO + c * 32, o);
-                    tc::wait_ld();
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                    tc::st32(trow + C::kTmemO + c * 32, o);
-                }
-                tc::wait_st();
-            }
             // P = 2^(x - m): the exponent argument in fp32 (packed pairs), the
             // power of two on the fp16x2 special-function path (two results per
             // instruction; fp16's 11-bit significand is finer than the bf16 P
-            // the MMA consumes), then bf16 into shared memory (128-byte
-            // swizzled K-major panels of 64 keys).  Row sums stay fp32.
+            // the MMA consumes).  Row sums stay fp32.
             float2 rs[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                             make_float2(0.f, 0.f)};
             const float2 sc2 = make_float2(xs, xs);
             const float2 nm2 = make_float2(-m_use, -m_use);
-            uint8_t* prow = smem + C::kOffP + (j & 1) * C::kPBuf + r * 128;
+            uint32_t pk[CPT / 2];
 #pragma unroll
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t pk[16];
+            for (int c = 0; c < CPT / 32; ++c)
 #pragma unroll
                 for (int e = 0; e < 32; e += 2) {
                     const float2 a = ffma2(make_float2(__uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1])),
                                            sc2, nm2);
                     const float2 pr = exp2_pair_f16(a);
                     rs[(e >> 1) & 3] = fadd2(rs[(e >> 1) & 3], pr);
-                    pk[e / 2] = pack_bf16x2(pr.x, pr.y);
+                    pk[(c * 32 + e) / 2] = pack_bf16x2(pr.x, pr.y);
                 }
+            const float2 rs01 = fadd2(rs[0], rs[1]), rs23 = fadd2(rs[2], rs[3]);
+            l = l * alpha + ((rs01.x + rs01.y) + (rs23.x + rs23.y));
+            // The P.V of tile j - 1 must be finished before P is overwritten
+            // and before O is rescaled.
+            bool go = true;
+            if (j > 0) {
+                go = __all_sync(0xffffffffu, wait_or_abort(B.o_done + 8 * ((j - 1) & 1),
+                                                           ((j - 1) >> 1) & 1, abort_flag, p.err));
+                if (go) tc::fence_after_sync();
+            }
+            if (go && j > 0 && __any_sync(0xffffffffu, reanchor)) {
+#pragma unroll 1
+                for (int c = 0; c < D / 64; ++c) {
+                    uint32_t o[32];
+                    const uint32_t col = C::kTmemO + half * (D / 2) + c * 32;
+                    tc::ld32(trow + col, o);
+                    tc::wait_ld();
 #pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    const int chunk = c * 4 + q4;  // 8-key chunk index within the row
+                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                    tc::st32(trow + col, o);
+                }
+                tc::wait_st();
+            }
+            if (go) {
+                // This half's CPT keys of row r -> 128-byte swizzled K-major
+                // panels of 64 keys.
+                uint8_t* prow = smem + C::kOffP + r * 128;
+#pragma unroll
+                for (int q4 = 0; q4 < CPT / 8; ++q4) {
+                    const int chunk = half * (CPT / 8) + q4;  // 8-key chunk within the row
                     const int pn = chunk >> 3, cc = chunk & 7;
                     *reinterpret_cast<uint4*>(prow + pn * (kRows * 128) + ((cc ^ (r & 7)) << 4)) =
                         make_uint4(pk[q4 * 4 + 0], pk[q4 * 4 + 1], pk[q4 * 4 + 2], pk[q4 * 4 + 3]);
                 }
+                fence_proxy_async_smem();
+                tc::fence_before_sync();
+                mbar_arrive(B.p_full + 8 * (j & 1));
             }
-            const float2 rs01 = fadd2(rs[0], rs[1]), rs23 = fadd2(rs[2], rs[3]);
-            const float rsum = (rs01.x + rs01.y) + (rs23.x + rs23.y);
-            l = l * alpha + rsum;
-            fence_proxy_async_smem();
-            tc::fence_before_sync();
-            mbar_arrive(B.p_full + 8 * (j & 1));
         }
         // ------------------------------ epilogue ---------------------------------
-        if (ok && __all_sync(0xffffffffu, wait_or_abort(B.o_done + 8 * ((n_tiles - 1) & 1),
-                                                        ((n_tiles - 1) >> 1) & 1, abort_flag, p.err))) {
-            tc::fence_after_sync();
-            float O_scale_num = 1.f;  // extra factor from the sink re-basing
-            float L = l;
-            bool zero = false;
-            if (p.flags & UA_FLAG_SINKS) {
-                const float s2 = __ldg(p.sinks + head) * kLog2e;
-                if (s2 == INFINITY) {
-                    zero = true;
-                } else if (s2 > m) {
-                    const float a = (m == -INFINITY) ? 0.f : fast_exp2(m - s2);
-                    O_scale_num = a;
-                    L = L * a + 1.0f;
-                } else if (s2 != -INFINITY) {
-                    L += fast_exp2(s2 - m);
+        if (ok) {
+            const bool done = __all_sync(0xffffffffu,
+                                         wait_or_abort(B.o_done + 8 * ((n_tiles - 1) & 1),
+                                                       ((n_tiles - 1) >> 1) & 1, abort_flag, p.err));
+            red[half * kRows + r] = l;
+            if (bar_and_sync(1, kSmThreads, done)) {
+                tc::fence_after_sync();
+                float O_scale_num = 1.f;  // extra factor from the sink re-basing
+                float L = l + red[(half ^ 1) * kRows + r];
+                bool zero = false;
+                if (p.flags & UA_FLAG_SINKS) {
+                    const float s2 = __ldg(p.sinks + head) * kLog2e;
+                    if (s2 == INFINITY) {
+                        zero = true;
+                    } else if (s2 > m) {
+                        const float a = (m == -INFINITY) ? 0.f : fast_exp2(m - s2);
+                        O_scale_num = a;
+                        L = L * a + 1.0f;
+                    } else if (s2 != -INFINITY) {
+                        L += fast_exp2(s2 - m);
+                    }
                 }
-            }
-            const float inv = (!zero && L > 0.f) ? O_scale_num * __frcp_rn(L) : 0.f;
-            __nv_bfloat16* orow = p.out + ((q0 + i) * p.hq + head) * (int64_t)D;
+                const float inv = (!zero && L > 0.f) ? O_scale_num * __frcp_rn(L) : 0.f;
+                __nv_bfloat16* orow = p.out + ((q0 + i) * p.hq + head) * (int64_t)D + half * (D / 2);
 #pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t o[32];
-                tc::ld32(trow + C::kTmemO + c * 32, o);
-                tc::wait_ld();
-                if (row_valid) {
+                for (int c = 0; c < D / 64; ++c) {
+                    uint32_t o[32];
+                    tc::ld32(trow + C::kTmemO + half * (D / 2) + c * 32, o);
+                    tc::wait_ld();
+                    if (row_valid) {
 #pragma unroll
-                    for (int e = 0; e < 32; e += 8) {
-                        uint4 v;
-                        v.x = pack_bf16x2(__uint_as_float(o[e + 0]) * inv, __uint_as_float(o[e + 1]) * inv);
-                        v.y = pack_bf16x2(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
-                        v.z = pack_bf16x2(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv);
-                        v.w = pack_bf16x2(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv);
-                        *reinterpret_cast<uint4*>(orow + c * 32 + e) = v;
+                        for (int e = 0; e < 32; e += 8) {
+                            uint4 v;
+                            v.x = pack_bf16x2(__uint_as_float(o[e + 0]) * inv, __uint_as_float(o[e + 1]) * inv);
+                            v.y = pack_bf16x2(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
+                            v.z = pack_bf16x2(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv);
+                            v.w = pack_bf16x2(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv);
+                            *reinterpret_cast<uint4*>(orow + c * 32 + e) = v;
+                        }
                     }
                 }
             }
@@ -548,7 +577,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 
     tc::fence_before_sync();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == kWarpMma) {
         tc::fence_after_sync();
         tc::tmem_dealloc(tmem, kTmemCols);
     }
