@@ -38,13 +38,18 @@ namespace {
 
 constexpr float kLazy = 8.0f;
 constexpr int kRows = 128;
-constexpr int kSmThreads = 256;             // two softmax warpgroups: column halves of each row
-constexpr int kThreads = kSmThreads + 64;   // + TMA producer warp + MMA warp
-constexpr int kWarpTma = 8;
-constexpr int kWarpMma = 9;
+// SPLIT softmax warpgroups share each row's BN key columns (SPLIT parts of
+// BN / SPLIT); one more warp issues TMA copies and one issues MMAs.
+template <int SPLIT>
+struct Roles {
+    static constexpr int kSmThreads = 128 * SPLIT;
+    static constexpr int kThreads = kSmThreads + 64;
+    static constexpr int kWarpTma = 4 * SPLIT;
+    static constexpr int kWarpMma = 4 * SPLIT + 1;
+};
 constexpr uint32_t kTmemCols = 512;
 
-template <int D, int BN, int NS>
+template <int D, int BN, int NS, int SPLIT>
 struct PCfg {
     static constexpr int kPanels = D / 64;
     static constexpr int kQPanel = kRows * 128;
@@ -61,8 +66,8 @@ struct PCfg {
     // q_full, k_full[NS], v_full[NS], k_empty[NS], v_empty[NS], s_full[2], p_full[2],
     // o_done[2], drain
     static constexpr int kNumBars = 1 + 4 * NS + 2 + 2 + 2 + 1;
-    static constexpr int kOffRed = kOffBar + kNumBars * 8;      // [2 parity][2 half][128] fp32
-    static constexpr int kOffMisc = kOffRed + 2 * 2 * kRows * 4;
+    static constexpr int kOffRed = kOffBar + kNumBars * 8;      // [2 parity][SPLIT][128] fp32
+    static constexpr int kOffMisc = kOffRed + 2 * SPLIT * kRows * 4;
     static constexpr int kSmem = kOffMisc + 16 + 1024;
     static constexpr int kTmemS = 0;
     static constexpr int kTmemO = 2 * BN;
@@ -149,11 +154,16 @@ __device__ __forceinline__ float tanh_via_exp2(float x) {
     return 1.0f - __fdividef(2.0f, e + 1.0f);
 }
 
-template <int D, int BN, int NS, bool PLAIN>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int D, int BN, int NS, int SPLIT, bool PLAIN>
+__global__ void __launch_bounds__(Roles<SPLIT>::kThreads, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
-    using C = PCfg<D, BN, NS>;
+    using C = PCfg<D, BN, NS, SPLIT>;
+    using R = Roles<SPLIT>;
+    constexpr int kThreads = R::kThreads;
+    constexpr int kSmThreads = R::kSmThreads;
+    constexpr int kWarpTma = R::kWarpTma;
+    constexpr int kWarpMma = R::kWarpMma;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -380,12 +390,14 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         }
     } else {
         // ------------------------- softmax + epilogue warps -----------------------
-        // Thread (half, r): row r of the tile (tensor-memory lane r) and the
-        // half of its BN key columns [half * CPT, half * CPT + CPT).  The two
-        // halves agree on the row max through shared memory once per tile.
-        constexpr int CPT = BN / 2;
+        // Thread (part, r): row r of the tile (tensor-memory lane r) and part
+        // `part` of its BN key columns [part * CPT, part * CPT + CPT).  The
+        // parts agree on the row max through shared memory once per tile.
+        constexpr int CPT = BN / SPLIT;
+        constexpr int OPT = D / SPLIT;   // output columns per thread
+        static_assert(CPT % 32 == 0 && OPT % 32 == 0, "column split");
         const int r = threadIdx.x & (kRows - 1);
-        const int half = threadIdx.x >> 7;
+        const int half = threadIdx.x >> 7;   // part index
         const int i = p0 + r / g;
         const int head = hkv * g + r % g;
         const bool row_valid = i <= p_last;
@@ -452,14 +464,17 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 pmax = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
                              fmaxf(mx[6], mx[7]));
             }
-            red[((j & 1) * 2 + half) * kRows + r] = pmax;
+            red[((j & 1) * SPLIT + half) * kRows + r] = pmax;
             // Exchange the partial maxima; the same barrier votes on whether
             // every softmax thread got its scores (else all leave together).
             if (!bar_and_sync(1, kSmThreads, got)) {
                 ok = false;
                 break;
             }
-            float tmax = fmaxf(pmax, red[((j & 1) * 2 + (half ^ 1)) * kRows + r]);
+            float tmax = pmax;
+#pragma unroll
+            for (int o = 1; o < SPLIT; ++o)
+                tmax = fmaxf(tmax, red[((j & 1) * SPLIT + ((half + o) % SPLIT)) * kRows + r]);
             if constexpr (PLAIN) tmax *= sl2;
             // Lazy re-anchor: move the reference max only when the tile's max
             // exceeds it by more than 8 (log2), so P stays at most 2^8.
@@ -502,9 +517,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             }
             if (go && j > 0 && __any_sync(0xffffffffu, reanchor)) {
 #pragma unroll 1
-                for (int c = 0; c < D / 64; ++c) {
+                for (int c = 0; c < OPT / 32; ++c) {
                     uint32_t o[32];
-                    const uint32_t col = C::kTmemO + half * (D / 2) + c * 32;
+                    const uint32_t col = C::kTmemO + half * OPT + c * 32;
                     tc::ld32(trow + col, o);
                     tc::wait_ld();
 #pragma unroll
@@ -538,7 +553,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             if (bar_and_sync(1, kSmThreads, done)) {
                 tc::fence_after_sync();
                 float O_scale_num = 1.f;  // extra factor from the sink re-basing
-                float L = l + red[(half ^ 1) * kRows + r];
+                float L = l;
+#pragma unroll
+                for (int o = 1; o < SPLIT; ++o) L += red[((half + o) % SPLIT) * kRows + r];
                 bool zero = false;
                 if (p.flags & UA_FLAG_SINKS) {
                     const float s2 = __ldg(p.sinks + head) * kLog2e;
@@ -553,11 +570,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     }
                 }
                 const float inv = (!zero && L > 0.f) ? O_scale_num * __frcp_rn(L) : 0.f;
-                __nv_bfloat16* orow = p.out + ((q0 + i) * p.hq + head) * (int64_t)D + half * (D / 2);
+                __nv_bfloat16* orow = p.out + ((q0 + i) * p.hq + head) * (int64_t)D + half * OPT;
 #pragma unroll 1
-                for (int c = 0; c < D / 64; ++c) {
+                for (int c = 0; c < OPT / 32; ++c) {
                     uint32_t o[32];
-                    tc::ld32(trow + C::kTmemO + half * (D / 2) + c * 32, o);
+                    tc::ld32(trow + C::kTmemO + half * OPT + c * 32, o);
                     tc::wait_ld();
                     if (row_valid) {
 #pragma unroll
@@ -583,12 +600,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     }
 }
 
-template <int D, int BN, int NS>
+template <int D, int BN, int NS, int SPLIT, bool PLAIN>
 cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                      const FwdParams& p, int tiles, cudaStream_t stream) {
-    using C = PCfg<D, BN, NS>;
-    const bool plain = (p.flags & (UA_FLAG_SOFTCAP | UA_FLAG_ALIBI)) == 0;
-    auto kern = plain ? prefill_kernel<D, BN, NS, true> : prefill_kernel<D, BN, NS, false>;
+    using C = PCfg<D, BN, NS, SPLIT>;
+    constexpr int kThreads = Roles<SPLIT>::kThreads;
+    auto kern = prefill_kernel<D, BN, NS, SPLIT, PLAIN>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)tiles, (unsigned)p.hk, (unsigned)p.num_seqs);
@@ -624,10 +641,19 @@ cudaError_t launch_prefill(const PrefillPlan& plan, const CUtensorMap& tm_k, con
     cuuint32_t box[3] = {64, (cuuint32_t)p.g, (cuuint32_t)(kRows / p.g)};
     if (!encode_bf16_sw128(&tq, p.q, 3, dims, strides, box)) return cudaErrorInvalidValue;
     if (plan.num_tiles <= 0) return cudaSuccess;
+    const bool plain = (p.flags & (UA_FLAG_SOFTCAP | UA_FLAG_ALIBI)) == 0;
     switch (p.d) {
-        case 64: return launch_t<64, 128, 4>(tq, tm_k, tm_v, p, plan.num_tiles, stream);
-        case 128: return launch_t<128, 128, 2>(tq, tm_k, tm_v, p, plan.num_tiles, stream);
-        case 256: return launch_t<256, 64, 2>(tq, tm_k, tm_v, p, plan.num_tiles, stream);
+        // Plain scores: two softmax warpgroups per row.  With softcap / ALiBi
+        // the per-score work doubles, so d = 128 spreads it over four.
+        case 64:
+            return plain ? launch_t<64, 128, 4, 2, true>(tq, tm_k, tm_v, p, plan.num_tiles, stream)
+                         : launch_t<64, 128, 4, 2, false>(tq, tm_k, tm_v, p, plan.num_tiles, stream);
+        case 128:
+            return plain ? launch_t<128, 128, 2, 2, true>(tq, tm_k, tm_v, p, plan.num_tiles, stream)
+                         : launch_t<128, 128, 2, 4, false>(tq, tm_k, tm_v, p, plan.num_tiles, stream);
+        case 256:
+            return plain ? launch_t<256, 64, 2, 2, true>(tq, tm_k, tm_v, p, plan.num_tiles, stream)
+                         : launch_t<256, 64, 2, 2, false>(tq, tm_k, tm_v, p, plan.num_tiles, stream);
         default: return cudaErrorInvalidValue;
     }
 }
