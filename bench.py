@@ -155,6 +155,21 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def aggregate_ranks(local_ms, local_bytes, device):
+    """Whole-job timing over ranks: (max of the ranks' timed milliseconds, sum of
+    the bytes every rank processed per step).  No data-path collective: each rank
+    owns an independent batch; this is the only cross-rank exchange."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(local_ms), int(local_bytes)
+    t = torch.tensor([float(local_ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    b = torch.tensor([int(local_bytes)], dtype=torch.int64, device=device)
+    dist.all_reduce(b, op=dist.ReduceOp.SUM)
+    return float(t.item()), int(b.item())
+
+
 def workload_units(w):
     """(algorithmic bytes, algorithmic flops) of one forward pass of w."""
     kv = w.kv_bytes_read()
@@ -299,13 +314,9 @@ def run_ours(args):
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    total_ms = sum(res["step_ms"])
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms, total_bytes = aggregate_ranks(sum(res["step_ms"]), nbytes, dev)
     ms_per_step = total_ms / args.steps
-    value = nbytes * world / (ms_per_step * 1e-3) / 1e9
+    value = total_bytes / (ms_per_step * 1e-3) / 1e9
     kern_ms = statistics.mean(res["kernel_ms"])
     achieved = nbytes / (kern_ms * 1e-3) / 1e9
     clocks = sampler.summary(res["t0"], res["t1"])
