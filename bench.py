@@ -179,8 +179,8 @@ def workload_units(w):
     return kv + qo + meta, flops
 
 
-def time_ours(w, steps, warmup, flush, torch, ua):
-    prob = ua.Problem.for_workload(w)
+def time_ours(w, steps, warmup, flush, torch, ua, path=0):
+    prob = ua.Problem.for_workload(w, path=path)
     out = torch.empty_like(w.q)
     stream = torch.cuda.current_stream()
     flush_buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=w.q.device)
@@ -395,7 +395,9 @@ def run_single(args):
     peaks, peak_src = load_peaks()
     w = W.make(args.workload, device="cuda")
     nbytes, flops = workload_units(w)
-    r = time_ours(w, args.steps, args.warmup, flush=True, torch=torch, ua=ua)
+    path = {"auto": ua.UA_PATH_AUTO, "split": ua.UA_PATH_SPLIT_KV,
+            "tensor": ua.UA_PATH_TENSOR_CORE}[args.path]
+    r = time_ours(w, args.steps, args.warmup, flush=True, torch=torch, ua=ua, path=path)
     ms = statistics.mean(r["step_ms"])
     km = statistics.mean(r["kernel_ms"])
     print(json.dumps({
@@ -468,6 +470,8 @@ def main():
                              "wide_mha_alibi"],
                     help="time only this workload and print its own short JSON line "
                          "(for profiling); the default is the full headline run")
+    ap.add_argument("--path", default="auto", choices=["auto", "split", "tensor"],
+                    help="kernel family for --workload (default: the library's choice)")
     args = ap.parse_args()
     if args.warmup < 3:
         log("warmup raised to 3")

@@ -85,6 +85,14 @@ enum {
 
 enum { UA_DTYPE_BF16 = 0 };
 
+/* Execution path.  AUTO picks per call (gfx950 spec section 6: a path whose
+ * query-tile grid fills the device versus split-KV segments plus a reduction):
+ * the CUDA-core split-KV kernel when a KV head has at most 16 packed query rows
+ * (decode-like calls), the tensor-core kernel otherwise.  SPLIT_KV and
+ * TENSOR_CORE force one family for every call (TENSOR_CORE needs 128 % g == 0;
+ * otherwise ua_forward returns UA_ERR_UNSUPPORTED). */
+enum { UA_PATH_AUTO = 0, UA_PATH_SPLIT_KV = 1, UA_PATH_TENSOR_CORE = 2 };
+
 /*
  * Static description of a problem family (UnifiedAttentionProblem in the
  * gfx950 spec: one flag per bias/mask term, section 1 last paragraph and
@@ -104,6 +112,7 @@ typedef struct ua_problem_desc {
     float scale;                /* tau > 0 (usually 1/sqrt(d)) */
     float softcap;              /* c > 0 when UA_FLAG_SOFTCAP, else ignored */
     int32_t window;             /* W >= 1 when UA_FLAG_WINDOW, else ignored */
+    uint32_t path;              /* UA_PATH_*: which kernel family serves the calls */
 } ua_problem_desc;
 
 typedef struct ua_problem ua_problem;

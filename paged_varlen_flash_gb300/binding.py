@@ -26,6 +26,10 @@ UA_DEVERR_TIMEOUT = 1 << 4
 
 UA_DTYPE_BF16 = 0
 
+UA_PATH_AUTO = 0
+UA_PATH_SPLIT_KV = 1
+UA_PATH_TENSOR_CORE = 2
+
 _lib = None
 
 
@@ -53,6 +57,7 @@ class ProblemDesc(ctypes.Structure):
         ("scale", ctypes.c_float),
         ("softcap", ctypes.c_float),
         ("window", ctypes.c_int32),
+        ("path", ctypes.c_uint32),
     ]
 
 
@@ -134,12 +139,12 @@ def flags_of(causal=True, softcap=0.0, alibi=False, window=0, sinks=False):
 
 def ua_problem_create(num_q_heads, num_kv_heads, head_size, block_size, num_blocks,
                       max_num_seqs, max_blocks_per_seq, max_total_q, flags, scale,
-                      softcap=0.0, window=0):
+                      softcap=0.0, window=0, path=UA_PATH_AUTO):
     """Returns an opaque problem handle (int); raises UAError on failure."""
     lib = load_library()
     d = ProblemDesc(num_q_heads, num_kv_heads, head_size, block_size, num_blocks,
                     max_num_seqs, max_blocks_per_seq, max_total_q, UA_DTYPE_BF16, flags,
-                    scale, softcap, window)
+                    scale, softcap, window, path)
     h = ctypes.c_void_p()
     st = lib.ua_problem_create(ctypes.byref(d), ctypes.byref(h))
     if st != UA_OK:
@@ -207,21 +212,22 @@ class Problem:
 
     def __init__(self, num_q_heads, num_kv_heads, head_size, block_size, num_blocks,
                  max_num_seqs, max_blocks_per_seq, max_total_q, flags, scale, softcap=0.0,
-                 window=0):
+                 window=0, path=UA_PATH_AUTO):
         self.handle = ua_problem_create(num_q_heads, num_kv_heads, head_size, block_size,
                                         num_blocks, max_num_seqs, max_blocks_per_seq,
-                                        max_total_q, flags, scale, softcap, window)
+                                        max_total_q, flags, scale, softcap, window, path)
         self.flags = flags
         self.head_size = head_size
         self.num_q_heads = num_q_heads
 
     @classmethod
-    def for_workload(cls, w, max_total_q=None, max_num_seqs=None, extra_flags=0):
+    def for_workload(cls, w, max_total_q=None, max_num_seqs=None, extra_flags=0,
+                     path=UA_PATH_AUTO):
         flags = flags_of(w.causal, w.softcap, w.alibi_slopes is not None, w.window,
                          w.sinks is not None) | extra_flags
         return cls(w.hq, w.hk, w.d, w.b, w.num_blocks, max_num_seqs or max(1, w.num_seqs),
                    w.max_blocks_per_seq, max_total_q or max(1, w.total_q), flags, w.scale,
-                   w.softcap, w.window)
+                   w.softcap, w.window, path)
 
     def forward(self, q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, num_seqs,
                 total_q, max_seqlen_q, max_seqlen_k, flags, sinks=None, alibi_slopes=None,

@@ -135,6 +135,7 @@ ua_status ua_problem_create(const ua_problem_desc* d, ua_problem** out) {
     if (d->head_size != 64 && d->head_size != 128 && d->head_size != 256) return UA_ERR_UNSUPPORTED;
     if (d->block_size != 16 && d->block_size != 32 && d->block_size != 64) return UA_ERR_UNSUPPORTED;
     if (d->num_blocks > (int64_t(1) << 31) - 1) return UA_ERR_UNSUPPORTED;
+    if (d->path > UA_PATH_TENSOR_CORE) return UA_ERR_INVALID_ARG;
 
     ua_problem* p = new (std::nothrow) ua_problem();
     if (!p) return UA_ERR_OUT_OF_MEMORY;
@@ -267,10 +268,16 @@ ua_status ua_forward(ua_problem* p, const void* q, const void* k_cache, const vo
 
     // ---- path choice ------------------------------------------------------
     const int64_t rows_per_kv = (int64_t)g * max_seqlen_q;
-    const bool use_tc = ua::prefill_shape_ok(fp) && rows_per_kv > 16;
+    const bool tc_ok = ua::prefill_shape_ok(fp);
+    bool use_tc = tc_ok && rows_per_kv > 16;
+    if (d.path == UA_PATH_SPLIT_KV) use_tc = false;
+    if (d.path == UA_PATH_TENSOR_CORE) {
+        if (!tc_ok) return UA_ERR_UNSUPPORTED;
+        use_tc = true;
+    }
     if (use_tc) {
         ua::PrefillPlan plan;
-        ua::plan_prefill(fp, p->num_sms, &plan);
+        ua::plan_prefill(fp, p->num_sms, p->ws_bytes, &plan);
         if (p->map_p_rows != plan.kv_box_rows) {
             if (!encode_cache_map(&p->map_kp, k_cache, d, plan.kv_box_rows) ||
                 !encode_cache_map(&p->map_vp, v_cache, d, plan.kv_box_rows)) {
@@ -280,8 +287,10 @@ ua_status ua_forward(ua_problem* p, const void* q, const void* k_cache, const vo
             }
             p->map_p_rows = plan.kv_box_rows;
         }
-        fp.splits = 1;
-        fp.chunk = 0;
+        fp.splits = plan.splits;
+        fp.chunk = plan.chunk;
+        fp.part_o = p->d_ws;
+        fp.part_ml = p->d_ws + (size_t)total_q * d.num_q_heads * plan.splits * d.head_size;
         prof_mark(p, true, st);
         cudaError_t e = ua::launch_prefill(plan, p->map_kp, p->map_vp, fp, st);
         prof_mark(p, false, st);
@@ -289,8 +298,15 @@ ua_status ua_forward(ua_problem* p, const void* q, const void* k_cache, const vo
             note_cuda(e, "prefill kernel launch");
             return UA_ERR_CUDA;
         }
+        if (plan.splits > 1) {
+            e = ua::launch_combine(fp, st);
+            if (e != cudaSuccess) {
+                note_cuda(e, "combine kernel launch");
+                return UA_ERR_CUDA;
+            }
+        }
         p->last_launches = plan.launches;
-        p->last_path = "prefill_tc";
+        p->last_path = plan.splits > 1 ? "tensor_core+combine" : "tensor_core";
         return UA_OK;
     }
 

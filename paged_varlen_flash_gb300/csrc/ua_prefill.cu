@@ -24,6 +24,7 @@
 //              shared memory and V read MN-major straight from its TMA tile.
 //
 // Tensor memory (512 columns): S0 [0, BN), S1 [BN, 2 BN), O [2 BN, 2 BN + D).
+#include <algorithm>
 #include <cstdint>
 #include <cstring>
 
@@ -171,7 +172,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     const int lane = threadIdx.x & 31;
     const int s = blockIdx.z;
     const int hkv = blockIdx.y;
-    const int qt = gridDim.x - 1 - blockIdx.x;  // heaviest (latest) tiles first
+    const bool split = p.splits > 1;             // write (m, l, o) partials per KV segment
+    const int seg = blockIdx.x % p.splits;
+    const int qt = (int)(gridDim.x / p.splits) - 1 - (int)(blockIdx.x / p.splits);  // heaviest first
     const int g = p.g;
     const int ppt = kRows / g;                  // positions per tile
     const int p0 = qt * ppt;
@@ -179,25 +182,39 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     int sq, sk;
     int64_t q0;
     const uint32_t st = seq_status(p, s, sq, sk, q0);
-    if (st && qt == 0 && hkv == 0 && threadIdx.x == 0) atomicOr(p.err, (int)st);
+    if (st && qt == 0 && hkv == 0 && seg == 0 && threadIdx.x == 0) atomicOr(p.err, (int)st);
     if (st & UA_DEVERR_CU_SEQLENS) return;
     if (p0 >= sq) return;
+    if (seg >= (split ? seq_segments(p, st, sk) : 1)) return;
     const int p_last = min(p0 + ppt, sq) - 1;
-    if (st) {  // malformed lengths: the tile's rows are written as zeros
+    const int ctx = sk - sq;
+    const bool causal = (p.flags & UA_FLAG_CAUSAL) != 0;
+    const bool window = (p.flags & UA_FLAG_WINDOW) != 0;
+    int k_end = causal ? min(sk, p_last + ctx + 1) : sk;
+    int k_beg = window ? max(0, p0 + ctx - p.window + 1) : 0;
+    if (split) {  // this CTA's KV segment; segments are whole BN tiles
+        k_beg = max(k_beg, seg * p.chunk);
+        k_end = min(k_end, seg * p.chunk + p.chunk);
+    }
+    if (st || k_beg >= k_end) {
+        // Malformed lengths (rows written as zeros) or a segment with no
+        // visible key for any row of the tile (an empty partial, m = -inf).
         for (int e = threadIdx.x; e < kRows * (D / 8); e += kThreads) {
             const int r = e / (D / 8), c = e % (D / 8);
             const int i = p0 + r / g;
             if (i > p_last) continue;
             const int64_t row = (q0 + i) * p.hq + hkv * g + r % g;
-            *reinterpret_cast<uint4*>(p.out + row * D + c * 8) = make_uint4(0, 0, 0, 0);
+            if (split) {
+                if (c == 0) {
+                    p.part_ml[(row * p.splits + seg) * 2 + 0] = -INFINITY;
+                    p.part_ml[(row * p.splits + seg) * 2 + 1] = 0.f;
+                }
+            } else {
+                *reinterpret_cast<uint4*>(p.out + row * D + c * 8) = make_uint4(0, 0, 0, 0);
+            }
         }
         return;
     }
-    const int ctx = sk - sq;
-    const bool causal = (p.flags & UA_FLAG_CAUSAL) != 0;
-    const bool window = (p.flags & UA_FLAG_WINDOW) != 0;
-    const int k_end = causal ? min(sk, p_last + ctx + 1) : sk;
-    const int k_beg = window ? max(0, p0 + ctx - p.window + 1) : 0;
     const int t_begin = k_beg / BN;
     const int n_tiles = (k_end + BN - 1) / BN - t_begin;
 
@@ -413,6 +430,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         const int kfree_hi = causal ? min(p0 + ctx, sk - 1) : sk - 1;
         const int kfree_lo = window ? max(0, p_last + ctx - p.window + 1) : 0;
 
+        // Warps whose 32 rows are all padding (past the sequence's last
+        // position) skip the score work; they still take part in every
+        // barrier.
+        const bool live = __any_sync(0xffffffffu, row_valid);
         float m = -INFINITY;  // running max, log2 units (identical in both halves)
         float l = 0.f;        // this half's share of the running denominator
         bool ok = true;
@@ -422,7 +443,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             uint32_t sr[CPT / 32][32];
             const int key0 = (t_begin + j) * BN + half * CPT;
             float pmax = -INFINITY;
-            if (got) {
+            if (got && live) {
                 tc::fence_after_sync();
 #pragma unroll
                 for (int c = 0; c < CPT / 32; ++c)
@@ -515,7 +536,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                                                            ((j - 1) >> 1) & 1, abort_flag, p.err));
                 if (go) tc::fence_after_sync();
             }
-            if (go && j > 0 && __any_sync(0xffffffffu, reanchor)) {
+            if (go && live && j > 0 && __any_sync(0xffffffffu, reanchor)) {
 #pragma unroll 1
                 for (int c = 0; c < OPT / 32; ++c) {
                     uint32_t o[32];
@@ -529,8 +550,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 tc::wait_st();
             }
             if (go) {
-                // This half's CPT keys of row r -> 128-byte swizzled K-major
-                // panels of 64 keys.
+                // This part's CPT keys of row r -> 128-byte swizzled K-major
+                // panels of 64 keys (padding-only warps leave their rows stale;
+                // those output rows are never stored).
+                if (live) {
                 uint8_t* prow = smem + C::kOffP + r * 128;
 #pragma unroll
                 for (int q4 = 0; q4 < CPT / 8; ++q4) {
@@ -538,6 +561,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     const int pn = chunk >> 3, cc = chunk & 7;
                     *reinterpret_cast<uint4*>(prow + pn * (kRows * 128) + ((cc ^ (r & 7)) << 4)) =
                         make_uint4(pk[q4 * 4 + 0], pk[q4 * 4 + 1], pk[q4 * 4 + 2], pk[q4 * 4 + 3]);
+                }
                 }
                 fence_proxy_async_smem();
                 tc::fence_before_sync();
@@ -550,7 +574,33 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                                          wait_or_abort(B.o_done + 8 * ((n_tiles - 1) & 1),
                                                        ((n_tiles - 1) >> 1) & 1, abort_flag, p.err));
             red[half * kRows + r] = l;
-            if (bar_and_sync(1, kSmThreads, done)) {
+            const bool all_done = bar_and_sync(1, kSmThreads, done);
+            if (all_done && live && split) {
+                // Split partial: raw o (this part's columns), m in log2 units, l.
+                tc::fence_after_sync();
+                float L = l;
+#pragma unroll
+                for (int o = 1; o < SPLIT; ++o) L += red[((half + o) % SPLIT) * kRows + r];
+                const int64_t row = (q0 + i) * p.hq + head;
+                float* po = p.part_o + (row * p.splits + seg) * D + half * OPT;
+                if (row_valid && half == 0) {
+                    p.part_ml[(row * p.splits + seg) * 2 + 0] = m;
+                    p.part_ml[(row * p.splits + seg) * 2 + 1] = L;
+                }
+#pragma unroll 1
+                for (int c = 0; c < OPT / 32; ++c) {
+                    uint32_t o[32];
+                    tc::ld32(trow + C::kTmemO + half * OPT + c * 32, o);
+                    tc::wait_ld();
+                    if (row_valid) {
+#pragma unroll
+                        for (int e = 0; e < 32; e += 4)
+                            *reinterpret_cast<float4*>(po + c * 32 + e) =
+                                make_float4(__uint_as_float(o[e]), __uint_as_float(o[e + 1]),
+                                            __uint_as_float(o[e + 2]), __uint_as_float(o[e + 3]));
+                    }
+                }
+            } else if (all_done && live && !split) {
                 tc::fence_after_sync();
                 float O_scale_num = 1.f;  // extra factor from the sink re-basing
                 float L = l;
@@ -608,7 +658,7 @@ cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
     auto kern = prefill_kernel<D, BN, NS, SPLIT, PLAIN>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
-    dim3 grid((unsigned)tiles, (unsigned)p.hk, (unsigned)p.num_seqs);
+    dim3 grid((unsigned)(tiles * p.splits), (unsigned)p.hk, (unsigned)p.num_seqs);
     kern<<<grid, kThreads, C::kSmem, stream>>>(tq, tk, tv, p);
     return cudaGetLastError();
 }
@@ -617,14 +667,32 @@ cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
 
 bool prefill_supported(int d) { return d == 64 || d == 128 || d == 256; }
 
-void plan_prefill(const FwdParams& p, int num_sms, PrefillPlan* plan) {
-    (void)num_sms;
+void plan_prefill(const FwdParams& p, int num_sms, size_t workspace_bytes, PrefillPlan* plan) {
     *plan = PrefillPlan();
     plan->kv_box_rows = p.b;
+    const int bn = p.d == 256 ? 64 : 128;
     const int ppt = kRows / p.g;
     plan->num_tiles = (p.max_seqlen_q + ppt - 1) / ppt;
-    plan->grid = plan->num_tiles * p.hk * p.num_seqs;
-    plan->launches = 1;
+    // Split the keys into segments only when the (tile, kv head, sequence)
+    // grid is too small to give every SM about four CTAs; each segment keeps
+    // at least eight KV tiles.
+    const int64_t base = (int64_t)plan->num_tiles * p.hk * p.num_seqs;
+    int splits = 1;
+    if (base < 4LL * num_sms) {
+        const int64_t want = (4LL * num_sms + base - 1) / base;
+        const int64_t by_len = std::max<int64_t>(1, p.max_seqlen_k / (8 * bn));
+        splits = (int)std::min<int64_t>(std::min<int64_t>(want, by_len), 64);
+        const size_t per_split = (size_t)p.total_q * p.hq * (p.d + 2) * sizeof(float);
+        splits = (int)std::min<size_t>((size_t)splits, per_split ? workspace_bytes / per_split : 1);
+        if (splits < 1) splits = 1;
+    }
+    if (splits > 1) {
+        const int per = (p.max_seqlen_k + splits - 1) / splits;
+        plan->chunk = (per + bn - 1) / bn * bn;
+        splits = (p.max_seqlen_k + plan->chunk - 1) / plan->chunk;
+    }
+    plan->splits = splits;
+    plan->launches = splits > 1 ? 2 : 1;
 }
 
 bool prefill_shape_ok(const FwdParams& p) {

@@ -7,8 +7,9 @@ namespace ua {
 
 struct PrefillPlan {
     int kv_box_rows = 64;  // slots per TMA box of the paged caches
-    int grid = 0;          // persistent CTAs
-    int num_tiles = 0;     // work items (q tile, kv head, sequence)
+    int num_tiles = 0;     // query tiles per (sequence, kv head) (grid x / splits)
+    int splits = 1;        // KV segments per tile (1 = the kernel writes O itself)
+    int chunk = 0;         // keys per segment (a multiple of the KV tile)
     int launches = 0;      // kernels enqueued per call
 };
 
@@ -19,8 +20,9 @@ bool prefill_supported(int d);
 // whole GQA groups: g divides 128).
 bool prefill_shape_ok(const FwdParams& p);
 
-// Fill *plan for the call described by p.
-void plan_prefill(const FwdParams& p, int num_sms, PrefillPlan* plan);
+// Fill *plan for the call described by p; split partials may use up to
+// `workspace_bytes` of the problem workspace.
+void plan_prefill(const FwdParams& p, int num_sms, size_t workspace_bytes, PrefillPlan* plan);
 
 // Enqueue the prefill path (p.out receives the final bf16 rows).
 cudaError_t launch_prefill(const PrefillPlan& plan, const CUtensorMap& tm_k,

@@ -29,9 +29,19 @@ def _built():
     ua.load_library()
 
 
-def run_gpu(w, problem=None, out=None):
+# Both kernel families are checked on every shape they can serve.
+PATHS = [ua.UA_PATH_SPLIT_KV, ua.UA_PATH_TENSOR_CORE]
+
+
+def tc_ok(w):
+    return 128 % (w.hq // w.hk) == 0
+
+
+def run_gpu(w, problem=None, out=None, path=ua.UA_PATH_AUTO):
+    if path == ua.UA_PATH_TENSOR_CORE and not tc_ok(w):
+        pytest.skip("g does not divide the 128-row tile")
     wd = w.to("cuda")
-    prob = problem or ua.Problem.for_workload(wd)
+    prob = problem or ua.Problem.for_workload(wd, path=path)
     res = prob.forward_workload(wd, out=out)
     err = prob.check_device_error()
     return res.float().cpu(), err, prob
@@ -64,23 +74,25 @@ SWEEP = [
 ]
 
 
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("case", range(len(SWEEP)))
-def test_small_sweep_matches_oracle(case):
+def test_small_sweep_matches_oracle(case, path):
     d, b, hq, hk, sq, ctx, fl = SWEEP[case]
     w = W.random_small(100 + case, num_seqs=5, hq=hq, hk=hk, d=d, b=b, sq=sq, ctx=ctx, **fl)
     want = oracle.forward_workload(w)
-    got, err, _ = run_gpu(w)
+    got, err, _ = run_gpu(w, path=path)
     assert err == 0
     check_close(got, want)
 
 
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("d,b,g,sq", [(64, 16, 4, 128), (128, 32, 4, 300), (128, 64, 16, 40),
-                                      (256, 64, 1, 128)])
-def test_prefill_shapes_match_oracle(d, b, g, sq):
-    w = W.random_small(200 + d + b + g, num_seqs=3, hq=2 * g, hk=2, d=d, b=b, sq=(sq // 2, sq),
+                                      (256, 64, 1, 128), (128, 16, 8, 1), (64, 32, 2, 3)])
+def test_prefill_shapes_match_oracle(d, b, g, sq, path):
+    w = W.random_small(200 + d + b + g, num_seqs=3, hq=2 * g, hk=2, d=d, b=b, sq=(sq // 2 + 1, sq),
                        ctx=(0, 100))
     want = oracle.forward_workload(w)
-    got, err, _ = run_gpu(w)
+    got, err, _ = run_gpu(w, path=path)
     assert err == 0
     check_close(got, want)
 
@@ -88,18 +100,22 @@ def test_prefill_shapes_match_oracle(d, b, g, sq):
 # ---------------------------------------------------------------------------
 # The five benchmark workloads.
 # ---------------------------------------------------------------------------
-def test_tiny_config_full():
+@pytest.mark.parametrize("path", PATHS)
+def test_tiny_config_full(path):
     w = W.make("tiny", poison=True)
     want = oracle.forward_workload(w)
-    got, err, prob = run_gpu(w)
+    got, err, prob = run_gpu(w, path=path)
     assert err == 0
     check_close(got, want)
 
 
+@pytest.mark.parametrize("path", [ua.UA_PATH_AUTO] + PATHS)
 @pytest.mark.parametrize("name", ["decode", "chunked", "long_prefill", "wide_mha_alibi"])
-def test_config_sampled_rows(name):
+def test_config_sampled_rows(name, path):
+    if path == ua.UA_PATH_SPLIT_KV and name in ("long_prefill", "wide_mha_alibi"):
+        pytest.skip("CUDA-core path on 2 TFLOP workloads: covered by the smaller prefill shapes")
     w = W.make(name, device="cuda", poison=(name != "long_prefill"))
-    prob = ua.Problem.for_workload(w)
+    prob = ua.Problem.for_workload(w, path=path)
     out = prob.forward_workload(w)
     assert prob.check_device_error() == 0
     ids = W.sample_rows(w, 400, seed=7)
@@ -129,10 +145,12 @@ def test_long_prefill_shuffled_table_bit_identical():
 # Bit-exact index work: one dominant key per (row, kv head) makes the output
 # equal to that key's position-tag row.
 # ---------------------------------------------------------------------------
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("d,b,hq,hk,sq,sk", [(64, 16, 8, 2, [7, 30, 1], [40, 30, 77]),
                                              (128, 16, 32, 8, [1, 1, 1], [300, 513, 17]),
-                                             (128, 64, 16, 4, [60, 2], [60, 700])])
-def test_position_tags_bit_exact(d, b, hq, hk, sq, sk):
+                                             (128, 64, 16, 4, [60, 2], [60, 700]),
+                                             (256, 32, 4, 4, [33, 1], [90, 2000])])
+def test_position_tags_bit_exact(d, b, hq, hk, sq, sk, path):
     need = sum((k + b - 1) // b for k in sk)
     w = W.build("tags", hq, hk, d, b, sq, sk, need + 7, 1.0, seed=5, values=False, poison=True,
                 bt_pad=2)
@@ -150,7 +168,7 @@ def test_position_tags_bit_exact(d, b, hq, hk, sq, sk):
             kl[s][t, hkv, i % d] = 64.0
     w.q = q.to(torch.bfloat16)
     scatter_logical(w, kl, [position_tags(k, w.hk, w.d) for k in sk])
-    got, err, _ = run_gpu(w)
+    got, err, _ = run_gpu(w, path=path)
     assert err == 0
     want = oracle.forward_workload(w)
     for tok, (s, i, ctx) in enumerate(token_of_row(w)):
@@ -162,10 +180,11 @@ def test_position_tags_bit_exact(d, b, hq, hk, sq, sk):
             assert np.all(row[4:] == 0)
 
 
-def test_block_permutation_bit_identical_on_gpu():
+@pytest.mark.parametrize("path", PATHS)
+def test_block_permutation_bit_identical_on_gpu(path):
     w = W.random_small(300, num_seqs=4, hq=8, hk=2, d=128, b=16, sq=(1, 20), ctx=(0, 400),
                        softcap=30.0, sinks=True)
-    a, err, _ = run_gpu(w)
+    a, err, _ = run_gpu(w, path=path)
     g = torch.Generator().manual_seed(1)
     perm = torch.randperm(w.num_blocks, generator=g)
     k2 = torch.empty_like(w.k_cache)
@@ -176,7 +195,7 @@ def test_block_permutation_bit_identical_on_gpu():
     used = bt >= 0
     bt[used] = perm[bt[used].long()].to(torch.int32)
     w.k_cache, w.v_cache, w.block_table = k2, v2, bt
-    b, err2, _ = run_gpu(w)
+    b, err2, _ = run_gpu(w, path=path)
     assert err == 0 and err2 == 0
     assert torch.equal(a, b)
 
@@ -185,7 +204,8 @@ def test_block_permutation_bit_identical_on_gpu():
 # Hand-derived worked examples (tests/golden) on the GPU.  bf16 output
 # rounding is relative, so the bound scales with |expected|.
 # ---------------------------------------------------------------------------
-def test_golden_examples_on_gpu():
+@pytest.mark.parametrize("path", PATHS)
+def test_golden_examples_on_gpu(path):
     from tests.test_oracle_pins import golden_cases, golden_workload
     for case in golden_cases():
         w, expected = golden_workload(case)
@@ -193,7 +213,7 @@ def test_golden_examples_on_gpu():
             w.sinks = w.sinks.float()
         if w.alibi_slopes is not None:
             w.alibi_slopes = w.alibi_slopes.float()
-        got, err, _ = run_gpu(w)
+        got, err, _ = run_gpu(w, path=path)
         assert err == 0, case["name"]
         tol = MAX_ABS * np.maximum(1.0, np.abs(expected))
         assert np.all(np.abs(got.numpy() - expected) <= tol), case["name"]
@@ -226,7 +246,8 @@ def test_host_contract_violations():
     assert prob.check_device_error() == 0
 
 
-def test_device_reports_bad_block_id_and_short_context():
+@pytest.mark.parametrize("path", PATHS)
+def test_device_reports_bad_block_id_and_short_context(path):
     w = W.random_small(401, num_seqs=3, hq=8, hk=2, d=128, b=16, sq=(1, 1), ctx=(40, 60),
                        poison=False)
     ref = oracle.forward_workload(w)
@@ -235,7 +256,7 @@ def test_device_reports_bad_block_id_and_short_context():
     bad.block_table = w.block_table.clone()
     bad.block_table[1, 0] = w.num_blocks + 5
     wd = bad.to("cuda")
-    prob = ua.Problem.for_workload(wd)
+    prob = ua.Problem.for_workload(wd, path=path)
     out = prob.forward_workload(wd)
     code = prob.check_device_error()
     assert code & ua.UA_DEVERR_BLOCK_ID
