@@ -42,6 +42,7 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 KERNEL_SOURCES = {
     "split_kernel": ["ua_split.cu", "ua_ptx.cuh", "ua_common.cuh"],
     "prefill_kernel": ["ua_prefill.cu", "ua_ptx.cuh", "ua_common.cuh", "ua_tc.cuh"],
+    "decode_tc_kernel": ["ua_decode_tc.cu", "ua_ptx.cuh", "ua_common.cuh", "ua_tc.cuh"],
 }
 
 
@@ -396,7 +397,7 @@ def run_single(args):
     w = W.make(args.workload, device="cuda")
     nbytes, flops = workload_units(w)
     path = {"auto": ua.UA_PATH_AUTO, "split": ua.UA_PATH_SPLIT_KV,
-            "tensor": ua.UA_PATH_TENSOR_CORE}[args.path]
+            "tensor": ua.UA_PATH_TENSOR_CORE, "decode": ua.UA_PATH_DECODE_TC}[args.path]
     r = time_ours(w, args.steps, args.warmup, flush=True, torch=torch, ua=ua, path=path)
     ms = statistics.mean(r["step_ms"])
     km = statistics.mean(r["kernel_ms"])
@@ -470,7 +471,7 @@ def main():
                              "wide_mha_alibi"],
                     help="time only this workload and print its own short JSON line "
                          "(for profiling); the default is the full headline run")
-    ap.add_argument("--path", default="auto", choices=["auto", "split", "tensor"],
+    ap.add_argument("--path", default="auto", choices=["auto", "split", "tensor", "decode"],
                     help="kernel family for --workload (default: the library's choice)")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -85,13 +85,19 @@ enum {
 
 enum { UA_DTYPE_BF16 = 0 };
 
-/* Execution path.  AUTO picks per call (gfx950 spec section 6: a path whose
- * query-tile grid fills the device versus split-KV segments plus a reduction):
- * the CUDA-core split-KV kernel when a KV head has at most 16 packed query rows
- * (decode-like calls), the tensor-core kernel otherwise.  SPLIT_KV and
- * TENSOR_CORE force one family for every call (TENSOR_CORE needs 128 % g == 0;
- * otherwise ua_forward returns UA_ERR_UNSUPPORTED). */
-enum { UA_PATH_AUTO = 0, UA_PATH_SPLIT_KV = 1, UA_PATH_TENSOR_CORE = 2 };
+/* Execution path (gfx950 spec section 6: a path whose query-tile grid fills
+ * the device versus split-KV segments plus a reduction).
+ *   SPLIT_KV     CUDA-core split-KV kernel + combine, any shape.
+ *   TENSOR_CORE  tcgen05 kernel over tiles of 128 packed (position, head)
+ *                rows, KV-split + combine when the tile grid is small;
+ *                needs 128 % g == 0.
+ *   DECODE_TC    tcgen05 kernel with the keys on the MMA M dimension for
+ *                calls with at most 16 packed rows per KV head; needs d = 128,
+ *                16 % g == 0 and g * max_seqlen_q <= 16.
+ *   AUTO         DECODE_TC when it applies, else TENSOR_CORE when it applies
+ *                and a KV head has more than 16 packed rows, else SPLIT_KV.
+ * A forced path that does not apply returns UA_ERR_UNSUPPORTED. */
+enum { UA_PATH_AUTO = 0, UA_PATH_SPLIT_KV = 1, UA_PATH_TENSOR_CORE = 2, UA_PATH_DECODE_TC = 3 };
 
 /*
  * Static description of a problem family (UnifiedAttentionProblem in the

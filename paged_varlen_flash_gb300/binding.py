@@ -29,6 +29,7 @@ UA_DTYPE_BF16 = 0
 UA_PATH_AUTO = 0
 UA_PATH_SPLIT_KV = 1
 UA_PATH_TENSOR_CORE = 2
+UA_PATH_DECODE_TC = 3
 
 _lib = None
 

@@ -13,6 +13,7 @@
 #include <mutex>
 
 #include "ua_common.cuh"
+#include "ua_decode_tc.h"
 #include "ua_prefill.h"
 #include "ua_split.h"
 
@@ -135,7 +136,7 @@ ua_status ua_problem_create(const ua_problem_desc* d, ua_problem** out) {
     if (d->head_size != 64 && d->head_size != 128 && d->head_size != 256) return UA_ERR_UNSUPPORTED;
     if (d->block_size != 16 && d->block_size != 32 && d->block_size != 64) return UA_ERR_UNSUPPORTED;
     if (d->num_blocks > (int64_t(1) << 31) - 1) return UA_ERR_UNSUPPORTED;
-    if (d->path > UA_PATH_TENSOR_CORE) return UA_ERR_INVALID_ARG;
+    if (d->path > UA_PATH_DECODE_TC) return UA_ERR_INVALID_ARG;
 
     ua_problem* p = new (std::nothrow) ua_problem();
     if (!p) return UA_ERR_OUT_OF_MEMORY;
@@ -269,24 +270,60 @@ ua_status ua_forward(ua_problem* p, const void* q, const void* k_cache, const vo
     // ---- path choice ------------------------------------------------------
     const int64_t rows_per_kv = (int64_t)g * max_seqlen_q;
     const bool tc_ok = ua::prefill_shape_ok(fp);
-    bool use_tc = tc_ok && rows_per_kv > 16;
-    if (d.path == UA_PATH_SPLIT_KV) use_tc = false;
+    const bool dec_ok = ua::decode_tc_shape_ok(fp);
+    bool use_dec = dec_ok;
+    bool use_tc = !dec_ok && tc_ok && rows_per_kv > 16;
+    if (d.path == UA_PATH_SPLIT_KV) use_dec = use_tc = false;
     if (d.path == UA_PATH_TENSOR_CORE) {
         if (!tc_ok) return UA_ERR_UNSUPPORTED;
+        use_dec = false;
         use_tc = true;
     }
-    if (use_tc) {
-        ua::PrefillPlan plan;
-        ua::plan_prefill(fp, p->num_sms, p->ws_bytes, &plan);
-        if (p->map_p_rows != plan.kv_box_rows) {
-            if (!encode_cache_map(&p->map_kp, k_cache, d, plan.kv_box_rows) ||
-                !encode_cache_map(&p->map_vp, v_cache, d, plan.kv_box_rows)) {
+    if (d.path == UA_PATH_DECODE_TC) {
+        if (!dec_ok) return UA_ERR_UNSUPPORTED;
+        use_dec = true;
+        use_tc = false;
+    }
+    if (use_dec || use_tc) {
+        // Both tensor-core kernels read the caches through boxes of b slots.
+        if (p->map_p_rows != d.block_size) {
+            if (!encode_cache_map(&p->map_kp, k_cache, d, d.block_size) ||
+                !encode_cache_map(&p->map_vp, v_cache, d, d.block_size)) {
                 std::snprintf(g_cuda_err, sizeof g_cuda_err, "cuTensorMapEncodeTiled failed");
                 p->map_p_rows = 0;
                 return UA_ERR_CUDA;
             }
-            p->map_p_rows = plan.kv_box_rows;
+            p->map_p_rows = d.block_size;
         }
+    }
+    if (use_dec) {
+        ua::DecodePlan plan;
+        ua::plan_decode_tc(fp, p->num_sms, p->ws_bytes, &plan);
+        fp.splits = plan.splits;
+        fp.chunk = plan.chunk;
+        fp.part_o = p->d_ws;
+        fp.part_ml = p->d_ws + (size_t)total_q * d.num_q_heads * plan.splits * d.head_size;
+        prof_mark(p, true, st);
+        cudaError_t e = ua::launch_decode_tc(plan, p->map_kp, p->map_vp, fp, st);
+        prof_mark(p, false, st);
+        if (e != cudaSuccess) {
+            note_cuda(e, "decode kernel launch");
+            return UA_ERR_CUDA;
+        }
+        if (plan.splits > 1) {
+            e = ua::launch_combine(fp, st);
+            if (e != cudaSuccess) {
+                note_cuda(e, "combine kernel launch");
+                return UA_ERR_CUDA;
+            }
+        }
+        p->last_launches = plan.launches;
+        p->last_path = plan.splits > 1 ? "decode_tc+combine" : "decode_tc";
+        return UA_OK;
+    }
+    if (use_tc) {
+        ua::PrefillPlan plan;
+        ua::plan_prefill(fp, p->num_sms, p->ws_bytes, &plan);
         fp.splits = plan.splits;
         fp.chunk = plan.chunk;
         fp.part_o = p->d_ws;

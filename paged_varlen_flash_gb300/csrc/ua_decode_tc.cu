@@ -1,0 +1,593 @@
+// ua_decode_tc.cu -- decode and small-chunk attention on the tcgen05 tensor
+// cores, with the keys on the MMA's M dimension.
+//
+// A decode step has only g * S_q <= 16 packed (position, head) rows per KV
+// head, so the products are laid out transposed:
+//
+//     S^T [128 keys x 16 rows] = K_tile [128 x d]  *  Q^T [d x 16]
+//     O^T [d x 16 rows]       += V_tile^T [d x 128] * P^T [128 x 16]
+//
+// Both are tcgen05.mma kind::f16 with M = 128, N = 16: K and V come straight
+// from their paged TMA tiles (V read MN-major, no transpose copy), Q^T and P^T
+// are 16-row K-major tiles in shared memory, S^T and O^T accumulate in tensor
+// memory (64 columns).  Tensor-memory lane = key for S^T and lane = head-dim
+// element for O^T, so each softmax thread owns one key of the tile; the
+// per-row maxima are reduced across the 128 keys with warp shuffles plus one
+// shared-memory exchange per tile.  The math is the same streaming (m, l, o)
+// recurrence in base 2 with the lazy re-anchor (gfx1151 ALGORITHM.md section
+// 3; gfx950 "Unified paged attention on gfx950, from the math up", section 2;
+// attention_dense.py lazy_rescale), split into KV segments whose partials the
+// combine kernel merges (gfx950 section 5).
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+
+#include "ua_common.cuh"
+#include "ua_decode_tc.h"
+#include "ua_ptx.cuh"
+#include "ua_tc.cuh"
+#include "ua_tmap.h"
+
+namespace ua {
+namespace {
+
+constexpr int kN = 16;          // packed rows per tile (MMA N)
+constexpr int kBN = 128;        // keys per KV tile (MMA M of S^T)
+constexpr int kD = 128;         // head size served by this kernel (MMA M of O^T)
+constexpr int kThreadsD = 192;  // 4 softmax warps, 1 TMA warp, 1 MMA warp
+constexpr int kWarpTmaD = 4;
+constexpr int kWarpMmaD = 5;
+constexpr uint32_t kTmemColsD = 64;
+constexpr float kLazyD = 8.0f;
+
+template <int NS>
+struct DCfg {
+    static constexpr int kPanels = kD / 64;
+    static constexpr int kQPanel = kN * 128;              // 16 rows x 64 dims
+    static constexpr int kQBytes = kPanels * kQPanel;
+    static constexpr int kKvPanel = kBN * 128;            // 128 keys x 64 dims
+    static constexpr int kKvBytes = kPanels * kKvPanel;
+    static constexpr int kPPanel = kN * 128;              // 16 rows x 64 keys
+    static constexpr int kPBuf = (kBN / 64) * kPPanel;    // one P^T tile
+    static constexpr int kOffQ = 0;
+    static constexpr int kOffK = 8192;
+    static constexpr int kOffV = kOffK + NS * kKvBytes;
+    static constexpr int kOffP = kOffV + NS * kKvBytes;   // two P^T buffers
+    static constexpr int kOffBar = kOffP + 2 * kPBuf;
+    // q_full, k_full[NS], v_full[NS], k_empty[NS], v_empty[NS], s_full[2],
+    // p_full[2], o_done[2], drain
+    static constexpr int kNumBars = 1 + 4 * NS + 7;
+    static constexpr int kOffRed = kOffBar + kNumBars * 8;    // maxima [2][4][16] fp32
+    static constexpr int kOffSum = kOffRed + 2 * 4 * kN * 4;  // row sums [4][16] fp32
+    static constexpr int kOffMisc = kOffSum + 4 * kN * 4;
+    static constexpr int kSmem = kOffMisc + 16 + 1024;
+    static constexpr int kTmemS = 0;    // S^T buffers: columns [0, 16) and [16, 32)
+    static constexpr int kTmemO = 32;   // O^T: columns [32, 48)
+    static_assert(kQBytes <= kOffK, "Q tile");
+    static_assert(kSmem <= 232448, "shared memory budget");
+};
+
+__device__ __forceinline__ bool dwait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                      int32_t* err) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t start = global_ns();
+    for (;;) {
+        for (int i = 0; i < 128; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (global_ns() - start > kWaitLimitNs) {
+            *abort_flag = 1;
+            atomicOr(err, (int)UA_DEVERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ bool dbar_and(int id, int count, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "barrier.cta.red.and.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
+
+__device__ __forceinline__ void ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+}
+
+__device__ __forceinline__ void st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15])
+        : "memory");
+}
+
+__device__ __forceinline__ float tanh_e2(float x) {
+    // tanh(x) = 1 - 2 / (e^{2x} + 1)
+    const float e = fast_exp2(x * (2.0f * kLog2e));
+    return 1.0f - __fdividef(2.0f, e + 1.0f);
+}
+
+template <int NS, bool PLAIN>
+__global__ void __launch_bounds__(kThreadsD, 1)
+decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                 const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+    using C = DCfg<NS>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int s = blockIdx.z;
+    const int hkv = blockIdx.y;
+    const int seg = blockIdx.x;
+    const bool split = p.splits > 1;
+    const int g = p.g;
+
+    int sq, sk;
+    int64_t q0;
+    const uint32_t st = seq_status(p, s, sq, sk, q0);
+    if (st && hkv == 0 && seg == 0 && threadIdx.x == 0) atomicOr(p.err, (int)st);
+    if (st & UA_DEVERR_CU_SEQLENS) return;
+    const int nrows = min(g * sq, kN);   // the planner guarantees g * S_q <= 16
+    if (nrows <= 0) return;
+    if (seg >= (split ? seq_segments(p, st, sk) : 1)) return;
+    const int ctx = sk - sq;
+    const bool causal = (p.flags & UA_FLAG_CAUSAL) != 0;
+    const bool window = (p.flags & UA_FLAG_WINDOW) != 0;
+    int k_end = causal ? min(sk, sq - 1 + ctx + 1) : sk;
+    int k_beg = window ? max(0, ctx - p.window + 1) : 0;
+    if (split) {
+        k_beg = max(k_beg, seg * p.chunk);
+        k_end = min(k_end, seg * p.chunk + p.chunk);
+    }
+    if (st || k_beg >= k_end) {
+        // Malformed lengths (rows written as zeros) or a segment no row sees
+        // (an empty partial, m = -inf).
+        for (int e = threadIdx.x; e < nrows * kD; e += kThreadsD) {
+            const int r = e / kD, c = e % kD;
+            const int64_t row = (q0 + r / g) * p.hq + hkv * g + r % g;
+            if (split) {
+                if (c == 0) {
+                    p.part_ml[(row * p.splits + seg) * 2 + 0] = -INFINITY;
+                    p.part_ml[(row * p.splits + seg) * 2 + 1] = 0.f;
+                }
+            } else {
+                p.out[row * kD + c] = __float2bfloat16_rn(0.f);
+            }
+        }
+        return;
+    }
+    const int t_begin = k_beg / kBN;
+    const int n_tiles = (k_end + kBN - 1) / kBN - t_begin;
+
+    uint64_t* bm = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+    const uint32_t q_full = smem_u32(&bm[0]);
+    const uint32_t k_full0 = smem_u32(&bm[1]);
+    const uint32_t v_full0 = smem_u32(&bm[1 + NS]);
+    const uint32_t k_empty0 = smem_u32(&bm[1 + 2 * NS]);
+    const uint32_t v_empty0 = smem_u32(&bm[1 + 3 * NS]);
+    const uint32_t s_full0 = smem_u32(&bm[1 + 4 * NS]);
+    const uint32_t p_full0 = smem_u32(&bm[3 + 4 * NS]);
+    const uint32_t o_done0 = smem_u32(&bm[5 + 4 * NS]);
+    const uint32_t drain = smem_u32(&bm[7 + 4 * NS]);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
+    float* red = reinterpret_cast<float*>(smem + C::kOffRed);
+    float* lsum = reinterpret_cast<float*>(smem + C::kOffSum);
+
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        for (int i = 0; i < NS; ++i) {
+            mbar_init(k_full0 + 8 * i, 1);
+            mbar_init(v_full0 + 8 * i, 1);
+            mbar_init(k_empty0 + 8 * i, 1);
+            mbar_init(v_empty0 + 8 * i, 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(s_full0 + 8 * i, 1);
+            mbar_init(p_full0 + 8 * i, 128);
+            mbar_init(o_done0 + 8 * i, 1);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == kWarpMmaD) {
+        tc::tmem_alloc(smem_u32(tmem_slot), kTmemColsD);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t sQ = smem_u32(smem + C::kOffQ);
+    const uint32_t sK = smem_u32(smem + C::kOffK);
+    const uint32_t sV = smem_u32(smem + C::kOffV);
+    const uint32_t sP = smem_u32(smem + C::kOffP);
+
+    if (warp == kWarpTmaD) {
+        // ------------------------------ TMA producer ------------------------------
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_q);
+            tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_v);
+            mbar_arrive_expect_tx(q_full, C::kQBytes);
+#pragma unroll
+            for (int pn = 0; pn < C::kPanels; ++pn)
+                tma_load_3d(sQ + pn * C::kQPanel, &tm_q, pn * 64, hkv * g, (int)q0, q_full);
+            const int b = p.b;
+            const int nblk_seq = (sk + b - 1) / b;
+            const int32_t* bt = p.block_table + (int64_t)s * p.bt_stride;
+            for (int j = 0; j < n_tiles; ++j) {
+                const int stg = j % NS;
+                const int key0 = (t_begin + j) * kBN;
+                const int blk0 = key0 / b;
+                const int nb = min(kBN / b, nblk_seq - blk0);
+                const uint32_t bytes = (uint32_t)nb * b * 128 * C::kPanels;
+                if (j >= NS && !dwait(k_empty0 + 8 * stg, ((j / NS) + 1) & 1, abort_flag, p.err)) break;
+                mbar_arrive_expect_tx(k_full0 + 8 * stg, bytes);
+                for (int bi = 0; bi < nb; ++bi) {
+                    const int32_t id = __ldg(bt + blk0 + bi);
+                    if (id < 0 || (int64_t)id >= p.num_blocks) atomicOr(p.err, (int)UA_DEVERR_BLOCK_ID);
+#pragma unroll
+                    for (int pn = 0; pn < C::kPanels; ++pn)
+                        tma_load_4d(sK + stg * C::kKvBytes + pn * C::kKvPanel + bi * b * 128, &tm_k,
+                                    pn * 64, hkv, 0, id, k_full0 + 8 * stg);
+                }
+                if (j >= NS && !dwait(v_empty0 + 8 * stg, ((j / NS) + 1) & 1, abort_flag, p.err)) break;
+                mbar_arrive_expect_tx(v_full0 + 8 * stg, bytes);
+                for (int bi = 0; bi < nb; ++bi) {
+                    const int32_t id = __ldg(bt + blk0 + bi);
+#pragma unroll
+                    for (int pn = 0; pn < C::kPanels; ++pn)
+                        tma_load_4d(sV + stg * C::kKvBytes + pn * C::kKvPanel + bi * b * 128, &tm_v,
+                                    pn * 64, hkv, 0, id, v_full0 + 8 * stg);
+                }
+            }
+            if (*abort_flag) {
+                // Let every copy this thread issued land before the CTA ends.
+                for (int j = max(0, n_tiles - NS); j < n_tiles; ++j) {
+                    mbar_wait_bounded(k_full0 + 8 * (j % NS), (j / NS) & 1);
+                    mbar_wait_bounded(v_full0 + 8 * (j % NS), (j / NS) & 1);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == kWarpMmaD) {
+        // ------------------------------ MMA issuer --------------------------------
+        constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(kBN, kN, false, false);
+        constexpr uint32_t idesc_pv = tc::idesc_bf16_f32(kD, kN, true, false);
+        auto wwait = [&](uint32_t bar, uint32_t par) {
+            return __all_sync(0xffffffffu, dwait(bar, par, abort_flag, p.err));
+        };
+        auto issue_qk = [&](int j) {
+            const int stg = j % NS;
+            const uint32_t kst = sK + stg * C::kKvBytes;
+            const uint32_t dS = tmem + C::kTmemS + (j & 1) * kN;
+#pragma unroll
+            for (int k = 0; k < kD / 16; ++k) {
+                const int pn = k >> 2, off = (k & 3) * 32;
+                const uint64_t a = tc::smem_desc_sw128(kst + pn * C::kKvPanel + off, 16, 1024);
+                const uint64_t bq = tc::smem_desc_sw128(sQ + pn * C::kQPanel + off, 16, 1024);
+                tc::mma_bf16(dS, a, bq, idesc_qk, k > 0 ? 1u : 0u);
+            }
+            tc::commit(s_full0 + 8 * (j & 1));
+            tc::commit(k_empty0 + 8 * stg);
+        };
+        bool ok = wwait(q_full, 0) && wwait(k_full0, 0);
+        if (ok) {
+            tc::fence_after_sync();
+            if (lane == 0) issue_qk(0);
+            __syncwarp();
+        }
+        for (int j = 0; ok && j < n_tiles; ++j) {
+            if (j + 1 < n_tiles) {
+                if (!wwait(k_full0 + 8 * ((j + 1) % NS), ((j + 1) / NS) & 1)) break;
+                tc::fence_after_sync();
+                if (lane == 0) issue_qk(j + 1);
+                __syncwarp();
+            }
+            const int stg = j % NS;
+            if (!wwait(p_full0 + 8 * (j & 1), (j >> 1) & 1)) break;
+            if (!wwait(v_full0 + 8 * stg, (j / NS) & 1)) break;
+            tc::fence_after_sync();
+            const int key0 = (t_begin + j) * kBN;
+            const int nvalid = min(kBN, sk - key0);
+            if (nvalid < kBN) {
+                // Keys past S_k: their V rows become zeros so that whatever
+                // the slots hold cannot reach O (0 * NaN is NaN).
+                uint8_t* vgen = smem + C::kOffV + stg * C::kKvBytes;
+                const int per_panel = (kBN - nvalid) * 8;
+                for (int e = lane; e < per_panel * C::kPanels; e += 32) {
+                    const int pn = e / per_panel, rem = e % per_panel;
+                    *reinterpret_cast<uint4*>(vgen + pn * C::kKvPanel + (nvalid + rem / 8) * 128 +
+                                              (rem % 8) * 16) = make_uint4(0, 0, 0, 0);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+            }
+            if (lane == 0) {
+                const uint32_t vst = sV + stg * C::kKvBytes;
+                const uint32_t pbuf = sP + (j & 1) * C::kPBuf;
+#pragma unroll
+                for (int kk = 0; kk < kBN / 16; ++kk) {
+                    const uint64_t a = tc::smem_desc_sw128(vst + kk * 16 * 128, C::kKvPanel, 1024);
+                    const uint64_t bp =
+                        tc::smem_desc_sw128(pbuf + (kk >> 2) * C::kPPanel + (kk & 3) * 32, 16, 1024);
+                    tc::mma_bf16(tmem + C::kTmemO, a, bp, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+                }
+                tc::commit(o_done0 + 8 * (j & 1));
+                tc::commit(v_empty0 + 8 * stg);
+            }
+            __syncwarp();
+        }
+        if (*abort_flag) {
+            // No MMA of this CTA may still run when the tensor memory is freed.
+            if (lane == 0) tc::commit(drain);
+            __syncwarp();
+            mbar_wait_bounded(drain, 0);
+        }
+    } else {
+        // --------------------------- softmax warps 0-3 ----------------------------
+        // Thread t: key t of each KV tile (S^T lane t) and head-dim element t of
+        // the output (O^T lane t).
+        const int t = threadIdx.x;
+        const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
+        const bool softcap = (p.flags & UA_FLAG_SOFTCAP) != 0;
+        const bool alibi = (p.flags & UA_FLAG_ALIBI) != 0;
+        const float sl2 = p.scale * kLog2e;
+        float m[kN], l[kN];
+#pragma unroll
+        for (int r = 0; r < kN; ++r) {
+            m[r] = -INFINITY;
+            l[r] = 0.f;
+        }
+        bool ok = true;
+        for (int j = 0; j < n_tiles; ++j) {
+            const bool got = __all_sync(0xffffffffu, dwait(s_full0 + 8 * (j & 1), (j >> 1) & 1,
+                                                           abort_flag, p.err));
+            const int key = (t_begin + j) * kBN + t;
+            float x[kN];
+            if (got) {
+                tc::fence_after_sync();
+                uint32_t sv[kN];
+                ld16(tl + C::kTmemS + (j & 1) * kN, sv);
+                tc::wait_ld();
+#pragma unroll
+                for (int r = 0; r < kN; ++r) {
+                    const int i = r / g;
+                    const int hi = causal ? min(i + ctx, sk - 1) : sk - 1;
+                    const int lo = window ? max(0, i + ctx - p.window + 1) : 0;
+                    float v;
+                    if constexpr (PLAIN) {
+                        v = __uint_as_float(sv[r]) * sl2;
+                    } else {
+                        float tt = __uint_as_float(sv[r]) * p.scale;
+                        if (softcap) tt = p.softcap * tanh_e2(tt / p.softcap);
+                        if (alibi) tt += __ldg(p.alibi + hkv * g + r % g) * (float)(key - ctx);
+                        v = tt * kLog2e;
+                    }
+                    x[r] = (r < nrows && key >= lo && key <= hi) ? v : -INFINITY;
+                }
+            } else {
+#pragma unroll
+                for (int r = 0; r < kN; ++r) x[r] = -INFINITY;
+            }
+            // Per-row maxima over this warp's 32 keys, then over the 4 warps.
+#pragma unroll
+            for (int r = 0; r < kN; ++r) {
+                if (r < nrows) {
+                    float w = x[r];
+                    w = fmaxf(w, __shfl_xor_sync(0xffffffffu, w, 1));
+                    w = fmaxf(w, __shfl_xor_sync(0xffffffffu, w, 2));
+                    w = fmaxf(w, __shfl_xor_sync(0xffffffffu, w, 4));
+                    w = fmaxf(w, __shfl_xor_sync(0xffffffffu, w, 8));
+                    w = fmaxf(w, __shfl_xor_sync(0xffffffffu, w, 16));
+                    if (lane == 0) red[((j & 1) * 4 + warp) * kN + r] = w;
+                }
+            }
+            if (!dbar_and(1, 128, got)) {
+                ok = false;
+                break;
+            }
+            float alpha[kN];
+            bool any_re = false;
+#pragma unroll
+            for (int r = 0; r < kN; ++r) {
+                alpha[r] = 1.f;
+                if (r < nrows) {
+                    const float* rr = red + (j & 1) * 4 * kN + r;
+                    const float tmax = fmaxf(fmaxf(rr[0], rr[kN]), fmaxf(rr[2 * kN], rr[3 * kN]));
+                    // Lazy re-anchor: only when the tile max exceeds m by > 8 (log2).
+                    if (tmax > m[r] + kLazyD) {
+                        alpha[r] = fast_exp2(m[r] - tmax);
+                        m[r] = tmax;
+                        any_re = true;
+                    }
+                }
+            }
+            // p = 2^(x - m) on the fp16x2 special-function path; per-thread
+            // partial row sums stay fp32.
+            uint32_t pb[kN / 2];
+#pragma unroll
+            for (int r = 0; r < kN; r += 2) {
+                const float a0 = x[r] - (m[r] == -INFINITY ? 0.f : m[r]);
+                const float a1 = x[r + 1] - (m[r + 1] == -INFINITY ? 0.f : m[r + 1]);
+                uint32_t h, e;
+                asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(a1), "f"(a0));
+                asm("ex2.approx.f16x2 %0, %1;" : "=r"(e) : "r"(h));
+                float p0, p1;
+                asm("{\n\t.reg .f16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\tcvt.f32.f16 %0, lo;\n\t"
+                    "cvt.f32.f16 %1, hi;\n\t}"
+                    : "=f"(p0), "=f"(p1)
+                    : "r"(e));
+                l[r] = l[r] * alpha[r] + p0;
+                l[r + 1] = l[r + 1] * alpha[r + 1] + p1;
+                pb[r / 2] = pack_bf16x2(p0, p1);
+            }
+            // P^T buffer (j & 1) was read by the P.V of tile j - 2; rescaling O
+            // needs the P.V of tile j - 1.
+            bool go = true;
+            if (j >= 2)
+                go = __all_sync(0xffffffffu, dwait(o_done0 + 8 * (j & 1), ((j - 2) >> 1) & 1,
+                                                   abort_flag, p.err));
+            if (go && any_re && j > 0) {
+                go = __all_sync(0xffffffffu, dwait(o_done0 + 8 * ((j - 1) & 1), ((j - 1) >> 1) & 1,
+                                                   abort_flag, p.err));
+                if (go) {
+                    tc::fence_after_sync();
+                    uint32_t o[kN];
+                    ld16(tl + C::kTmemO, o);
+                    tc::wait_ld();
+#pragma unroll
+                    for (int r = 0; r < kN; ++r) o[r] = __float_as_uint(__uint_as_float(o[r]) * alpha[r]);
+                    st16(tl + C::kTmemO, o);
+                    tc::wait_st();
+                }
+            }
+            if (go) {
+                // P^T row r, key t: K-major [16 rows][128 keys] in two 64-key
+                // 128-byte-swizzled panels.
+                uint8_t* pbase = smem + C::kOffP + (j & 1) * C::kPBuf + (t >> 6) * C::kPPanel;
+                const int kin = t & 63;
+#pragma unroll
+                for (int r = 0; r < kN; ++r) {
+                    const uint16_t v = (r & 1) ? (uint16_t)(pb[r / 2] >> 16) : (uint16_t)(pb[r / 2] & 0xffffu);
+                    *reinterpret_cast<uint16_t*>(pbase + r * 128 + (((kin >> 3) ^ (r & 7)) << 4) +
+                                                 (kin & 7) * 2) = v;
+                }
+                fence_proxy_async_smem();
+                tc::fence_before_sync();
+                mbar_arrive(p_full0 + 8 * (j & 1));
+            }
+        }
+        // ------------------------------ epilogue ---------------------------------
+        if (ok) {
+            const bool done = __all_sync(0xffffffffu,
+                                         dwait(o_done0 + 8 * ((n_tiles - 1) & 1),
+                                               ((n_tiles - 1) >> 1) & 1, abort_flag, p.err));
+            // Row sums over the 128 keys: warp shuffles, then the 4 warps.
+#pragma unroll
+            for (int r = 0; r < kN; ++r) {
+                if (r < nrows) {
+                    float w = l[r];
+                    w += __shfl_xor_sync(0xffffffffu, w, 1);
+                    w += __shfl_xor_sync(0xffffffffu, w, 2);
+                    w += __shfl_xor_sync(0xffffffffu, w, 4);
+                    w += __shfl_xor_sync(0xffffffffu, w, 8);
+                    w += __shfl_xor_sync(0xffffffffu, w, 16);
+                    if (lane == 0) lsum[warp * kN + r] = w;
+                }
+            }
+            if (dbar_and(1, 128, done)) {
+                tc::fence_after_sync();
+                uint32_t o[kN];
+                ld16(tl + C::kTmemO, o);
+                tc::wait_ld();
+#pragma unroll
+                for (int r = 0; r < kN; ++r) {
+                    if (r >= nrows) continue;
+                    const float L0 = lsum[r] + lsum[kN + r] + lsum[2 * kN + r] + lsum[3 * kN + r];
+                    const int64_t row = (q0 + r / g) * p.hq + hkv * g + r % g;
+                    const float ov = __uint_as_float(o[r]);
+                    if (split) {
+                        p.part_o[(row * p.splits + seg) * kD + t] = ov;
+                        if (t == 0) {
+                            p.part_ml[(row * p.splits + seg) * 2 + 0] = m[r];
+                            p.part_ml[(row * p.splits + seg) * 2 + 1] = L0;
+                        }
+                    } else {
+                        float num = 1.f, L = L0;
+                        bool zero = false;
+                        if (p.flags & UA_FLAG_SINKS) {
+                            const float s2 = __ldg(p.sinks + hkv * g + r % g) * kLog2e;
+                            if (s2 == INFINITY) {
+                                zero = true;
+                            } else if (s2 > m[r]) {
+                                const float a = (m[r] == -INFINITY) ? 0.f : fast_exp2(m[r] - s2);
+                                num = a;
+                                L = L * a + 1.0f;
+                            } else if (s2 != -INFINITY) {
+                                L += fast_exp2(s2 - m[r]);
+                            }
+                        }
+                        const float inv = (!zero && L > 0.f) ? num * __frcp_rn(L) : 0.f;
+                        p.out[row * kD + t] = __float2bfloat16_rn(ov * inv);
+                    }
+                }
+            }
+        }
+    }
+
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == kWarpMmaD) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, kTmemColsD);
+    }
+}
+
+}  // namespace
+
+bool decode_tc_shape_ok(const FwdParams& p) {
+    return p.d == kD && p.g >= 1 && p.g <= kN && (kN % p.g) == 0 &&
+           (int64_t)p.g * p.max_seqlen_q <= kN;
+}
+
+void plan_decode_tc(const FwdParams& p, int num_sms, size_t workspace_bytes, DecodePlan* plan) {
+    *plan = DecodePlan();
+    plan->kv_box_rows = p.b;
+    // Segments of whole 128-key tiles, at least 8 tiles each, aiming at about
+    // four CTAs per SM.
+    const int64_t base = (int64_t)p.hk * p.num_seqs;
+    const int64_t want = (4LL * num_sms + base - 1) / base;
+    const int64_t by_len = std::max<int64_t>(1, p.max_seqlen_k / (8 * kBN));
+    int splits = (int)std::min<int64_t>(std::min<int64_t>(want, by_len), 64);
+    const size_t per_split = (size_t)p.total_q * p.hq * (p.d + 2) * sizeof(float);
+    splits = (int)std::min<size_t>((size_t)splits, per_split ? workspace_bytes / per_split : 1);
+    if (splits < 1) splits = 1;
+    if (splits > 1) {
+        const int per = (p.max_seqlen_k + splits - 1) / splits;
+        plan->chunk = (per + kBN - 1) / kBN * kBN;
+        splits = (p.max_seqlen_k + plan->chunk - 1) / plan->chunk;
+    }
+    plan->splits = splits;
+    plan->launches = splits > 1 ? 2 : 1;
+}
+
+cudaError_t launch_decode_tc(const DecodePlan& plan, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                             const FwdParams& p, cudaStream_t stream) {
+    // Q map: [total_q, H_q, d]; box = 64 dims x g heads x 16/g positions = 16 rows.
+    CUtensorMap tq;
+    cuuint64_t dims[3] = {(cuuint64_t)p.d, (cuuint64_t)p.hq, (cuuint64_t)p.total_q};
+    cuuint64_t strides[2] = {2ull * p.d, 2ull * p.d * p.hq};
+    cuuint32_t box[3] = {64, (cuuint32_t)p.g, (cuuint32_t)(kN / p.g)};
+    if (!encode_bf16_sw128(&tq, p.q, 3, dims, strides, box)) return cudaErrorInvalidValue;
+    constexpr int NS = 3;
+    using C = DCfg<NS>;
+    const bool plain = (p.flags & (UA_FLAG_SOFTCAP | UA_FLAG_ALIBI)) == 0;
+    auto kern = plain ? decode_tc_kernel<NS, true> : decode_tc_kernel<NS, false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    if (e != cudaSuccess) return e;
+    dim3 grid((unsigned)plan.splits, (unsigned)p.hk, (unsigned)p.num_seqs);
+    kern<<<grid, kThreadsD, C::kSmem, stream>>>(tq, tm_k, tm_v, p);
+    return cudaGetLastError();
+}
+
+}  // namespace ua

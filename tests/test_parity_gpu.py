@@ -29,17 +29,24 @@ def _built():
     ua.load_library()
 
 
-# Both kernel families are checked on every shape they can serve.
-PATHS = [ua.UA_PATH_SPLIT_KV, ua.UA_PATH_TENSOR_CORE]
+# Every kernel family is checked on every shape it can serve.
+PATHS = [ua.UA_PATH_SPLIT_KV, ua.UA_PATH_TENSOR_CORE, ua.UA_PATH_DECODE_TC]
 
 
 def tc_ok(w):
     return 128 % (w.hq // w.hk) == 0
 
 
+def dec_ok(w):
+    g = w.hq // w.hk
+    return w.d == 128 and 16 % g == 0 and g * w.max_seqlen_q <= 16
+
+
 def run_gpu(w, problem=None, out=None, path=ua.UA_PATH_AUTO):
     if path == ua.UA_PATH_TENSOR_CORE and not tc_ok(w):
         pytest.skip("g does not divide the 128-row tile")
+    if path == ua.UA_PATH_DECODE_TC and not dec_ok(w):
+        pytest.skip("not a decode-shaped call for the transposed kernel")
     wd = w.to("cuda")
     prob = problem or ua.Problem.for_workload(wd, path=path)
     res = prob.forward_workload(wd, out=out)
@@ -114,6 +121,8 @@ def test_tiny_config_full(path):
 def test_config_sampled_rows(name, path):
     if path == ua.UA_PATH_SPLIT_KV and name in ("long_prefill", "wide_mha_alibi"):
         pytest.skip("CUDA-core path on 2 TFLOP workloads: covered by the smaller prefill shapes")
+    if path == ua.UA_PATH_DECODE_TC and name != "decode":
+        pytest.skip("not a decode-shaped workload")
     w = W.make(name, device="cuda", poison=(name != "long_prefill"))
     prob = ua.Problem.for_workload(w, path=path)
     out = prob.forward_workload(w)
