@@ -296,46 +296,76 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             if (lane == 0) issue_qk(0);
             __syncwarp();
         }
-        for (int j = 0; ok && j < n_tiles; ++j) {
-            if (j + 1 < n_tiles) {
-                if (!wwait(k_full0 + 8 * ((j + 1) % NS), ((j + 1) / NS) & 1)) break;
+        // Event loop: issue QK^T(nq) as soon as its K tile has landed and
+        // P.V(np) as soon as P and V are ready, whichever comes first, so a
+        // late K tile never holds back the P.V that frees a V stage.  QK^T(j)
+        // reuses the S^T buffer of tile j - 2, which the softmax released
+        // before P.V(j - 2) was issued (hence nq <= np + 1).
+        int nq = 1, np = 0;
+        uint64_t idle_since = 0;
+        while (ok && np < n_tiles) {
+            bool progressed = false;
+            if (nq < n_tiles && nq <= np + 1 &&
+                __all_sync(0xffffffffu, mbar_try_wait(k_full0 + 8 * (nq % NS), (nq / NS) & 1))) {
                 tc::fence_after_sync();
-                if (lane == 0) issue_qk(j + 1);
+                if (lane == 0) issue_qk(nq);
                 __syncwarp();
+                ++nq;
+                progressed = true;
             }
-            const int stg = j % NS;
-            if (!wwait(p_full0 + 8 * (j & 1), (j >> 1) & 1)) break;
-            if (!wwait(v_full0 + 8 * stg, (j / NS) & 1)) break;
-            tc::fence_after_sync();
-            const int key0 = (t_begin + j) * kBN;
-            const int nvalid = min(kBN, sk - key0);
-            if (nvalid < kBN) {
-                // Keys past S_k: their V rows become zeros so that whatever
-                // the slots hold cannot reach O (0 * NaN is NaN).
-                uint8_t* vgen = smem + C::kOffV + stg * C::kKvBytes;
-                const int per_panel = (kBN - nvalid) * 8;
-                for (int e = lane; e < per_panel * C::kPanels; e += 32) {
-                    const int pn = e / per_panel, rem = e % per_panel;
-                    *reinterpret_cast<uint4*>(vgen + pn * C::kKvPanel + (nvalid + rem / 8) * 128 +
-                                              (rem % 8) * 16) = make_uint4(0, 0, 0, 0);
+            const int stg = np % NS;
+            if (np < nq &&
+                __all_sync(0xffffffffu, mbar_try_wait(p_full0 + 8 * (np & 1), (np >> 1) & 1) &&
+                                            mbar_try_wait(v_full0 + 8 * stg, (np / NS) & 1))) {
+                tc::fence_after_sync();
+                const int key0 = (t_begin + np) * kBN;
+                const int nvalid = min(kBN, sk - key0);
+                if (nvalid < kBN) {
+                    // Keys past S_k: their V rows become zeros so that whatever
+                    // the slots hold cannot reach O (0 * NaN is NaN).
+                    uint8_t* vgen = smem + C::kOffV + stg * C::kKvBytes;
+                    const int per_panel = (kBN - nvalid) * 8;
+                    for (int e = lane; e < per_panel * C::kPanels; e += 32) {
+                        const int pn = e / per_panel, rem = e % per_panel;
+                        *reinterpret_cast<uint4*>(vgen + pn * C::kKvPanel + (nvalid + rem / 8) * 128 +
+                                                  (rem % 8) * 16) = make_uint4(0, 0, 0, 0);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
                 }
-                fence_proxy_async_smem();
-                __syncwarp();
-            }
-            if (lane == 0) {
-                const uint32_t vst = sV + stg * C::kKvBytes;
-                const uint32_t pbuf = sP + (j & 1) * C::kPBuf;
+                if (lane == 0) {
+                    const uint32_t vst = sV + stg * C::kKvBytes;
+                    const uint32_t pbuf = sP + (np & 1) * C::kPBuf;
 #pragma unroll
-                for (int kk = 0; kk < kBN / 16; ++kk) {
-                    const uint64_t a = tc::smem_desc_sw128(vst + kk * 16 * 128, C::kKvPanel, 1024);
-                    const uint64_t bp =
-                        tc::smem_desc_sw128(pbuf + (kk >> 2) * C::kPPanel + (kk & 3) * 32, 16, 1024);
-                    tc::mma_bf16(tmem + C::kTmemO, a, bp, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < kBN / 16; ++kk) {
+                        const uint64_t a = tc::smem_desc_sw128(vst + kk * 16 * 128, C::kKvPanel, 1024);
+                        const uint64_t bp =
+                            tc::smem_desc_sw128(pbuf + (kk >> 2) * C::kPPanel + (kk & 3) * 32, 16, 1024);
+                        tc::mma_bf16(tmem + C::kTmemO, a, bp, idesc_pv, (np > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    tc::commit(o_done0 + 8 * (np & 1));
+                    tc::commit(v_empty0 + 8 * stg);
                 }
-                tc::commit(o_done0 + 8 * (j & 1));
-                tc::commit(v_empty0 + 8 * stg);
+                __syncwarp();
+                ++np;
+                progressed = true;
             }
-            __syncwarp();
+            if (progressed) {
+                idle_since = 0;
+            } else {
+                if (*abort_flag) break;
+                const uint64_t now = global_ns();
+                if (idle_since == 0) {
+                    idle_since = now;
+                } else if (now - idle_since > kWaitLimitNs) {
+                    if (lane == 0) {
+                        *abort_flag = 1;
+                        atomicOr(p.err, (int)UA_DEVERR_TIMEOUT);
+                    }
+                    __syncwarp();
+                    break;
+                }
+            }
         }
         if (*abort_flag) {
             // No MMA of this CTA may still run when the tensor memory is freed.

@@ -352,51 +352,76 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             if (lane == 0) issue_qk(0);
             __syncwarp();
         }
-        for (int j = 0; ok && j < n_tiles; ++j) {
-            if (j + 1 < n_tiles) {
-                const int st1 = (j + 1) % NS;
-                if (!wwait(B.k_full0 + 8 * st1, ((j + 1) / NS) & 1)) break;
+        // Event loop: issue QK^T(nq) as soon as its K tile has landed and
+        // P.V(np) as soon as P and V are ready, whichever comes first, so a
+        // late K tile never holds back the P.V that frees a V stage.  QK^T(j)
+        // reuses the S buffer of tile j - 2, which the softmax released before
+        // P.V(j - 2) was issued (hence nq <= np + 1).
+        int nq = 1, np = 0;
+        uint64_t idle_since = 0;
+        while (ok && np < n_tiles) {
+            bool progressed = false;
+            if (nq < n_tiles && nq <= np + 1 &&
+                __all_sync(0xffffffffu, mbar_try_wait(B.k_full0 + 8 * (nq % NS), (nq / NS) & 1))) {
                 tc::fence_after_sync();
-                if (lane == 0) issue_qk(j + 1);
+                if (lane == 0) issue_qk(nq);
                 __syncwarp();
+                ++nq;
+                progressed = true;
             }
-            const int stg = j % NS;
-            if (!wwait(B.p_full + 8 * (j & 1), (j >> 1) & 1)) break;
-            if (!wwait(B.v_full0 + 8 * stg, (j / NS) & 1)) break;
-            tc::fence_after_sync();
-            const uint32_t vst = sV + stg * C::kKvBytes;
-            const int key0 = (t_begin + j) * BN;
-            const int nvalid = min(BN, sk - key0);
-            if (nvalid < BN) {
-                // Keys past S_k: whatever those slots hold must not reach O
-                // (0 * NaN is NaN), so their V rows become zeros.
-                uint8_t* vgen = smem + C::kOffV + stg * C::kKvBytes;
-                const int nbytes_row = 128;
-                for (int e = lane; e < (BN - nvalid) * C::kPanels * (nbytes_row / 16); e += 32) {
-                    const int per_panel = (BN - nvalid) * (nbytes_row / 16);
-                    const int pn = e / per_panel;
-                    const int rem = e % per_panel;
-                    const int row = nvalid + rem / (nbytes_row / 16);
-                    const int ch = rem % (nbytes_row / 16);
-                    *reinterpret_cast<uint4*>(vgen + pn * C::kKvPanel + row * 128 + ch * 16) =
-                        make_uint4(0, 0, 0, 0);
+            const int stg = np % NS;
+            if (np < nq &&
+                __all_sync(0xffffffffu, mbar_try_wait(B.p_full + 8 * (np & 1), (np >> 1) & 1) &&
+                                            mbar_try_wait(B.v_full0 + 8 * stg, (np / NS) & 1))) {
+                tc::fence_after_sync();
+                const uint32_t vst = sV + stg * C::kKvBytes;
+                const int key0 = (t_begin + np) * BN;
+                const int nvalid = min(BN, sk - key0);
+                if (nvalid < BN) {
+                    // Keys past S_k: whatever those slots hold must not reach O
+                    // (0 * NaN is NaN), so their V rows become zeros.
+                    uint8_t* vgen = smem + C::kOffV + stg * C::kKvBytes;
+                    const int per_panel = (BN - nvalid) * 8;
+                    for (int e = lane; e < per_panel * C::kPanels; e += 32) {
+                        const int pn = e / per_panel, rem = e % per_panel;
+                        *reinterpret_cast<uint4*>(vgen + pn * C::kKvPanel + (nvalid + rem / 8) * 128 +
+                                                  (rem % 8) * 16) = make_uint4(0, 0, 0, 0);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
                 }
-                fence_proxy_async_smem();
-                __syncwarp();
-            }
-            if (lane == 0) {
-                const uint32_t dO = tmem + C::kTmemO;
+                if (lane == 0) {
+                    const uint32_t dO = tmem + C::kTmemO;
 #pragma unroll
-                for (int k = 0; k < BN / 16; ++k) {
-                    const int pn = k >> 2, off = (k & 3) * 32;
-                    const uint64_t a = tc::smem_desc_sw128(sP + pn * (kRows * 128) + off, 16, 1024);
-                    const uint64_t bdesc = tc::smem_desc_sw128(vst + k * 16 * 128, C::kKvPanel, 1024);
-                    tc::mma_bf16(dO, a, bdesc, idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
+                    for (int k = 0; k < BN / 16; ++k) {
+                        const int pn = k >> 2, off = (k & 3) * 32;
+                        const uint64_t a = tc::smem_desc_sw128(sP + pn * (kRows * 128) + off, 16, 1024);
+                        const uint64_t bdesc = tc::smem_desc_sw128(vst + k * 16 * 128, C::kKvPanel, 1024);
+                        tc::mma_bf16(dO, a, bdesc, idesc_pv, (np > 0 || k > 0) ? 1u : 0u);
+                    }
+                    tc::commit(B.o_done + 8 * (np & 1));
+                    tc::commit(B.v_empty0 + 8 * stg);
                 }
-                tc::commit(B.o_done + 8 * (j & 1));
-                tc::commit(B.v_empty0 + 8 * stg);
+                __syncwarp();
+                ++np;
+                progressed = true;
             }
-            __syncwarp();
+            if (progressed) {
+                idle_since = 0;
+            } else {
+                if (*abort_flag) break;
+                const uint64_t now = global_ns();
+                if (idle_since == 0) {
+                    idle_since = now;
+                } else if (now - idle_since > kWaitLimitNs) {
+                    if (lane == 0) {
+                        *abort_flag = 1;
+                        atomicOr(p.err, (int)UA_DEVERR_TIMEOUT);
+                    }
+                    __syncwarp();
+                    break;
+                }
+            }
         }
         if (*abort_flag) {
             // Make sure no MMA of this CTA is still running before the tensor
