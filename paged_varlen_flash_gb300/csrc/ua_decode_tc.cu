@@ -34,9 +34,10 @@ namespace {
 constexpr int kN = 16;          // packed rows per tile (MMA N)
 constexpr int kBN = 128;        // keys per KV tile (MMA M of S^T)
 constexpr int kD = 128;         // head size served by this kernel (MMA M of O^T)
-constexpr int kThreadsD = 192;  // 4 softmax warps, 1 TMA warp, 1 MMA warp
+constexpr int kThreadsD = 224;  // 4 softmax warps, TMA warp, QK^T issuer, P.V issuer
 constexpr int kWarpTmaD = 4;
-constexpr int kWarpMmaD = 5;
+constexpr int kWarpMmaD = 5;    // QK^T issuer (also allocates tensor memory)
+constexpr int kWarpPvD = 6;     // P.V issuer
 constexpr uint32_t kTmemColsD = 64;
 constexpr float kLazyD = 8.0f;
 
@@ -55,8 +56,8 @@ struct DCfg {
     static constexpr int kOffP = kOffV + NS * kKvBytes;   // two P^T buffers
     static constexpr int kOffBar = kOffP + 2 * kPBuf;
     // q_full, k_full[NS], v_full[NS], k_empty[NS], v_empty[NS], s_full[2],
-    // p_full[2], o_done[2], drain
-    static constexpr int kNumBars = 1 + 4 * NS + 7;
+    // p_full[2], o_done[2], drain[2]
+    static constexpr int kNumBars = 1 + 4 * NS + 8;
     static constexpr int kOffRed = kOffBar + kNumBars * 8;    // maxima [2][4][16] fp32
     static constexpr int kOffSum = kOffRed + 2 * 4 * kN * 4;  // row sums [4][16] fp32
     static constexpr int kOffMisc = kOffSum + 4 * kN * 4;
@@ -205,6 +206,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             mbar_init(o_done0 + 8 * i, 1);
         }
         mbar_init(drain, 1);
+        mbar_init(drain + 8, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -223,6 +225,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 
     if (warp == kWarpTmaD) {
         // ------------------------------ TMA producer ------------------------------
+        // The whole warp issues: lane i owns paged block i of each KV tile (its
+        // id load and its TMA boxes), so one tile's boxes go out in parallel
+        // instead of one after another from a single thread.
         if (lane == 0) {
             tma_prefetch_desc(&tm_q);
             tma_prefetch_desc(&tm_k);
@@ -231,94 +236,95 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 #pragma unroll
             for (int pn = 0; pn < C::kPanels; ++pn)
                 tma_load_3d(sQ + pn * C::kQPanel, &tm_q, pn * 64, hkv * g, (int)q0, q_full);
-            const int b = p.b;
-            const int nblk_seq = (sk + b - 1) / b;
-            const int32_t* bt = p.block_table + (int64_t)s * p.bt_stride;
-            for (int j = 0; j < n_tiles; ++j) {
-                const int stg = j % NS;
-                const int key0 = (t_begin + j) * kBN;
-                const int blk0 = key0 / b;
-                const int nb = min(kBN / b, nblk_seq - blk0);
-                const uint32_t bytes = (uint32_t)nb * b * 128 * C::kPanels;
-                if (j >= NS && !dwait(k_empty0 + 8 * stg, ((j / NS) + 1) & 1, abort_flag, p.err)) break;
-                mbar_arrive_expect_tx(k_full0 + 8 * stg, bytes);
-                for (int bi = 0; bi < nb; ++bi) {
-                    const int32_t id = __ldg(bt + blk0 + bi);
-                    if (id < 0 || (int64_t)id >= p.num_blocks) atomicOr(p.err, (int)UA_DEVERR_BLOCK_ID);
-#pragma unroll
-                    for (int pn = 0; pn < C::kPanels; ++pn)
-                        tma_load_4d(sK + stg * C::kKvBytes + pn * C::kKvPanel + bi * b * 128, &tm_k,
-                                    pn * 64, hkv, 0, id, k_full0 + 8 * stg);
-                }
-                if (j >= NS && !dwait(v_empty0 + 8 * stg, ((j / NS) + 1) & 1, abort_flag, p.err)) break;
-                mbar_arrive_expect_tx(v_full0 + 8 * stg, bytes);
-                for (int bi = 0; bi < nb; ++bi) {
-                    const int32_t id = __ldg(bt + blk0 + bi);
-#pragma unroll
-                    for (int pn = 0; pn < C::kPanels; ++pn)
-                        tma_load_4d(sV + stg * C::kKvBytes + pn * C::kKvPanel + bi * b * 128, &tm_v,
-                                    pn * 64, hkv, 0, id, v_full0 + 8 * stg);
-                }
+        }
+        const int b = p.b;
+        const int nblk_seq = (sk + b - 1) / b;
+        const int32_t* bt = p.block_table + (int64_t)s * p.bt_stride;
+        int issued = 0;
+        for (int j = 0; j < n_tiles; ++j) {
+            const int stg = j % NS;
+            const int key0 = (t_begin + j) * kBN;
+            const int blk0 = key0 / b;
+            const int nb = min(kBN / b, nblk_seq - blk0);
+            const uint32_t bytes = (uint32_t)nb * b * 128 * C::kPanels;
+            int32_t id = 0;
+            if (lane < nb) {
+                id = __ldg(bt + blk0 + lane);
+                if (id < 0 || (int64_t)id >= p.num_blocks) atomicOr(p.err, (int)UA_DEVERR_BLOCK_ID);
             }
-            if (*abort_flag) {
-                // Let every copy this thread issued land before the CTA ends.
-                for (int j = max(0, n_tiles - NS); j < n_tiles; ++j) {
-                    mbar_wait_bounded(k_full0 + 8 * (j % NS), (j / NS) & 1);
-                    mbar_wait_bounded(v_full0 + 8 * (j % NS), (j / NS) & 1);
-                }
+            if (j >= NS && !__all_sync(0xffffffffu, dwait(k_empty0 + 8 * stg, ((j / NS) + 1) & 1,
+                                                           abort_flag, p.err)))
+                break;
+            if (lane == 0) mbar_arrive_expect_tx(k_full0 + 8 * stg, bytes);
+            __syncwarp();
+            if (lane < nb) {
+#pragma unroll
+                for (int pn = 0; pn < C::kPanels; ++pn)
+                    tma_load_4d(sK + stg * C::kKvBytes + pn * C::kKvPanel + lane * b * 128, &tm_k,
+                                pn * 64, hkv, 0, id, k_full0 + 8 * stg);
+            }
+            if (j >= NS && !__all_sync(0xffffffffu, dwait(v_empty0 + 8 * stg, ((j / NS) + 1) & 1,
+                                                           abort_flag, p.err)))
+                break;
+            if (lane == 0) mbar_arrive_expect_tx(v_full0 + 8 * stg, bytes);
+            __syncwarp();
+            if (lane < nb) {
+#pragma unroll
+                for (int pn = 0; pn < C::kPanels; ++pn)
+                    tma_load_4d(sV + stg * C::kKvBytes + pn * C::kKvPanel + lane * b * 128, &tm_v,
+                                pn * 64, hkv, 0, id, v_full0 + 8 * stg);
+            }
+            issued = j + 1;
+        }
+        if (*abort_flag && lane == 0) {
+            // Let every copy this warp issued land before the CTA ends.
+            for (int j = max(0, issued - NS); j < issued; ++j) {
+                mbar_wait_bounded(k_full0 + 8 * (j % NS), (j / NS) & 1);
+                mbar_wait_bounded(v_full0 + 8 * (j % NS), (j / NS) & 1);
             }
         }
         __syncwarp();
-    } else if (warp == kWarpMmaD) {
-        // ------------------------------ MMA issuer --------------------------------
+    } else if (warp == kWarpMmaD || warp == kWarpPvD) {
+        // ---------------------- MMA issuers (one thread each) ----------------------
+        // Two warps, each blocking only on the barriers its own MMAs need, so
+        // neither spins and neither holds the other back: warp 5 issues
+        // S^T(j) = K(j) Q^T once K(j) has landed and the softmax has released
+        // S^T buffer (j & 1) (P of tile j - 2 published); warp 6 issues
+        // O^T += V(j)^T P^T(j) once P(j) and V(j) are ready.
         constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(kBN, kN, false, false);
         constexpr uint32_t idesc_pv = tc::idesc_bf16_f32(kD, kN, true, false);
         auto wwait = [&](uint32_t bar, uint32_t par) {
             return __all_sync(0xffffffffu, dwait(bar, par, abort_flag, p.err));
         };
-        auto issue_qk = [&](int j) {
-            const int stg = j % NS;
-            const uint32_t kst = sK + stg * C::kKvBytes;
-            const uint32_t dS = tmem + C::kTmemS + (j & 1) * kN;
+        if (warp == kWarpMmaD) {
+            bool ok = wwait(q_full, 0);
+            for (int j = 0; ok && j < n_tiles; ++j) {
+                if (j >= 2 && !wwait(p_full0 + 8 * (j & 1), ((j - 2) >> 1) & 1)) break;
+                const int stg = j % NS;
+                if (!wwait(k_full0 + 8 * stg, (j / NS) & 1)) break;
+                tc::fence_after_sync();
+                if (lane == 0) {
+                    const uint32_t kst = sK + stg * C::kKvBytes;
+                    const uint32_t dS = tmem + C::kTmemS + (j & 1) * kN;
 #pragma unroll
-            for (int k = 0; k < kD / 16; ++k) {
-                const int pn = k >> 2, off = (k & 3) * 32;
-                const uint64_t a = tc::smem_desc_sw128(kst + pn * C::kKvPanel + off, 16, 1024);
-                const uint64_t bq = tc::smem_desc_sw128(sQ + pn * C::kQPanel + off, 16, 1024);
-                tc::mma_bf16(dS, a, bq, idesc_qk, k > 0 ? 1u : 0u);
-            }
-            tc::commit(s_full0 + 8 * (j & 1));
-            tc::commit(k_empty0 + 8 * stg);
-        };
-        bool ok = wwait(q_full, 0) && wwait(k_full0, 0);
-        if (ok) {
-            tc::fence_after_sync();
-            if (lane == 0) issue_qk(0);
-            __syncwarp();
-        }
-        // Event loop: issue QK^T(nq) as soon as its K tile has landed and
-        // P.V(np) as soon as P and V are ready, whichever comes first, so a
-        // late K tile never holds back the P.V that frees a V stage.  QK^T(j)
-        // reuses the S^T buffer of tile j - 2, which the softmax released
-        // before P.V(j - 2) was issued (hence nq <= np + 1).
-        int nq = 1, np = 0;
-        uint64_t idle_since = 0;
-        while (ok && np < n_tiles) {
-            bool progressed = false;
-            if (nq < n_tiles && nq <= np + 1 &&
-                __all_sync(0xffffffffu, mbar_try_wait(k_full0 + 8 * (nq % NS), (nq / NS) & 1))) {
-                tc::fence_after_sync();
-                if (lane == 0) issue_qk(nq);
+                    for (int k = 0; k < kD / 16; ++k) {
+                        const int pn = k >> 2, off = (k & 3) * 32;
+                        const uint64_t a = tc::smem_desc_sw128(kst + pn * C::kKvPanel + off, 16, 1024);
+                        const uint64_t bq = tc::smem_desc_sw128(sQ + pn * C::kQPanel + off, 16, 1024);
+                        tc::mma_bf16(dS, a, bq, idesc_qk, k > 0 ? 1u : 0u);
+                    }
+                    tc::commit(s_full0 + 8 * (j & 1));
+                    tc::commit(k_empty0 + 8 * stg);
+                }
                 __syncwarp();
-                ++nq;
-                progressed = true;
             }
-            const int stg = np % NS;
-            if (np < nq &&
-                __all_sync(0xffffffffu, mbar_try_wait(p_full0 + 8 * (np & 1), (np >> 1) & 1) &&
-                                            mbar_try_wait(v_full0 + 8 * stg, (np / NS) & 1))) {
+        } else {
+            for (int j = 0; j < n_tiles; ++j) {
+                const int stg = j % NS;
+                if (!wwait(p_full0 + 8 * (j & 1), (j >> 1) & 1)) break;
+                if (!wwait(v_full0 + 8 * stg, (j / NS) & 1)) break;
                 tc::fence_after_sync();
-                const int key0 = (t_begin + np) * kBN;
+                const int key0 = (t_begin + j) * kBN;
                 const int nvalid = min(kBN, sk - key0);
                 if (nvalid < kBN) {
                     // Keys past S_k: their V rows become zeros so that whatever
@@ -335,43 +341,26 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 }
                 if (lane == 0) {
                     const uint32_t vst = sV + stg * C::kKvBytes;
-                    const uint32_t pbuf = sP + (np & 1) * C::kPBuf;
+                    const uint32_t pbuf = sP + (j & 1) * C::kPBuf;
 #pragma unroll
                     for (int kk = 0; kk < kBN / 16; ++kk) {
                         const uint64_t a = tc::smem_desc_sw128(vst + kk * 16 * 128, C::kKvPanel, 1024);
                         const uint64_t bp =
                             tc::smem_desc_sw128(pbuf + (kk >> 2) * C::kPPanel + (kk & 3) * 32, 16, 1024);
-                        tc::mma_bf16(tmem + C::kTmemO, a, bp, idesc_pv, (np > 0 || kk > 0) ? 1u : 0u);
+                        tc::mma_bf16(tmem + C::kTmemO, a, bp, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
                     }
-                    tc::commit(o_done0 + 8 * (np & 1));
+                    tc::commit(o_done0 + 8 * (j & 1));
                     tc::commit(v_empty0 + 8 * stg);
                 }
                 __syncwarp();
-                ++np;
-                progressed = true;
-            }
-            if (progressed) {
-                idle_since = 0;
-            } else {
-                if (*abort_flag) break;
-                const uint64_t now = global_ns();
-                if (idle_since == 0) {
-                    idle_since = now;
-                } else if (now - idle_since > kWaitLimitNs) {
-                    if (lane == 0) {
-                        *abort_flag = 1;
-                        atomicOr(p.err, (int)UA_DEVERR_TIMEOUT);
-                    }
-                    __syncwarp();
-                    break;
-                }
             }
         }
         if (*abort_flag) {
-            // No MMA of this CTA may still run when the tensor memory is freed.
-            if (lane == 0) tc::commit(drain);
+            // No MMA this thread issued may still run when tensor memory is freed.
+            const uint32_t dr = drain + 8 * (warp - kWarpMmaD);
+            if (lane == 0) tc::commit(dr);
             __syncwarp();
-            mbar_wait_bounded(drain, 0);
+            mbar_wait_bounded(dr, 0);
         }
     } else {
         // --------------------------- softmax warps 0-3 ----------------------------
@@ -383,10 +372,18 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         const bool alibi = (p.flags & UA_FLAG_ALIBI) != 0;
         const float sl2 = p.scale * kLog2e;
         float m[kN], l[kN];
+        // Visible key range [lo, hi] of each packed row (constant per CTA);
+        // padding rows get an empty range.
+        int rlo[kN], rhi[kN];
+        float rslope[kN];
 #pragma unroll
         for (int r = 0; r < kN; ++r) {
             m[r] = -INFINITY;
             l[r] = 0.f;
+            const int i = r / g;
+            rhi[r] = r < nrows ? (causal ? min(i + ctx, sk - 1) : sk - 1) : -1;
+            rlo[r] = window ? max(0, i + ctx - p.window + 1) : 0;
+            rslope[r] = (!PLAIN && alibi && r < nrows) ? __ldg(p.alibi + hkv * g + r % g) : 0.f;
         }
         bool ok = true;
         for (int j = 0; j < n_tiles; ++j) {
@@ -401,19 +398,16 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 tc::wait_ld();
 #pragma unroll
                 for (int r = 0; r < kN; ++r) {
-                    const int i = r / g;
-                    const int hi = causal ? min(i + ctx, sk - 1) : sk - 1;
-                    const int lo = window ? max(0, i + ctx - p.window + 1) : 0;
                     float v;
                     if constexpr (PLAIN) {
                         v = __uint_as_float(sv[r]) * sl2;
                     } else {
                         float tt = __uint_as_float(sv[r]) * p.scale;
                         if (softcap) tt = p.softcap * tanh_e2(tt / p.softcap);
-                        if (alibi) tt += __ldg(p.alibi + hkv * g + r % g) * (float)(key - ctx);
+                        if (alibi) tt += rslope[r] * (float)(key - ctx);
                         v = tt * kLog2e;
                     }
-                    x[r] = (r < nrows && key >= lo && key <= hi) ? v : -INFINITY;
+                    x[r] = (key >= rlo[r] && key <= rhi[r]) ? v : -INFINITY;
                 }
             } else {
 #pragma unroll
@@ -498,6 +492,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 const int kin = t & 63;
 #pragma unroll
                 for (int r = 0; r < kN; ++r) {
+                    if (r >= nrows) continue;  // padding columns of O^T are never read
                     const uint16_t v = (r & 1) ? (uint16_t)(pb[r / 2] >> 16) : (uint16_t)(pb[r / 2] & 0xffffu);
                     *reinterpret_cast<uint16_t*>(pbase + r * 128 + (((kin >> 3) ^ (r & 7)) << 4) +
                                                  (kin & 7) * 2) = v;

@@ -40,13 +40,14 @@ namespace {
 constexpr float kLazy = 8.0f;
 constexpr int kRows = 128;
 // SPLIT softmax warpgroups share each row's BN key columns (SPLIT parts of
-// BN / SPLIT); one more warp issues TMA copies and one issues MMAs.
+// BN / SPLIT); one more warp issues TMA copies, one issues QK^T and one P.V.
 template <int SPLIT>
 struct Roles {
     static constexpr int kSmThreads = 128 * SPLIT;
-    static constexpr int kThreads = kSmThreads + 64;
+    static constexpr int kThreads = kSmThreads + 96;
     static constexpr int kWarpTma = 4 * SPLIT;
-    static constexpr int kWarpMma = 4 * SPLIT + 1;
+    static constexpr int kWarpMma = 4 * SPLIT + 1;   // QK^T issuer, tensor-memory owner
+    static constexpr int kWarpPv = 4 * SPLIT + 2;    // P.V issuer
 };
 constexpr uint32_t kTmemCols = 512;
 
@@ -65,8 +66,8 @@ struct PCfg {
     static constexpr int kOffP = kOffV + NS * kKvBytes;
     static constexpr int kOffBar = kOffP + kPBytes;
     // q_full, k_full[NS], v_full[NS], k_empty[NS], v_empty[NS], s_full[2], p_full[2],
-    // o_done[2], drain
-    static constexpr int kNumBars = 1 + 4 * NS + 2 + 2 + 2 + 1;
+    // o_done[2], drain[2]
+    static constexpr int kNumBars = 1 + 4 * NS + 2 + 2 + 2 + 2;
     static constexpr int kOffRed = kOffBar + kNumBars * 8;      // [2 parity][SPLIT][128] fp32
     static constexpr int kOffMisc = kOffRed + 2 * SPLIT * kRows * 4;
     static constexpr int kSmem = kOffMisc + 16 + 1024;
@@ -165,6 +166,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     constexpr int kSmThreads = R::kSmThreads;
     constexpr int kWarpTma = R::kWarpTma;
     constexpr int kWarpMma = R::kWarpMma;
+    constexpr int kWarpPv = R::kWarpPv;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -252,6 +254,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         mbar_init(B.o_done, 1);
         mbar_init(B.o_done + 8, 1);
         mbar_init(B.drain, 1);
+        mbar_init(B.drain + 8, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -271,6 +274,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 
     if (warp == kWarpTma) {
         // ------------------------------ TMA producer ------------------------------
+        // The whole warp issues: lane i owns paged block i of each KV tile (its
+        // id load and its TMA boxes), so one tile's boxes go out in parallel
+        // instead of one after another from a single thread.
         if (lane == 0) {
             tma_prefetch_desc(&tm_q);
             tma_prefetch_desc(&tm_k);
@@ -279,103 +285,96 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 #pragma unroll
             for (int pn = 0; pn < C::kPanels; ++pn)
                 tma_load_3d(sQ + pn * C::kQPanel, &tm_q, pn * 64, hkv * g, (int)(q0 + p0), B.q_full);
-            const int b = p.b;
-            const int nblk_seq = (sk + b - 1) / b;
-            const int32_t* bt = p.block_table + (int64_t)s * p.bt_stride;
-            for (int j = 0; j < n_tiles; ++j) {
-                const int stg = j % NS;
-                if (j >= NS && !wait_or_abort(B.k_empty0 + 8 * stg, ((j / NS) + 1) & 1, abort_flag,
-                                              p.err))
-                    break;
-                const int key0 = (t_begin + j) * BN;
-                const int blk0 = key0 / b;
-                const int nb = min(BN / b, nblk_seq - blk0);
-                const uint32_t bytes = (uint32_t)nb * b * 128 * C::kPanels;
-                const uint32_t kst = sK + stg * C::kKvBytes;
-                const uint32_t vst = sV + stg * C::kKvBytes;
-                mbar_arrive_expect_tx(B.k_full0 + 8 * stg, bytes);
-                for (int bi = 0; bi < nb; ++bi) {
-                    const int32_t id = __ldg(bt + blk0 + bi);
-                    if (id < 0 || (int64_t)id >= p.num_blocks) atomicOr(p.err, (int)UA_DEVERR_BLOCK_ID);
-#pragma unroll
-                    for (int pn = 0; pn < C::kPanels; ++pn)
-                        tma_load_4d(kst + pn * C::kKvPanel + bi * b * 128, &tm_k, pn * 64, hkv, 0, id,
-                                    B.k_full0 + 8 * stg);
-                }
-                if (j >= NS && !wait_or_abort(B.v_empty0 + 8 * stg, ((j / NS) + 1) & 1, abort_flag,
-                                              p.err))
-                    break;
-                mbar_arrive_expect_tx(B.v_full0 + 8 * stg, bytes);
-                for (int bi = 0; bi < nb; ++bi) {
-                    const int32_t id = __ldg(bt + blk0 + bi);
-#pragma unroll
-                    for (int pn = 0; pn < C::kPanels; ++pn)
-                        tma_load_4d(vst + pn * C::kKvPanel + bi * b * 128, &tm_v, pn * 64, hkv, 0, id,
-                                    B.v_full0 + 8 * stg);
-                }
+        }
+        const int b = p.b;
+        const int nblk_seq = (sk + b - 1) / b;
+        const int32_t* bt = p.block_table + (int64_t)s * p.bt_stride;
+        int issued = 0;
+        for (int j = 0; j < n_tiles; ++j) {
+            const int stg = j % NS;
+            const int key0 = (t_begin + j) * BN;
+            const int blk0 = key0 / b;
+            const int nb = min(BN / b, nblk_seq - blk0);
+            const uint32_t bytes = (uint32_t)nb * b * 128 * C::kPanels;
+            int32_t id = 0;
+            if (lane < nb) {
+                id = __ldg(bt + blk0 + lane);
+                if (id < 0 || (int64_t)id >= p.num_blocks) atomicOr(p.err, (int)UA_DEVERR_BLOCK_ID);
             }
-            if (*abort_flag) {
-                // Let every copy this thread issued land before the CTA ends.
-                for (int j = max(0, n_tiles - NS); j < n_tiles; ++j) {
-                    const int stg = j % NS;
-                    mbar_wait_bounded(B.k_full0 + 8 * stg, (j / NS) & 1);
-                    mbar_wait_bounded(B.v_full0 + 8 * stg, (j / NS) & 1);
-                }
+            if (j >= NS && !__all_sync(0xffffffffu, wait_or_abort(B.k_empty0 + 8 * stg, ((j / NS) + 1) & 1,
+                                                                   abort_flag, p.err)))
+                break;
+            if (lane == 0) mbar_arrive_expect_tx(B.k_full0 + 8 * stg, bytes);
+            __syncwarp();
+            if (lane < nb) {
+#pragma unroll
+                for (int pn = 0; pn < C::kPanels; ++pn)
+                    tma_load_4d(sK + stg * C::kKvBytes + pn * C::kKvPanel + lane * b * 128, &tm_k,
+                                pn * 64, hkv, 0, id, B.k_full0 + 8 * stg);
+            }
+            if (j >= NS && !__all_sync(0xffffffffu, wait_or_abort(B.v_empty0 + 8 * stg, ((j / NS) + 1) & 1,
+                                                                   abort_flag, p.err)))
+                break;
+            if (lane == 0) mbar_arrive_expect_tx(B.v_full0 + 8 * stg, bytes);
+            __syncwarp();
+            if (lane < nb) {
+#pragma unroll
+                for (int pn = 0; pn < C::kPanels; ++pn)
+                    tma_load_4d(sV + stg * C::kKvBytes + pn * C::kKvPanel + lane * b * 128, &tm_v,
+                                pn * 64, hkv, 0, id, B.v_full0 + 8 * stg);
+            }
+            issued = j + 1;
+        }
+        if (*abort_flag && lane == 0) {
+            // Let every copy this warp issued land before the CTA ends.
+            for (int j = max(0, issued - NS); j < issued; ++j) {
+                mbar_wait_bounded(B.k_full0 + 8 * (j % NS), (j / NS) & 1);
+                mbar_wait_bounded(B.v_full0 + 8 * (j % NS), (j / NS) & 1);
             }
         }
         __syncwarp();
-    } else if (warp == kWarpMma) {
-        // ------------------------------ MMA issuer --------------------------------
+    } else if (warp == kWarpMma || warp == kWarpPv) {
+        // ---------------------- MMA issuers (one thread each) ----------------------
+        // Two warps, each blocking only on the barriers its own MMAs need, so
+        // neither spins and neither holds the other back: one issues
+        // S(j) = Q K(j)^T once K(j) has landed and the softmax has released S
+        // buffer (j & 1) (P of tile j - 2 published); the other issues
+        // O += P(j) V(j) once P(j) and V(j) are ready.
         constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(kRows, BN, false, false);
         constexpr uint32_t idesc_pv = tc::idesc_bf16_f32(kRows, D, false, true);
         auto wwait = [&](uint32_t bar, uint32_t par) {
             return __all_sync(0xffffffffu, wait_or_abort(bar, par, abort_flag, p.err));
         };
-        bool ok = wwait(B.q_full, 0);
-        auto issue_qk = [&](int j) {
-            const int stg = j % NS;
-            const uint32_t kst = sK + stg * C::kKvBytes;
-            const uint32_t dS = tmem + C::kTmemS + (j & 1) * BN;
-#pragma unroll
-            for (int k = 0; k < D / 16; ++k) {
-                const int pn = k >> 2, off = (k & 3) * 32;
-                const uint64_t a = tc::smem_desc_sw128(sQ + pn * C::kQPanel + off, 16, 1024);
-                const uint64_t bdesc = tc::smem_desc_sw128(kst + pn * C::kKvPanel + off, 16, 1024);
-                tc::mma_bf16(dS, a, bdesc, idesc_qk, k > 0 ? 1u : 0u);
-            }
-            tc::commit(B.s_full0 + 8 * (j & 1));
-            tc::commit(B.k_empty0 + 8 * stg);
-        };
-        if (ok) ok = wwait(B.k_full0, 0);
-        if (ok) {
-            tc::fence_after_sync();
-            if (lane == 0) issue_qk(0);
-            __syncwarp();
-        }
-        // Event loop: issue QK^T(nq) as soon as its K tile has landed and
-        // P.V(np) as soon as P and V are ready, whichever comes first, so a
-        // late K tile never holds back the P.V that frees a V stage.  QK^T(j)
-        // reuses the S buffer of tile j - 2, which the softmax released before
-        // P.V(j - 2) was issued (hence nq <= np + 1).
-        int nq = 1, np = 0;
-        uint64_t idle_since = 0;
-        while (ok && np < n_tiles) {
-            bool progressed = false;
-            if (nq < n_tiles && nq <= np + 1 &&
-                __all_sync(0xffffffffu, mbar_try_wait(B.k_full0 + 8 * (nq % NS), (nq / NS) & 1))) {
+        if (warp == kWarpMma) {
+            bool ok = wwait(B.q_full, 0);
+            for (int j = 0; ok && j < n_tiles; ++j) {
+                if (j >= 2 && !wwait(B.p_full + 8 * (j & 1), ((j - 2) >> 1) & 1)) break;
+                const int stg = j % NS;
+                if (!wwait(B.k_full0 + 8 * stg, (j / NS) & 1)) break;
                 tc::fence_after_sync();
-                if (lane == 0) issue_qk(nq);
+                if (lane == 0) {
+                    const uint32_t kst = sK + stg * C::kKvBytes;
+                    const uint32_t dS = tmem + C::kTmemS + (j & 1) * BN;
+#pragma unroll
+                    for (int k = 0; k < D / 16; ++k) {
+                        const int pn = k >> 2, off = (k & 3) * 32;
+                        const uint64_t a = tc::smem_desc_sw128(sQ + pn * C::kQPanel + off, 16, 1024);
+                        const uint64_t bdesc = tc::smem_desc_sw128(kst + pn * C::kKvPanel + off, 16, 1024);
+                        tc::mma_bf16(dS, a, bdesc, idesc_qk, k > 0 ? 1u : 0u);
+                    }
+                    tc::commit(B.s_full0 + 8 * (j & 1));
+                    tc::commit(B.k_empty0 + 8 * stg);
+                }
                 __syncwarp();
-                ++nq;
-                progressed = true;
             }
-            const int stg = np % NS;
-            if (np < nq &&
-                __all_sync(0xffffffffu, mbar_try_wait(B.p_full + 8 * (np & 1), (np >> 1) & 1) &&
-                                            mbar_try_wait(B.v_full0 + 8 * stg, (np / NS) & 1))) {
+        } else {
+            for (int j = 0; j < n_tiles; ++j) {
+                const int stg = j % NS;
+                if (!wwait(B.p_full + 8 * (j & 1), (j >> 1) & 1)) break;
+                if (!wwait(B.v_full0 + 8 * stg, (j / NS) & 1)) break;
                 tc::fence_after_sync();
                 const uint32_t vst = sV + stg * C::kKvBytes;
-                const int key0 = (t_begin + np) * BN;
+                const int key0 = (t_begin + j) * BN;
                 const int nvalid = min(BN, sk - key0);
                 if (nvalid < BN) {
                     // Keys past S_k: whatever those slots hold must not reach O
@@ -397,38 +396,20 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                         const int pn = k >> 2, off = (k & 3) * 32;
                         const uint64_t a = tc::smem_desc_sw128(sP + pn * (kRows * 128) + off, 16, 1024);
                         const uint64_t bdesc = tc::smem_desc_sw128(vst + k * 16 * 128, C::kKvPanel, 1024);
-                        tc::mma_bf16(dO, a, bdesc, idesc_pv, (np > 0 || k > 0) ? 1u : 0u);
+                        tc::mma_bf16(dO, a, bdesc, idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
                     }
-                    tc::commit(B.o_done + 8 * (np & 1));
+                    tc::commit(B.o_done + 8 * (j & 1));
                     tc::commit(B.v_empty0 + 8 * stg);
                 }
                 __syncwarp();
-                ++np;
-                progressed = true;
-            }
-            if (progressed) {
-                idle_since = 0;
-            } else {
-                if (*abort_flag) break;
-                const uint64_t now = global_ns();
-                if (idle_since == 0) {
-                    idle_since = now;
-                } else if (now - idle_since > kWaitLimitNs) {
-                    if (lane == 0) {
-                        *abort_flag = 1;
-                        atomicOr(p.err, (int)UA_DEVERR_TIMEOUT);
-                    }
-                    __syncwarp();
-                    break;
-                }
             }
         }
         if (*abort_flag) {
-            // Make sure no MMA of this CTA is still running before the tensor
-            // memory is released.
-            if (lane == 0) tc::commit(B.drain);
+            // No MMA this thread issued may still run when tensor memory is freed.
+            const uint32_t dr = B.drain + 8 * (warp - kWarpMma);
+            if (lane == 0) tc::commit(dr);
             __syncwarp();
-            mbar_wait_bounded(B.drain, 0);
+            mbar_wait_bounded(dr, 0);
         }
     } else {
         // ------------------------- softmax + epilogue warps -----------------------
