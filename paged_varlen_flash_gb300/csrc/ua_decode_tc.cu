@@ -118,13 +118,27 @@ __device__ __forceinline__ void st16(uint32_t taddr, const uint32_t (&r)[16]) {
         : "memory");
 }
 
+// Warp-wide float max through the integer reduction unit: IEEE-754 floats
+// compare like sign-magnitude integers, so flipping the magnitude bits of
+// negative values gives an order-preserving signed-integer key; one
+// redux.sync.max.s32 then replaces a five-step shuffle tree.
+__device__ __forceinline__ float warp_max_f32(float v) {
+    const int b = __float_as_int(v);
+    int key = b >= 0 ? b : (b ^ 0x7fffffff);
+    int r;
+    asm volatile("redux.sync.max.s32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(key));
+    return __int_as_float(r >= 0 ? r : (r ^ 0x7fffffff));
+}
+
 __device__ __forceinline__ float tanh_e2(float x) {
     // tanh(x) = 1 - 2 / (e^{2x} + 1)
     const float e = fast_exp2(x * (2.0f * kLog2e));
     return 1.0f - __fdividef(2.0f, e + 1.0f);
 }
 
-template <int NS, bool PLAIN>
+// NR: packed rows the softmax threads track (4, 8 or 16 >= g * S_q); the MMAs
+// always run N = 16 and ignore the padding columns.
+template <int NS, int NR, bool PLAIN>
 __global__ void __launch_bounds__(kThreadsD, 1)
 decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
@@ -371,13 +385,13 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         const bool softcap = (p.flags & UA_FLAG_SOFTCAP) != 0;
         const bool alibi = (p.flags & UA_FLAG_ALIBI) != 0;
         const float sl2 = p.scale * kLog2e;
-        float m[kN], l[kN];
+        float m[NR], l[NR];
         // Visible key range [lo, hi] of each packed row (constant per CTA);
         // padding rows get an empty range.
-        int rlo[kN], rhi[kN];
-        float rslope[kN];
+        int rlo[NR], rhi[NR];
+        float rslope[NR];
 #pragma unroll
-        for (int r = 0; r < kN; ++r) {
+        for (int r = 0; r < NR; ++r) {
             m[r] = -INFINITY;
             l[r] = 0.f;
             const int i = r / g;
@@ -390,14 +404,14 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             const bool got = __all_sync(0xffffffffu, dwait(s_full0 + 8 * (j & 1), (j >> 1) & 1,
                                                            abort_flag, p.err));
             const int key = (t_begin + j) * kBN + t;
-            float x[kN];
+            float x[NR];
             if (got) {
                 tc::fence_after_sync();
                 uint32_t sv[kN];
                 ld16(tl + C::kTmemS + (j & 1) * kN, sv);
                 tc::wait_ld();
 #pragma unroll
-                for (int r = 0; r < kN; ++r) {
+                for (int r = 0; r < NR; ++r) {
                     float v;
                     if constexpr (PLAIN) {
                         v = __uint_as_float(sv[r]) * sl2;
@@ -411,18 +425,13 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 }
             } else {
 #pragma unroll
-                for (int r = 0; r < kN; ++r) x[r] = -INFINITY;
+                for (int r = 0; r < NR; ++r) x[r] = -INFINITY;
             }
             // Per-row maxima over this warp's 32 keys, then over the 4 warps.
 #pragma unroll
-            for (int r = 0; r < kN; ++r) {
+            for (int r = 0; r < NR; ++r) {
                 if (r < nrows) {
-                    float w = x[r];
-                    w = fmaxf(w, __shfl_xor_sync(0xffffffffu, w, 1));
-                    w = fmaxf(w, __shfl_xor_sync(0xffffffffu, w, 2));
-                    w = fmaxf(w, __shfl_xor_sync(0xffffffffu, w, 4));
-                    w = fmaxf(w, __shfl_xor_sync(0xffffffffu, w, 8));
-                    w = fmaxf(w, __shfl_xor_sync(0xffffffffu, w, 16));
+                    const float w = warp_max_f32(x[r]);
                     if (lane == 0) red[((j & 1) * 4 + warp) * kN + r] = w;
                 }
             }
@@ -430,10 +439,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 ok = false;
                 break;
             }
-            float alpha[kN];
+            float alpha[NR];
             bool any_re = false;
 #pragma unroll
-            for (int r = 0; r < kN; ++r) {
+            for (int r = 0; r < NR; ++r) {
                 alpha[r] = 1.f;
                 if (r < nrows) {
                     const float* rr = red + (j & 1) * 4 * kN + r;
@@ -448,9 +457,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             }
             // p = 2^(x - m) on the fp16x2 special-function path; per-thread
             // partial row sums stay fp32.
-            uint32_t pb[kN / 2];
+            uint32_t pb[NR / 2];
 #pragma unroll
-            for (int r = 0; r < kN; r += 2) {
+            for (int r = 0; r < NR; r += 2) {
                 const float a0 = x[r] - (m[r] == -INFINITY ? 0.f : m[r]);
                 const float a1 = x[r + 1] - (m[r + 1] == -INFINITY ? 0.f : m[r + 1]);
                 uint32_t h, e;
@@ -480,7 +489,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     ld16(tl + C::kTmemO, o);
                     tc::wait_ld();
 #pragma unroll
-                    for (int r = 0; r < kN; ++r) o[r] = __float_as_uint(__uint_as_float(o[r]) * alpha[r]);
+                    for (int r = 0; r < NR; ++r) o[r] = __float_as_uint(__uint_as_float(o[r]) * alpha[r]);
                     st16(tl + C::kTmemO, o);
                     tc::wait_st();
                 }
@@ -491,7 +500,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 uint8_t* pbase = smem + C::kOffP + (j & 1) * C::kPBuf + (t >> 6) * C::kPPanel;
                 const int kin = t & 63;
 #pragma unroll
-                for (int r = 0; r < kN; ++r) {
+                for (int r = 0; r < NR; ++r) {
                     if (r >= nrows) continue;  // padding columns of O^T are never read
                     const uint16_t v = (r & 1) ? (uint16_t)(pb[r / 2] >> 16) : (uint16_t)(pb[r / 2] & 0xffffu);
                     *reinterpret_cast<uint16_t*>(pbase + r * 128 + (((kin >> 3) ^ (r & 7)) << 4) +
@@ -509,7 +518,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                                                ((n_tiles - 1) >> 1) & 1, abort_flag, p.err));
             // Row sums over the 128 keys: warp shuffles, then the 4 warps.
 #pragma unroll
-            for (int r = 0; r < kN; ++r) {
+            for (int r = 0; r < NR; ++r) {
                 if (r < nrows) {
                     float w = l[r];
                     w += __shfl_xor_sync(0xffffffffu, w, 1);
@@ -526,7 +535,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 ld16(tl + C::kTmemO, o);
                 tc::wait_ld();
 #pragma unroll
-                for (int r = 0; r < kN; ++r) {
+                for (int r = 0; r < NR; ++r) {
                     if (r >= nrows) continue;
                     const float L0 = lsum[r] + lsum[kN + r] + lsum[2 * kN + r] + lsum[3 * kN + r];
                     const int64_t row = (q0 + r / g) * p.hq + hkv * g + r % g;
@@ -607,7 +616,10 @@ cudaError_t launch_decode_tc(const DecodePlan& plan, const CUtensorMap& tm_k, co
     constexpr int NS = 3;
     using C = DCfg<NS>;
     const bool plain = (p.flags & (UA_FLAG_SOFTCAP | UA_FLAG_ALIBI)) == 0;
-    auto kern = plain ? decode_tc_kernel<NS, true> : decode_tc_kernel<NS, false>;
+    const int rows = p.g * p.max_seqlen_q;
+    auto kern = rows <= 4 ? (plain ? decode_tc_kernel<NS, 4, true> : decode_tc_kernel<NS, 4, false>)
+              : rows <= 8 ? (plain ? decode_tc_kernel<NS, 8, true> : decode_tc_kernel<NS, 8, false>)
+                          : (plain ? decode_tc_kernel<NS, 16, true> : decode_tc_kernel<NS, 16, false>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)plan.splits, (unsigned)p.hk, (unsigned)p.num_seqs);
