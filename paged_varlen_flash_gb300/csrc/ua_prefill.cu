@@ -289,18 +289,24 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         const int b = p.b;
         const int nblk_seq = (sk + b - 1) / b;
         const int32_t* bt = p.block_table + (int64_t)s * p.bt_stride;
+        // Block ids are fetched one tile ahead so their load latency overlaps
+        // the current tile's waits and copies.
+        auto tile_id = [&](int j) -> int32_t {
+            const int blk0 = (t_begin + j) * BN / b;
+            return lane < min(BN / b, nblk_seq - blk0) ? __ldg(bt + blk0 + lane) : 0;
+        };
         int issued = 0;
+        int32_t id_next = n_tiles > 0 ? tile_id(0) : 0;
         for (int j = 0; j < n_tiles; ++j) {
             const int stg = j % NS;
             const int key0 = (t_begin + j) * BN;
             const int blk0 = key0 / b;
             const int nb = min(BN / b, nblk_seq - blk0);
             const uint32_t bytes = (uint32_t)nb * b * 128 * C::kPanels;
-            int32_t id = 0;
-            if (lane < nb) {
-                id = __ldg(bt + blk0 + lane);
-                if (id < 0 || (int64_t)id >= p.num_blocks) atomicOr(p.err, (int)UA_DEVERR_BLOCK_ID);
-            }
+            const int32_t id = id_next;
+            if (j + 1 < n_tiles) id_next = tile_id(j + 1);
+            if (lane < nb && (id < 0 || (int64_t)id >= p.num_blocks))
+                atomicOr(p.err, (int)UA_DEVERR_BLOCK_ID);
             if (j >= NS && !__all_sync(0xffffffffu, wait_or_abort(B.k_empty0 + 8 * stg, ((j / NS) + 1) & 1,
                                                                    abort_flag, p.err)))
                 break;
