@@ -80,3 +80,9 @@ def test_traffic_record_goes_stale_when_the_kernel_changes(tmp_path, monkeypatch
     rec["split_kernel"]["source_sha256"] = "0" * 64
     path.write_text(json.dumps(rec))
     assert bench.recorded_traffic("split_kernel", "decode") is None
+
+
+def test_dominant_kernel_follows_the_reported_path():
+    assert bench.dominant_kernel("decode_tc+combine") == "decode_tc_kernel"
+    assert bench.dominant_kernel("tensor_core") == "prefill_kernel"
+    assert bench.dominant_kernel("split_kv+combine") == "split_kernel"
