@@ -16,7 +16,7 @@
 //              also tensor-memory lane r, so row max and row sum need no
 //              cross-thread reduction;
 //   warp 4     TMA producer: Q tile once (a 3-D box of g heads x 128/g
-//              positions), then K and V tiles through an NS-stage ring, one box
+//              positions), then K and V tiles through NK- and NV-stage rings, one box
 //              per (paged block, 64-wide head-dim panel), block ids read from
 //              the block table;
 //   warp 5     tensor-memory allocator and MMA issuer: S = Q K^T into one of two
@@ -30,6 +30,7 @@
 
 #include "ua_common.cuh"
 #include "ua_prefill.h"
+#include "ua_prefill_common.cuh"
 #include "ua_ptx.cuh"
 #include "ua_tc.cuh"
 #include "ua_tmap.h"
@@ -37,130 +38,39 @@
 namespace ua {
 namespace {
 
-constexpr float kLazy = 8.0f;
-constexpr int kRows = 128;
-// SPLIT softmax warpgroups share each row's BN key columns (SPLIT parts of
-// BN / SPLIT); one more warp issues TMA copies, one issues QK^T and one P.V.
-template <int SPLIT>
-struct Roles {
-    static constexpr int kSmThreads = 128 * SPLIT;
-    static constexpr int kThreads = kSmThreads + 96;
-    static constexpr int kWarpTma = 4 * SPLIT;
-    static constexpr int kWarpMma = 4 * SPLIT + 1;   // QK^T issuer, tensor-memory owner
-    static constexpr int kWarpPv = 4 * SPLIT + 2;    // P.V issuer
-};
-constexpr uint32_t kTmemCols = 512;
+using namespace pf;
 
-template <int D, int BN, int NS, int SPLIT>
+template <int D, int BN, int NK, int NV, int SPLIT>
 struct PCfg {
     static constexpr int kPanels = D / 64;
     static constexpr int kQPanel = kRows * 128;
     static constexpr int kQBytes = kPanels * kQPanel;
     static constexpr int kKvPanel = BN * 128;
     static constexpr int kKvBytes = kPanels * kKvPanel;
-    static constexpr int kPPanels = BN / 64;
-    static constexpr int kPBytes = kPPanels * kRows * 128;
+    static constexpr int kPBytes = 0;   // P lives in tensor memory
     static constexpr int kOffQ = 0;
     static constexpr int kOffK = kOffQ + kQBytes;
-    static constexpr int kOffV = kOffK + NS * kKvBytes;
-    static constexpr int kOffP = kOffV + NS * kKvBytes;
+    static constexpr int kOffV = kOffK + NK * kKvBytes;
+    static constexpr int kOffP = kOffV + NV * kKvBytes;
     static constexpr int kOffBar = kOffP + kPBytes;
-    // q_full, k_full[NS], v_full[NS], k_empty[NS], v_empty[NS], s_full[2], p_full[2],
+    // q_full, k_full[NK], v_full[NV], k_empty[NK], v_empty[NV], s_full[2], p_full[2],
     // o_done[2], drain[2]
-    static constexpr int kNumBars = 1 + 4 * NS + 2 + 2 + 2 + 2;
+    static constexpr int kNumBars = 1 + 2 * NK + 2 * NV + 2 + 2 + 2 + 2;
     static constexpr int kOffRed = kOffBar + kNumBars * 8;      // [2 parity][SPLIT][128] fp32
     static constexpr int kOffMisc = kOffRed + 2 * SPLIT * kRows * 4;
     static constexpr int kSmem = kOffMisc + 16 + 1024;
     static constexpr int kTmemS = 0;
     static constexpr int kTmemO = 2 * BN;
-    static_assert(2 * BN + D <= (int)kTmemCols, "tensor memory budget");
+    static constexpr int kTmemP = 2 * BN + D;   // two bf16 P buffers of BN / 2 columns
+    static_assert(2 * BN + D + BN <= (int)kTmemCols, "tensor memory budget");
     static_assert(kSmem <= 232448, "shared memory budget");
 };
 
-struct Bars {
-    uint32_t q_full, k_full0, v_full0, k_empty0, v_empty0, s_full0, p_full, o_done, drain;
-};
-
-// Wait on an mbarrier phase; gives up (and raises the CTA's abort flag and the
-// device error bit) after about a second, or as soon as another role aborted.
-__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
-                                              volatile int* abort_flag, int32_t* err) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t start = global_ns();
-    for (;;) {
-        for (int i = 0; i < 128; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
-        if (*abort_flag) return false;
-        if (global_ns() - start > kWaitLimitNs) {
-            *abort_flag = 1;
-            atomicOr(err, (int)UA_DEVERR_TIMEOUT);
-            return false;
-        }
-    }
-}
-
-__device__ __forceinline__ float fmax3(float a, float b, float c) {
-    float d;
-    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-    return d;
-}
-
-__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
-    uint64_t d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;"
-        : "=l"(d)
-        : "l"(*reinterpret_cast<uint64_t*>(&a)), "l"(*reinterpret_cast<uint64_t*>(&b)),
-          "l"(*reinterpret_cast<uint64_t*>(&c)));
-    return *reinterpret_cast<float2*>(&d);
-}
-
-__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
-    uint64_t d;
-    asm("add.rn.f32x2 %0, %1, %2;"
-        : "=l"(d)
-        : "l"(*reinterpret_cast<uint64_t*>(&a)), "l"(*reinterpret_cast<uint64_t*>(&b)));
-    return *reinterpret_cast<float2*>(&d);
-}
-
-// 2^a for a pair: the argument rounded to fp16, the hardware fp16x2 base-2
-// exponential, and the two results widened back to fp32.  -inf maps to 0.
-__device__ __forceinline__ float2 exp2_pair_f16(float2 a) {
-    uint32_t h, e;
-    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(a.y), "f"(a.x));
-    asm("ex2.approx.f16x2 %0, %1;" : "=r"(e) : "r"(h));
-    float lo, hi;
-    asm("{\n\t.reg .f16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
-        : "=f"(lo), "=f"(hi)
-        : "r"(e));
-    return make_float2(lo, hi);
-}
-
-// Named barrier over `count` threads that also returns the AND of `pred`
-// across them.
-__device__ __forceinline__ bool bar_and_sync(int id, int count, bool pred) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.u32 p, %1, 0;\n\t"
-        "barrier.cta.red.and.pred q, %2, %3, p;\n\t"
-        "selp.u32 %0, 1, 0, q;\n\t}"
-        : "=r"(r)
-        : "r"((uint32_t)pred), "r"(id), "r"(count)
-        : "memory");
-    return r != 0;
-}
-
-__device__ __forceinline__ float tanh_via_exp2(float x) {
-    // tanh(x) = 1 - 2 / (e^{2x} + 1)
-    const float e = fast_exp2(x * (2.0f * kLog2e));
-    return 1.0f - __fdividef(2.0f, e + 1.0f);
-}
-
-template <int D, int BN, int NS, int SPLIT, bool PLAIN>
+template <int D, int BN, int NK, int NV, int SPLIT, bool PLAIN>
 __global__ void __launch_bounds__(Roles<SPLIT>::kThreads, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
-    using C = PCfg<D, BN, NS, SPLIT>;
+    using C = PCfg<D, BN, NK, NV, SPLIT>;
     using R = Roles<SPLIT>;
     constexpr int kThreads = R::kThreads;
     constexpr int kSmThreads = R::kSmThreads;
@@ -224,27 +134,30 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     Bars B;
     B.q_full = smem_u32(&bar_mem[0]);
     B.k_full0 = smem_u32(&bar_mem[1]);
-    B.v_full0 = smem_u32(&bar_mem[1 + NS]);
+    B.v_full0 = smem_u32(&bar_mem[1 + NK]);
     // A K stage is free once its QK^T has run, a V stage once its P.V has run,
     // so the next K tile can be requested a whole softmax earlier than V.
-    B.k_empty0 = smem_u32(&bar_mem[1 + 2 * NS]);
-    B.v_empty0 = smem_u32(&bar_mem[1 + 3 * NS]);
-    B.s_full0 = smem_u32(&bar_mem[1 + 4 * NS]);
+    B.k_empty0 = smem_u32(&bar_mem[1 + NK + NV]);
+    B.v_empty0 = smem_u32(&bar_mem[1 + 2 * NK + NV]);
+    constexpr int kBarS = 1 + 2 * NK + 2 * NV;
+    B.s_full0 = smem_u32(&bar_mem[kBarS]);
     // Per-parity barriers: softmax warps may run one tile ahead of the MMA
     // warp, so P-ready and PV-done are tracked separately for even and odd
     // tiles (a single barrier could see arrivals of two tiles in one phase).
-    B.p_full = smem_u32(&bar_mem[3 + 4 * NS]);
-    B.o_done = smem_u32(&bar_mem[5 + 4 * NS]);
-    B.drain = smem_u32(&bar_mem[7 + 4 * NS]);
+    B.p_full = smem_u32(&bar_mem[kBarS + 2]);
+    B.o_done = smem_u32(&bar_mem[kBarS + 4]);
+    B.drain = smem_u32(&bar_mem[kBarS + 6]);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
 
     if (threadIdx.x == 0) {
         mbar_init(B.q_full, 1);
-        for (int i = 0; i < NS; ++i) {
+        for (int i = 0; i < NK; ++i) {
             mbar_init(B.k_full0 + 8 * i, 1);
-            mbar_init(B.v_full0 + 8 * i, 1);
             mbar_init(B.k_empty0 + 8 * i, 1);
+        }
+        for (int i = 0; i < NV; ++i) {
+            mbar_init(B.v_full0 + 8 * i, 1);
             mbar_init(B.v_empty0 + 8 * i, 1);
         }
         mbar_init(B.s_full0, 1);
@@ -270,7 +183,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     const uint32_t sQ = smem_u32(smem + C::kOffQ);
     const uint32_t sK = smem_u32(smem + C::kOffK);
     const uint32_t sV = smem_u32(smem + C::kOffV);
-    const uint32_t sP = smem_u32(smem + C::kOffP);
 
     if (warp == kWarpTma) {
         // ------------------------------ TMA producer ------------------------------
@@ -298,7 +210,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         int issued = 0;
         int32_t id_next = n_tiles > 0 ? tile_id(0) : 0;
         for (int j = 0; j < n_tiles; ++j) {
-            const int stg = j % NS;
+            const int stk = j % NK, stv = j % NV;
             const int key0 = (t_begin + j) * BN;
             const int blk0 = key0 / b;
             const int nb = min(BN / b, nblk_seq - blk0);
@@ -307,36 +219,36 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             if (j + 1 < n_tiles) id_next = tile_id(j + 1);
             if (lane < nb && (id < 0 || (int64_t)id >= p.num_blocks))
                 atomicOr(p.err, (int)UA_DEVERR_BLOCK_ID);
-            if (j >= NS && !__all_sync(0xffffffffu, wait_or_abort(B.k_empty0 + 8 * stg, ((j / NS) + 1) & 1,
+            if (j >= NK && !__all_sync(0xffffffffu, wait_or_abort(B.k_empty0 + 8 * stk, ((j / NK) + 1) & 1,
                                                                    abort_flag, p.err)))
                 break;
-            if (lane == 0) mbar_arrive_expect_tx(B.k_full0 + 8 * stg, bytes);
+            if (lane == 0) mbar_arrive_expect_tx(B.k_full0 + 8 * stk, bytes);
             __syncwarp();
             if (lane < nb) {
 #pragma unroll
                 for (int pn = 0; pn < C::kPanels; ++pn)
-                    tma_load_4d(sK + stg * C::kKvBytes + pn * C::kKvPanel + lane * b * 128, &tm_k,
-                                pn * 64, hkv, 0, id, B.k_full0 + 8 * stg);
+                    tma_load_4d(sK + stk * C::kKvBytes + pn * C::kKvPanel + lane * b * 128, &tm_k,
+                                pn * 64, hkv, 0, id, B.k_full0 + 8 * stk);
             }
-            if (j >= NS && !__all_sync(0xffffffffu, wait_or_abort(B.v_empty0 + 8 * stg, ((j / NS) + 1) & 1,
+            if (j >= NV && !__all_sync(0xffffffffu, wait_or_abort(B.v_empty0 + 8 * stv, ((j / NV) + 1) & 1,
                                                                    abort_flag, p.err)))
                 break;
-            if (lane == 0) mbar_arrive_expect_tx(B.v_full0 + 8 * stg, bytes);
+            if (lane == 0) mbar_arrive_expect_tx(B.v_full0 + 8 * stv, bytes);
             __syncwarp();
             if (lane < nb) {
 #pragma unroll
                 for (int pn = 0; pn < C::kPanels; ++pn)
-                    tma_load_4d(sV + stg * C::kKvBytes + pn * C::kKvPanel + lane * b * 128, &tm_v,
-                                pn * 64, hkv, 0, id, B.v_full0 + 8 * stg);
+                    tma_load_4d(sV + stv * C::kKvBytes + pn * C::kKvPanel + lane * b * 128, &tm_v,
+                                pn * 64, hkv, 0, id, B.v_full0 + 8 * stv);
             }
             issued = j + 1;
         }
         if (*abort_flag && lane == 0) {
             // Let every copy this warp issued land before the CTA ends.
-            for (int j = max(0, issued - NS); j < issued; ++j) {
-                mbar_wait_bounded(B.k_full0 + 8 * (j % NS), (j / NS) & 1);
-                mbar_wait_bounded(B.v_full0 + 8 * (j % NS), (j / NS) & 1);
-            }
+            for (int j = max(0, issued - NK); j < issued; ++j)
+                mbar_wait_bounded(B.k_full0 + 8 * (j % NK), (j / NK) & 1);
+            for (int j = max(0, issued - NV); j < issued; ++j)
+                mbar_wait_bounded(B.v_full0 + 8 * (j % NV), (j / NV) & 1);
         }
         __syncwarp();
     } else if (warp == kWarpMma || warp == kWarpPv) {
@@ -355,8 +267,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             bool ok = wwait(B.q_full, 0);
             for (int j = 0; ok && j < n_tiles; ++j) {
                 if (j >= 2 && !wwait(B.p_full + 8 * (j & 1), ((j - 2) >> 1) & 1)) break;
-                const int stg = j % NS;
-                if (!wwait(B.k_full0 + 8 * stg, (j / NS) & 1)) break;
+                const int stg = j % NK;
+                if (!wwait(B.k_full0 + 8 * stg, (j / NK) & 1)) break;
                 tc::fence_after_sync();
                 if (lane == 0) {
                     const uint32_t kst = sK + stg * C::kKvBytes;
@@ -375,9 +287,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             }
         } else {
             for (int j = 0; j < n_tiles; ++j) {
-                const int stg = j % NS;
+                const int stg = j % NV;
                 if (!wwait(B.p_full + 8 * (j & 1), (j >> 1) & 1)) break;
-                if (!wwait(B.v_full0 + 8 * stg, (j / NS) & 1)) break;
+                if (!wwait(B.v_full0 + 8 * stg, (j / NV) & 1)) break;
                 tc::fence_after_sync();
                 const uint32_t vst = sV + stg * C::kKvBytes;
                 const int key0 = (t_begin + j) * BN;
@@ -397,12 +309,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 }
                 if (lane == 0) {
                     const uint32_t dO = tmem + C::kTmemO;
+                    const uint32_t aP = tmem + C::kTmemP + (j & 1) * (BN / 2);
 #pragma unroll
                     for (int k = 0; k < BN / 16; ++k) {
-                        const int pn = k >> 2, off = (k & 3) * 32;
-                        const uint64_t a = tc::smem_desc_sw128(sP + pn * (kRows * 128) + off, 16, 1024);
+                        // A = P from tensor memory: 16 keys per MMA = 8 columns.
                         const uint64_t bdesc = tc::smem_desc_sw128(vst + k * 16 * 128, C::kKvPanel, 1024);
-                        tc::mma_bf16(dO, a, bdesc, idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
+                        tc::mma_bf16_ts(dO, aP + k * 8, bdesc, idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
                     }
                     tc::commit(B.o_done + 8 * (j & 1));
                     tc::commit(B.v_empty0 + 8 * stg);
@@ -540,10 +452,15 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 }
             const float2 rs01 = fadd2(rs[0], rs[1]), rs23 = fadd2(rs[2], rs[3]);
             l = l * alpha + ((rs01.x + rs01.y) + (rs23.x + rs23.y));
-            // The P.V of tile j - 1 must be finished before P is overwritten
-            // and before O is rescaled.
+            // P buffer (j & 1) in tensor memory was read by the P.V of tile
+            // j - 2; rescaling O needs the P.V of tile j - 1 to have finished.
             bool go = true;
-            if (j > 0) {
+            if (j >= 2) {
+                go = __all_sync(0xffffffffu, wait_or_abort(B.o_done + 8 * (j & 1),
+                                                           ((j - 2) >> 1) & 1, abort_flag, p.err));
+                if (go) tc::fence_after_sync();
+            }
+            if (go && live && j > 0 && __any_sync(0xffffffffu, reanchor)) {
                 go = __all_sync(0xffffffffu, wait_or_abort(B.o_done + 8 * ((j - 1) & 1),
                                                            ((j - 1) >> 1) & 1, abort_flag, p.err));
                 if (go) tc::fence_after_sync();
@@ -562,20 +479,20 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 tc::wait_st();
             }
             if (go) {
-                // This part's CPT keys of row r -> 128-byte swizzled K-major
-                // panels of 64 keys (padding-only warps leave their rows stale;
-                // those output rows are never stored).
+                // This part's CPT keys of row r -> tensor-memory P buffer
+                // (j & 1): lane r, two bf16 keys per 32-bit column, the A
+                // operand of the P.V MMA.  Padding-only warps leave their rows
+                // stale; those output rows are never stored.
                 if (live) {
-                uint8_t* prow = smem + C::kOffP + r * 128;
-#pragma unroll
-                for (int q4 = 0; q4 < CPT / 8; ++q4) {
-                    const int chunk = half * (CPT / 8) + q4;  // 8-key chunk within the row
-                    const int pn = chunk >> 3, cc = chunk & 7;
-                    *reinterpret_cast<uint4*>(prow + pn * (kRows * 128) + ((cc ^ (r & 7)) << 4)) =
-                        make_uint4(pk[q4 * 4 + 0], pk[q4 * 4 + 1], pk[q4 * 4 + 2], pk[q4 * 4 + 3]);
+                    const uint32_t pcol = C::kTmemP + (j & 1) * (BN / 2) + half * (CPT / 2);
+                    if constexpr (CPT / 2 == 32) {
+                        tc::st32(trow + pcol, pk);
+                    } else {
+                        static_assert(CPT / 2 == 16, "P columns per thread");
+                        tc::st16(trow + pcol, pk);
+                    }
+                    tc::wait_st();
                 }
-                }
-                fence_proxy_async_smem();
                 tc::fence_before_sync();
                 mbar_arrive(B.p_full + 8 * (j & 1));
             }
@@ -662,12 +579,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     }
 }
 
-template <int D, int BN, int NS, int SPLIT, bool PLAIN>
+template <int D, int BN, int NK, int NV, int SPLIT, bool PLAIN>
 cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                      const FwdParams& p, int tiles, cudaStream_t stream) {
-    using C = PCfg<D, BN, NS, SPLIT>;
+    using C = PCfg<D, BN, NK, NV, SPLIT>;
     constexpr int kThreads = Roles<SPLIT>::kThreads;
-    auto kern = prefill_kernel<D, BN, NS, SPLIT, PLAIN>;
+    auto kern = prefill_kernel<D, BN, NK, NV, SPLIT, PLAIN>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)(tiles * p.splits), (unsigned)p.hk, (unsigned)p.num_seqs);
@@ -688,7 +605,9 @@ void plan_prefill(const FwdParams& p, int num_sms, size_t workspace_bytes, Prefi
     // Split the keys into segments only when the (tile, kv head, sequence)
     // grid is too small to give every SM about four CTAs; each segment keeps
     // at least eight KV tiles.
-    const int64_t base = (int64_t)plan->num_tiles * p.hk * p.num_seqs;
+    // CTAs per (sequence, kv head): tile pairs where the pair kernel serves d.
+    const int ctas = prefill_pair_supported(p.d) ? (plan->num_tiles + 1) / 2 : plan->num_tiles;
+    const int64_t base = (int64_t)ctas * p.hk * p.num_seqs;
     int splits = 1;
     if (base < 4LL * num_sms) {
         const int64_t want = (4LL * num_sms + base - 1) / base;
@@ -721,19 +640,21 @@ cudaError_t launch_prefill(const PrefillPlan& plan, const CUtensorMap& tm_k, con
     cuuint32_t box[3] = {64, (cuuint32_t)p.g, (cuuint32_t)(kRows / p.g)};
     if (!encode_bf16_sw128(&tq, p.q, 3, dims, strides, box)) return cudaErrorInvalidValue;
     if (plan.num_tiles <= 0) return cudaSuccess;
+    if (prefill_pair_supported(p.d))
+        return launch_prefill_pair(tq, tm_k, tm_v, p, (plan.num_tiles + 1) / 2, stream);
     const bool plain = (p.flags & (UA_FLAG_SOFTCAP | UA_FLAG_ALIBI)) == 0;
     switch (p.d) {
         // Plain scores: two softmax warpgroups per row.  With softcap / ALiBi
         // the per-score work doubles, so d = 128 spreads it over four.
         case 64:
-            return plain ? launch_t<64, 128, 4, 2, true>(tq, tm_k, tm_v, p, plan.num_tiles, stream)
-                         : launch_t<64, 128, 4, 2, false>(tq, tm_k, tm_v, p, plan.num_tiles, stream);
+            return plain ? launch_t<64, 128, 4, 4, 2, true>(tq, tm_k, tm_v, p, plan.num_tiles, stream)
+                         : launch_t<64, 128, 4, 4, 2, false>(tq, tm_k, tm_v, p, plan.num_tiles, stream);
         case 128:
-            return plain ? launch_t<128, 128, 2, 2, true>(tq, tm_k, tm_v, p, plan.num_tiles, stream)
-                         : launch_t<128, 128, 2, 4, false>(tq, tm_k, tm_v, p, plan.num_tiles, stream);
+            return plain ? launch_t<128, 128, 2, 3, 2, true>(tq, tm_k, tm_v, p, plan.num_tiles, stream)
+                         : launch_t<128, 128, 2, 3, 4, false>(tq, tm_k, tm_v, p, plan.num_tiles, stream);
         case 256:
-            return plain ? launch_t<256, 64, 2, 2, true>(tq, tm_k, tm_v, p, plan.num_tiles, stream)
-                         : launch_t<256, 64, 2, 2, false>(tq, tm_k, tm_v, p, plan.num_tiles, stream);
+            return plain ? launch_t<256, 64, 2, 2, 2, true>(tq, tm_k, tm_v, p, plan.num_tiles, stream)
+                         : launch_t<256, 64, 2, 2, 2, false>(tq, tm_k, tm_v, p, plan.num_tiles, stream);
         default: return cudaErrorInvalidValue;
     }
 }

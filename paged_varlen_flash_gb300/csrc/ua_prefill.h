@@ -24,6 +24,15 @@ bool prefill_shape_ok(const FwdParams& p);
 // `workspace_bytes` of the problem workspace.
 void plan_prefill(const FwdParams& p, int num_sms, size_t workspace_bytes, PrefillPlan* plan);
 
+// Head sizes served by the two-tiles-per-CTA kernel (256 query rows share each
+// K/V tile); the others use one 128-row tile per CTA.
+bool prefill_pair_supported(int d);
+
+// Enqueue the two-tiles-per-CTA kernel over `pairs` tile pairs per (sequence,
+// kv head); tq is the Q tensor map (boxes of the tile's 128 packed rows).
+cudaError_t launch_prefill_pair(const CUtensorMap& tq, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                                const FwdParams& p, int pairs, cudaStream_t stream);
+
 // Enqueue the prefill path (p.out receives the final bf16 rows).
 cudaError_t launch_prefill(const PrefillPlan& plan, const CUtensorMap& tm_k,
                            const CUtensorMap& tm_v, const FwdParams& p, cudaStream_t stream);
