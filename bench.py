@@ -41,7 +41,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 KERNEL_SOURCES = {
     "split_kernel": ["ua_split.cu", "ua_ptx.cuh", "ua_common.cuh"],
-    "prefill_kernel": ["ua_prefill.cu", "ua_ptx.cuh", "ua_common.cuh", "ua_tc.cuh"],
+    "prefill_kernel": ["ua_prefill.cu", "ua_prefill_common.cuh", "ua_ptx.cuh", "ua_common.cuh", "ua_tc.cuh"],
+    "prefill_pair_kernel": ["ua_prefill_pair.cu", "ua_prefill_common.cuh", "ua_ptx.cuh", "ua_common.cuh",
+                            "ua_tc.cuh"],
     "decode_tc_kernel": ["ua_decode_tc.cu", "ua_ptx.cuh", "ua_common.cuh", "ua_tc.cuh"],
 }
 
@@ -176,6 +178,8 @@ def dominant_kernel(path):
     library reports (the combine kernel is ~2% of a split call)."""
     if path.startswith("decode_tc"):
         return "decode_tc_kernel"
+    if path.startswith("tensor_core_pair"):
+        return "prefill_pair_kernel"
     if path.startswith("tensor_core"):
         return "prefill_kernel"
     return "split_kernel"

@@ -343,7 +343,10 @@ ua_status ua_forward(ua_problem* p, const void* q, const void* k_cache, const vo
             }
         }
         p->last_launches = plan.launches;
-        p->last_path = plan.splits > 1 ? "tensor_core+combine" : "tensor_core";
+        if (ua::prefill_pair_supported(fp.d))
+            p->last_path = plan.splits > 1 ? "tensor_core_pair+combine" : "tensor_core_pair";
+        else
+            p->last_path = plan.splits > 1 ? "tensor_core+combine" : "tensor_core";
         return UA_OK;
     }
 
