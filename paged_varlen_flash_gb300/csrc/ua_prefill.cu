@@ -35,6 +35,14 @@
 #include "ua_tc.cuh"
 #include "ua_tmap.h"
 
+// Cluster size of the d = 256 kernel: 2 shares each K/V tile between two
+// CTAs on adjacent query tiles through TMA multicast.  Measured on the wide
+// MHA prefill it is slower than one CTA per tile (the coupled CTAs wait on
+// each other's releases), so 1 is the default.
+#ifndef UA_PF256_CL
+#define UA_PF256_CL 1
+#endif
+
 namespace ua {
 namespace {
 
@@ -66,7 +74,13 @@ struct PCfg {
     static_assert(kSmem <= 232448, "shared memory budget");
 };
 
-template <int D, int BN, int NK, int NV, int SPLIT, bool PLAIN>
+// CL = 2: the CTA is one of a cluster of two working on adjacent query tiles
+// of the same (sequence, KV head, segment).  Each CTA fetches half of every
+// K/V tile's head-dim panels and multicasts them to both, so each SM's copy
+// engine moves half the bytes per flop; a stage is reloaded only after both
+// CTAs' MMAs released it.  Both CTAs walk the union of their key ranges (a
+// row still masks keys outside its own range).
+template <int D, int BN, int NK, int NV, int SPLIT, bool PLAIN, int CL>
 __global__ void __launch_bounds__(Roles<SPLIT>::kThreads, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
@@ -85,25 +99,39 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     const int s = blockIdx.z;
     const int hkv = blockIdx.y;
     const bool split = p.splits > 1;             // write (m, l, o) partials per KV segment
-    const int seg = blockIdx.x % p.splits;
-    const int qt = (int)(gridDim.x / p.splits) - 1 - (int)(blockIdx.x / p.splits);  // heaviest first
+    static_assert(CL == 1 || CL == 2, "cluster size");
+    uint32_t rank = 0;
+    int seg, qt;
+    if constexpr (CL == 2) {
+        rank = cluster_ctarank();
+        const int cx = (int)(blockIdx.x >> 1);   // cluster index along x
+        const int npairs = (int)(gridDim.x >> 1) / p.splits;
+        seg = cx % p.splits;
+        qt = 2 * (npairs - 1 - cx / p.splits) + (int)rank;   // heaviest pairs first
+    } else {
+        seg = blockIdx.x % p.splits;
+        qt = (int)(gridDim.x / p.splits) - 1 - (int)(blockIdx.x / p.splits);  // heaviest first
+    }
     const int g = p.g;
     const int ppt = kRows / g;                  // positions per tile
     const int p0 = qt * ppt;
+    const int pc0 = (qt - (int)rank) * ppt;     // first position of the cluster's tiles
 
     int sq, sk;
     int64_t q0;
     const uint32_t st = seq_status(p, s, sq, sk, q0);
     if (st && qt == 0 && hkv == 0 && seg == 0 && threadIdx.x == 0) atomicOr(p.err, (int)st);
+    // Every early exit below is taken by both CTAs of a cluster or by neither.
     if (st & UA_DEVERR_CU_SEQLENS) return;
-    if (p0 >= sq) return;
+    if (pc0 >= sq) return;
     if (seg >= (split ? seq_segments(p, st, sk) : 1)) return;
-    const int p_last = min(p0 + ppt, sq) - 1;
+    const int p_last = min(p0 + ppt, sq) - 1;   // < p0: this tile lies past the sequence (CL = 2)
+    const int pc_last = min(pc0 + CL * ppt, sq) - 1;
     const int ctx = sk - sq;
     const bool causal = (p.flags & UA_FLAG_CAUSAL) != 0;
     const bool window = (p.flags & UA_FLAG_WINDOW) != 0;
-    int k_end = causal ? min(sk, p_last + ctx + 1) : sk;
-    int k_beg = window ? max(0, p0 + ctx - p.window + 1) : 0;
+    int k_end = causal ? min(sk, pc_last + ctx + 1) : sk;
+    int k_beg = window ? max(0, pc0 + ctx - p.window + 1) : 0;
     if (split) {  // this CTA's KV segment; segments are whole BN tiles
         k_beg = max(k_beg, seg * p.chunk);
         k_end = min(k_end, seg * p.chunk + p.chunk);
@@ -129,6 +157,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     }
     const int t_begin = k_beg / BN;
     const int n_tiles = (k_end + BN - 1) / BN - t_begin;
+    // Step j visits key tile t_last - j: from the diagonal backwards.  The
+    // result does not depend on the order; with causal ALiBi the scores grow
+    // toward the diagonal, so this order meets each row's largest scores
+    // first and the running max (and O) rarely needs re-anchoring.
+    const int t_last = t_begin + n_tiles - 1;
 
     uint64_t* bar_mem = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
     Bars B;
@@ -154,11 +187,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         mbar_init(B.q_full, 1);
         for (int i = 0; i < NK; ++i) {
             mbar_init(B.k_full0 + 8 * i, 1);
-            mbar_init(B.k_empty0 + 8 * i, 1);
+            mbar_init(B.k_empty0 + 8 * i, CL);   // one release per CTA of the cluster
         }
         for (int i = 0; i < NV; ++i) {
             mbar_init(B.v_full0 + 8 * i, 1);
-            mbar_init(B.v_empty0 + 8 * i, 1);
+            mbar_init(B.v_empty0 + 8 * i, CL);
         }
         mbar_init(B.s_full0, 1);
         mbar_init(B.s_full0 + 8, 1);
@@ -176,7 +209,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         tc::tmem_relinquish();
     }
     tc::fence_before_sync();
-    __syncthreads();
+    // With a cluster: no copy lands in, and no release arrives at, the peer
+    // before its barriers exist.
+    if constexpr (CL == 2) cluster_sync(); else __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
 
@@ -204,20 +239,20 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         // Block ids are fetched one tile ahead so their load latency overlaps
         // the current tile's waits and copies.
         auto tile_id = [&](int j) -> int32_t {
-            const int blk0 = (t_begin + j) * BN / b;
+            const int blk0 = (t_last - j) * BN / b;
             return lane < min(BN / b, nblk_seq - blk0) ? __ldg(bt + blk0 + lane) : 0;
         };
         int issued = 0;
         int32_t id_next = n_tiles > 0 ? tile_id(0) : 0;
         for (int j = 0; j < n_tiles; ++j) {
             const int stk = j % NK, stv = j % NV;
-            const int key0 = (t_begin + j) * BN;
+            const int key0 = (t_last - j) * BN;
             const int blk0 = key0 / b;
             const int nb = min(BN / b, nblk_seq - blk0);
             const uint32_t bytes = (uint32_t)nb * b * 128 * C::kPanels;
             const int32_t id = id_next;
             if (j + 1 < n_tiles) id_next = tile_id(j + 1);
-            if (lane < nb && (id < 0 || (int64_t)id >= p.num_blocks))
+            if (rank == 0 && lane < nb && (id < 0 || (int64_t)id >= p.num_blocks))
                 atomicOr(p.err, (int)UA_DEVERR_BLOCK_ID);
             if (j >= NK && !__all_sync(0xffffffffu, wait_or_abort(B.k_empty0 + 8 * stk, ((j / NK) + 1) & 1,
                                                                    abort_flag, p.err)))
@@ -226,9 +261,14 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             __syncwarp();
             if (lane < nb) {
 #pragma unroll
-                for (int pn = 0; pn < C::kPanels; ++pn)
-                    tma_load_4d(sK + stk * C::kKvBytes + pn * C::kKvPanel + lane * b * 128, &tm_k,
-                                pn * 64, hkv, 0, id, B.k_full0 + 8 * stk);
+                for (int q = 0; q < C::kPanels / CL; ++q) {
+                    const int pn = (int)rank * (C::kPanels / CL) + q;
+                    const uint32_t dst = sK + stk * C::kKvBytes + pn * C::kKvPanel + lane * b * 128;
+                    if constexpr (CL == 2)
+                        tma_load_4d_mc(dst, &tm_k, pn * 64, hkv, 0, id, B.k_full0 + 8 * stk, 0x3);
+                    else
+                        tma_load_4d(dst, &tm_k, pn * 64, hkv, 0, id, B.k_full0 + 8 * stk);
+                }
             }
             if (j >= NV && !__all_sync(0xffffffffu, wait_or_abort(B.v_empty0 + 8 * stv, ((j / NV) + 1) & 1,
                                                                    abort_flag, p.err)))
@@ -237,9 +277,14 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             __syncwarp();
             if (lane < nb) {
 #pragma unroll
-                for (int pn = 0; pn < C::kPanels; ++pn)
-                    tma_load_4d(sV + stv * C::kKvBytes + pn * C::kKvPanel + lane * b * 128, &tm_v,
-                                pn * 64, hkv, 0, id, B.v_full0 + 8 * stv);
+                for (int q = 0; q < C::kPanels / CL; ++q) {
+                    const int pn = (int)rank * (C::kPanels / CL) + q;
+                    const uint32_t dst = sV + stv * C::kKvBytes + pn * C::kKvPanel + lane * b * 128;
+                    if constexpr (CL == 2)
+                        tma_load_4d_mc(dst, &tm_v, pn * 64, hkv, 0, id, B.v_full0 + 8 * stv, 0x3);
+                    else
+                        tma_load_4d(dst, &tm_v, pn * 64, hkv, 0, id, B.v_full0 + 8 * stv);
+                }
             }
             issued = j + 1;
         }
@@ -281,7 +326,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                         tc::mma_bf16(dS, a, bdesc, idesc_qk, k > 0 ? 1u : 0u);
                     }
                     tc::commit(B.s_full0 + 8 * (j & 1));
-                    tc::commit(B.k_empty0 + 8 * stg);
+                    if constexpr (CL == 2) {
+                        // Release the stage in both CTAs (only if it is reloaded:
+                        // no arrival may be in flight to a CTA that has finished).
+                        if (j + NK < n_tiles) tc::commit_mc(B.k_empty0 + 8 * stg, 0x3);
+                    } else {
+                        tc::commit(B.k_empty0 + 8 * stg);
+                    }
                 }
                 __syncwarp();
             }
@@ -292,7 +343,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 if (!wwait(B.v_full0 + 8 * stg, (j / NV) & 1)) break;
                 tc::fence_after_sync();
                 const uint32_t vst = sV + stg * C::kKvBytes;
-                const int key0 = (t_begin + j) * BN;
+                const int key0 = (t_last - j) * BN;
                 const int nvalid = min(BN, sk - key0);
                 if (nvalid < BN) {
                     // Keys past S_k: whatever those slots hold must not reach O
@@ -317,7 +368,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                         tc::mma_bf16_ts(dO, aP + k * 8, bdesc, idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
                     }
                     tc::commit(B.o_done + 8 * (j & 1));
-                    tc::commit(B.v_empty0 + 8 * stg);
+                    if constexpr (CL == 2) {
+                        if (j + NV < n_tiles) tc::commit_mc(B.v_empty0 + 8 * stg, 0x3);
+                    } else {
+                        tc::commit(B.v_empty0 + 8 * stg);
+                    }
                 }
                 __syncwarp();
             }
@@ -348,6 +403,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         const bool alibi = (p.flags & UA_FLAG_ALIBI) != 0;
         const float sl2 = p.scale * kLog2e;
         const float slope = alibi ? __ldg(p.alibi + head) : 0.f;
+        const float inv_cap = softcap ? 1.0f / p.softcap : 0.f;
         const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16);
         float* red = reinterpret_cast<float*>(smem + C::kOffRed);
         // Keys every row of the tile sees: [kfree_lo, kfree_hi].
@@ -365,7 +421,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             const bool got = __all_sync(0xffffffffu, wait_or_abort(B.s_full0 + 8 * (j & 1), (j >> 1) & 1,
                                                                    abort_flag, p.err));
             uint32_t sr[CPT / 32][32];
-            const int key0 = (t_begin + j) * BN + half * CPT;
+            const int key0 = (t_last - j) * BN + half * CPT;
             float pmax = -INFINITY;
             if (got && live) {
                 tc::fence_after_sync();
@@ -375,13 +431,16 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 tc::wait_ld();
                 const bool mask_free = key0 >= kfree_lo && key0 + CPT - 1 <= kfree_hi;
                 if constexpr (!PLAIN) {
+                    // ALiBi: one int -> float conversion per tile; the per-key
+                    // offsets are compile-time constants.
+                    const float abias = slope * (float)(key0 - ctx);
 #pragma unroll
                     for (int c = 0; c < CPT / 32; ++c)
 #pragma unroll
                         for (int e = 0; e < 32; ++e) {
                             float t = __uint_as_float(sr[c][e]) * p.scale;
-                            if (softcap) t = p.softcap * tanh_via_exp2(t / p.softcap);
-                            if (alibi) t += slope * (float)(key0 + c * 32 + e - ctx);
+                            if (softcap) t = p.softcap * tanh_via_exp2(t * inv_cap);
+                            if (alibi) t += abias + slope * (float)(c * 32 + e);
                             sr[c][e] = __float_as_uint(t * kLog2e);
                         }
                 }
@@ -432,9 +491,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             const float m_use = (m == -INFINITY) ? 0.f : m;
             const float xs = PLAIN ? sl2 : 1.0f;
             // P = 2^(x - m): the exponent argument in fp32 (packed pairs), the
-            // power of two on the fp16x2 special-function path (two results per
-            // instruction; fp16's 11-bit significand is finer than the bf16 P
-            // the MMA consumes).  Row sums stay fp32.
+            // power of two on the fp32 special-function path, row sums in fp32,
+            // P rounded to bf16 for the MMA.
             float2 rs[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                             make_float2(0.f, 0.f)};
             const float2 sc2 = make_float2(xs, xs);
@@ -446,7 +504,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 for (int e = 0; e < 32; e += 2) {
                     const float2 a = ffma2(make_float2(__uint_as_float(sr[c][e]), __uint_as_float(sr[c][e + 1])),
                                            sc2, nm2);
-                    const float2 pr = exp2_pair_f16(a);
+                    const float2 pr = exp2_pair_f32(a);
                     rs[(e >> 1) & 3] = fadd2(rs[(e >> 1) & 3], pr);
                     pk[(c * 32 + e) / 2] = pack_bf16x2(pr.x, pr.y);
                 }
@@ -572,24 +630,40 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     }
 
     tc::fence_before_sync();
-    __syncthreads();
+    // With a cluster: neither CTA leaves while the other may still write into
+    // its shared memory.
+    if constexpr (CL == 2) cluster_sync(); else __syncthreads();
     if (warp == kWarpMma) {
         tc::fence_after_sync();
         tc::tmem_dealloc(tmem, kTmemCols);
     }
 }
 
-template <int D, int BN, int NK, int NV, int SPLIT, bool PLAIN>
+template <int D, int BN, int NK, int NV, int SPLIT, bool PLAIN, int CL>
 cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                      const FwdParams& p, int tiles, cudaStream_t stream) {
     using C = PCfg<D, BN, NK, NV, SPLIT>;
     constexpr int kThreads = Roles<SPLIT>::kThreads;
-    auto kern = prefill_kernel<D, BN, NK, NV, SPLIT, PLAIN>;
+    auto kern = prefill_kernel<D, BN, NK, NV, SPLIT, PLAIN, CL>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
-    dim3 grid((unsigned)(tiles * p.splits), (unsigned)p.hk, (unsigned)p.num_seqs);
-    kern<<<grid, kThreads, C::kSmem, stream>>>(tq, tk, tv, p);
-    return cudaGetLastError();
+    // With clusters of two, grid x holds (pair, segment, rank); an odd tile
+    // count leaves the last pair's second tile empty (it still fetches its
+    // half of each K/V tile).
+    const int units = CL == 2 ? (tiles + 1) / 2 * 2 : tiles;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(units * p.splits), (unsigned)p.hk, (unsigned)p.num_seqs);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = C::kSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CL;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, p);
 }
 
 }  // namespace
@@ -643,20 +717,9 @@ cudaError_t launch_prefill(const PrefillPlan& plan, const CUtensorMap& tm_k, con
     if (prefill_pair_supported(p.d))
         return launch_prefill_pair(tq, tm_k, tm_v, p, (plan.num_tiles + 1) / 2, stream);
     const bool plain = (p.flags & (UA_FLAG_SOFTCAP | UA_FLAG_ALIBI)) == 0;
-    switch (p.d) {
-        // Plain scores: two softmax warpgroups per row.  With softcap / ALiBi
-        // the per-score work doubles, so d = 128 spreads it over four.
-        case 64:
-            return plain ? launch_t<64, 128, 4, 4, 2, true>(tq, tm_k, tm_v, p, plan.num_tiles, stream)
-                         : launch_t<64, 128, 4, 4, 2, false>(tq, tm_k, tm_v, p, plan.num_tiles, stream);
-        case 128:
-            return plain ? launch_t<128, 128, 2, 3, 2, true>(tq, tm_k, tm_v, p, plan.num_tiles, stream)
-                         : launch_t<128, 128, 2, 3, 4, false>(tq, tm_k, tm_v, p, plan.num_tiles, stream);
-        case 256:
-            return plain ? launch_t<256, 64, 2, 2, 2, true>(tq, tm_k, tm_v, p, plan.num_tiles, stream)
-                         : launch_t<256, 64, 2, 2, 2, false>(tq, tm_k, tm_v, p, plan.num_tiles, stream);
-        default: return cudaErrorInvalidValue;
-    }
+    if (p.d != 256) return cudaErrorInvalidValue;
+    return plain ? launch_t<256, 64, 2, 2, 2, true, UA_PF256_CL>(tq, tm_k, tm_v, p, plan.num_tiles, stream)
+                 : launch_t<256, 64, 2, 2, 2, false, UA_PF256_CL>(tq, tm_k, tm_v, p, plan.num_tiles, stream);
 }
 
 }  // namespace ua
