@@ -1,29 +1,33 @@
-// ua_prefill.cu -- prefill / chunked-prefill attention on the tcgen05 tensor
-// cores of sm_103a.
+// ua_prefill.cu -- prefill / chunked-prefill attention for head size 256 on
+// the tcgen05 tensor cores of sm_103a (head sizes 64 and 128 use the two-tile
+// kernel of ua_prefill_pair.cu), plus the prefill planner and launcher.
 //
 // Work unit: one CTA per (tile of 128 packed (position, head) rows of one KV
-// head, sequence).  The g query heads that share a KV head are packed into the
-// tile's rows, so one QK^T MMA serves the whole group (gfx950 "Unified paged
-// attention on gfx950, from the math up", section 4, GQA packing).  The CTA
-// walks its visible KV tiles with the streaming (m, l, o) recurrence of
-// gfx1151 ALGORITHM.md section 3, in base 2 (gfx950 section 2), with the lazy
-// re-anchor threshold of 8 and the loop split into mask-free and masked tiles
-// plus the causal early exit and the sliding-window start tile of
-// attention_dense.py (section 8.1 of the gfx950 page).
+// head, sequence[, KV segment]).  The g query heads that share a KV head are
+// packed into the tile's rows, so one QK^T MMA serves the whole group (gfx950
+// "Unified paged attention on gfx950, from the math up", section 4, GQA
+// packing).  The CTA walks its visible KV tiles with the streaming (m, l, o)
+// recurrence of gfx1151 ALGORITHM.md section 3, in base 2 (gfx950 section 2),
+// with the lazy re-anchor threshold of 8, mask-free interior tiles and the
+// causal early exit and sliding-window start tile of attention_dense.py
+// (section 8.1 of the gfx950 page).  Key tiles are visited from the diagonal
+// backwards (the result does not depend on the order).
 //
-// Roles (6 warps):
-//   warps 0-3  softmax + epilogue: thread r owns row r of the tile, which is
-//              also tensor-memory lane r, so row max and row sum need no
-//              cross-thread reduction;
-//   warp 4     TMA producer: Q tile once (a 3-D box of g heads x 128/g
-//              positions), then K and V tiles through NK- and NV-stage rings, one box
-//              per (paged block, 64-wide head-dim panel), block ids read from
-//              the block table;
-//   warp 5     tensor-memory allocator and MMA issuer: S = Q K^T into one of two
-//              tensor-memory S buffers, then O += P V with P (bf16) staged in
-//              shared memory and V read MN-major straight from its TMA tile.
+// Roles (11 warps):
+//   warps 0-7  softmax + epilogue: two warpgroups share each row's BN key
+//              columns (one shared-memory max exchange per tile); thread
+//              (part, r) owns row r, which is tensor-memory lane r;
+//   warp 8     TMA producer: Q tile once (a 3-D box of g heads x 128/g
+//              positions), then K and V tiles through NK- and NV-stage rings,
+//              one box per (paged block, 64-wide head-dim panel), block ids
+//              read from the block table one tile ahead;
+//   warp 9     tensor-memory allocator and QK^T issuer;
+//   warp 10    P.V issuer (P bf16 from tensor memory, V MN-major straight
+//              from its TMA tile).
 //
-// Tensor memory (512 columns): S0 [0, BN), S1 [BN, 2 BN), O [2 BN, 2 BN + D).
+// Tensor memory (512 columns): S0 [0, BN), S1 [BN, 2 BN), O [2 BN, 2 BN + D),
+// three bf16 P buffers after O (the softmax writing P(j) waits only for the
+// P.V of tile j - 3).
 #include <algorithm>
 #include <cstdint>
 #include <cstring>
@@ -61,16 +65,16 @@ struct PCfg {
     static constexpr int kOffV = kOffK + NK * kKvBytes;
     static constexpr int kOffP = kOffV + NV * kKvBytes;
     static constexpr int kOffBar = kOffP + kPBytes;
-    // q_full, k_full[NK], v_full[NV], k_empty[NK], v_empty[NV], s_full[2], p_full[2],
-    // o_done[2], drain[2]
-    static constexpr int kNumBars = 1 + 2 * NK + 2 * NV + 2 + 2 + 2 + 2;
+    // q_full, k_full[NK], v_full[NV], k_empty[NK], v_empty[NV], s_full[2],
+    // p_full[3], o_done[3] (per P buffer), drain[2]
+    static constexpr int kNumBars = 1 + 2 * NK + 2 * NV + 2 + 3 + 3 + 2;
     static constexpr int kOffRed = kOffBar + kNumBars * 8;      // [2 parity][SPLIT][128] fp32
     static constexpr int kOffMisc = kOffRed + 2 * SPLIT * kRows * 4;
     static constexpr int kSmem = kOffMisc + 16 + 1024;
     static constexpr int kTmemS = 0;
     static constexpr int kTmemO = 2 * BN;
-    static constexpr int kTmemP = 2 * BN + D;   // two bf16 P buffers of BN / 2 columns
-    static_assert(2 * BN + D + BN <= (int)kTmemCols, "tensor memory budget");
+    static constexpr int kTmemP = 2 * BN + D;   // three bf16 P buffers of BN / 2 columns
+    static_assert(2 * BN + D + 3 * (BN / 2) <= (int)kTmemCols, "tensor memory budget");
     static_assert(kSmem <= 232448, "shared memory budget");
 };
 
@@ -177,9 +181,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     // Per-parity barriers: softmax warps may run one tile ahead of the MMA
     // warp, so P-ready and PV-done are tracked separately for even and odd
     // tiles (a single barrier could see arrivals of two tiles in one phase).
-    B.p_full = smem_u32(&bar_mem[kBarS + 2]);
-    B.o_done = smem_u32(&bar_mem[kBarS + 4]);
-    B.drain = smem_u32(&bar_mem[kBarS + 6]);
+    B.p_full = smem_u32(&bar_mem[kBarS + 2]);   // P buffer j % 3 written
+    B.o_done = smem_u32(&bar_mem[kBarS + 5]);   // the P.V reading buffer j % 3 done
+    B.drain = smem_u32(&bar_mem[kBarS + 8]);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
 
@@ -195,10 +199,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         }
         mbar_init(B.s_full0, 1);
         mbar_init(B.s_full0 + 8, 1);
-        mbar_init(B.p_full, kSmThreads);
-        mbar_init(B.p_full + 8, kSmThreads);
-        mbar_init(B.o_done, 1);
-        mbar_init(B.o_done + 8, 1);
+        for (int x = 0; x < 3; ++x) {
+            mbar_init(B.p_full + 8 * x, kSmThreads);
+            mbar_init(B.o_done + 8 * x, 1);
+        }
         mbar_init(B.drain, 1);
         mbar_init(B.drain + 8, 1);
         *abort_flag = 0;
@@ -311,7 +315,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         if (warp == kWarpMma) {
             bool ok = wwait(B.q_full, 0);
             for (int j = 0; ok && j < n_tiles; ++j) {
-                if (j >= 2 && !wwait(B.p_full + 8 * (j & 1), ((j - 2) >> 1) & 1)) break;
+                if (j >= 2 && !wwait(B.p_full + 8 * ((j - 2) % 3), ((j - 2) / 3) & 1)) break;
                 const int stg = j % NK;
                 if (!wwait(B.k_full0 + 8 * stg, (j / NK) & 1)) break;
                 tc::fence_after_sync();
@@ -339,7 +343,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         } else {
             for (int j = 0; j < n_tiles; ++j) {
                 const int stg = j % NV;
-                if (!wwait(B.p_full + 8 * (j & 1), (j >> 1) & 1)) break;
+                if (!wwait(B.p_full + 8 * (j % 3), (j / 3) & 1)) break;
                 if (!wwait(B.v_full0 + 8 * stg, (j / NV) & 1)) break;
                 tc::fence_after_sync();
                 const uint32_t vst = sV + stg * C::kKvBytes;
@@ -360,14 +364,14 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 }
                 if (lane == 0) {
                     const uint32_t dO = tmem + C::kTmemO;
-                    const uint32_t aP = tmem + C::kTmemP + (j & 1) * (BN / 2);
+                    const uint32_t aP = tmem + C::kTmemP + (j % 3) * (BN / 2);
 #pragma unroll
                     for (int k = 0; k < BN / 16; ++k) {
                         // A = P from tensor memory: 16 keys per MMA = 8 columns.
                         const uint64_t bdesc = tc::smem_desc_sw128(vst + k * 16 * 128, C::kKvPanel, 1024);
                         tc::mma_bf16_ts(dO, aP + k * 8, bdesc, idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
                     }
-                    tc::commit(B.o_done + 8 * (j & 1));
+                    tc::commit(B.o_done + 8 * (j % 3));
                     if constexpr (CL == 2) {
                         if (j + NV < n_tiles) tc::commit_mc(B.v_empty0 + 8 * stg, 0x3);
                     } else {
@@ -510,17 +514,17 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 }
             const float2 rs01 = fadd2(rs[0], rs[1]), rs23 = fadd2(rs[2], rs[3]);
             l = l * alpha + ((rs01.x + rs01.y) + (rs23.x + rs23.y));
-            // P buffer (j & 1) in tensor memory was read by the P.V of tile
-            // j - 2; rescaling O needs the P.V of tile j - 1 to have finished.
+            // P buffer j % 3 in tensor memory was read by the P.V of tile
+            // j - 3; rescaling O needs the P.V of tile j - 1 to have finished.
             bool go = true;
-            if (j >= 2) {
-                go = __all_sync(0xffffffffu, wait_or_abort(B.o_done + 8 * (j & 1),
-                                                           ((j - 2) >> 1) & 1, abort_flag, p.err));
+            if (j >= 3) {
+                go = __all_sync(0xffffffffu, wait_or_abort(B.o_done + 8 * (j % 3),
+                                                           ((j - 3) / 3) & 1, abort_flag, p.err));
                 if (go) tc::fence_after_sync();
             }
             if (go && live && j > 0 && __any_sync(0xffffffffu, reanchor)) {
-                go = __all_sync(0xffffffffu, wait_or_abort(B.o_done + 8 * ((j - 1) & 1),
-                                                           ((j - 1) >> 1) & 1, abort_flag, p.err));
+                go = __all_sync(0xffffffffu, wait_or_abort(B.o_done + 8 * ((j - 1) % 3),
+                                                           ((j - 1) / 3) & 1, abort_flag, p.err));
                 if (go) tc::fence_after_sync();
             }
             if (go && live && j > 0 && __any_sync(0xffffffffu, reanchor)) {
@@ -538,11 +542,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             }
             if (go) {
                 // This part's CPT keys of row r -> tensor-memory P buffer
-                // (j & 1): lane r, two bf16 keys per 32-bit column, the A
+                // j % 3: lane r, two bf16 keys per 32-bit column, the A
                 // operand of the P.V MMA.  Padding-only warps leave their rows
                 // stale; those output rows are never stored.
                 if (live) {
-                    const uint32_t pcol = C::kTmemP + (j & 1) * (BN / 2) + half * (CPT / 2);
+                    const uint32_t pcol = C::kTmemP + (j % 3) * (BN / 2) + half * (CPT / 2);
                     if constexpr (CPT / 2 == 32) {
                         tc::st32(trow + pcol, pk);
                     } else {
@@ -552,14 +556,14 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     tc::wait_st();
                 }
                 tc::fence_before_sync();
-                mbar_arrive(B.p_full + 8 * (j & 1));
+                mbar_arrive(B.p_full + 8 * (j % 3));
             }
         }
         // ------------------------------ epilogue ---------------------------------
         if (ok) {
             const bool done = __all_sync(0xffffffffu,
-                                         wait_or_abort(B.o_done + 8 * ((n_tiles - 1) & 1),
-                                                       ((n_tiles - 1) >> 1) & 1, abort_flag, p.err));
+                                         wait_or_abort(B.o_done + 8 * ((n_tiles - 1) % 3),
+                                                       ((n_tiles - 1) / 3) & 1, abort_flag, p.err));
             red[half * kRows + r] = l;
             const bool all_done = bar_and_sync(1, kSmThreads, done);
             if (all_done && live && split) {

@@ -433,13 +433,16 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 tc::wait_ld();
                 const bool mask_free = key0 >= kfree_lo && key0 + kBN - 1 <= kfree_hi;
                 if constexpr (!PLAIN) {
+                    // ALiBi: one int -> float conversion per tile; the per-key
+                    // offsets are compile-time constants.
+                    const float abias = slope * (float)(key0 - ctx);
 #pragma unroll
                     for (int c = 0; c < kBN / 32; ++c)
 #pragma unroll
                         for (int e = 0; e < 32; ++e) {
                             float t = __uint_as_float(sr[c][e]) * p.scale;
                             if (softcap) t = p.softcap * tanh_via_exp2(t * inv_cap);
-                            if (alibi) t += slope * (float)(key0 + c * 32 + e - ctx);
+                            if (alibi) t += abias + slope * (float)(c * 32 + e);
                             sr[c][e] = __float_as_uint(t * kLog2e);
                         }
                 }
