@@ -9,9 +9,11 @@ evaluates and the passages it follows).  This module only marshals numpy /
 torch CPU arrays into that library.
 
 Parity status: every term of the definition is pinned by the closed-form and
-invariant tests in ``tests/test_oracle_pins.py``; the one part left unpinned is
-the absolute accuracy of libm's ``tanh`` inside the softcap term, which is far
-below any tolerance used against the GPU.
+invariant tests in ``tests/test_oracle_pins.py`` (the e4m3 decoder of the fp8
+KV cache against PyTorch's float8_e4m3fn conversion for all 256 codes, and
+fp8 attention against the same attention on the decoded values); the one
+part left unpinned is the absolute accuracy of libm's ``tanh`` inside the
+softcap term, which is far below any tolerance used against the GPU.
 """
 import ctypes
 import os
@@ -45,7 +47,7 @@ def _load():
         common = [ctypes.c_int32] * 5 + [ctypes.c_int64] + [ctypes.c_void_p] * 4 + [
             ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_double,
             ctypes.c_int32, ctypes.c_double, ctypes.c_int32, ctypes.c_void_p,
-            ctypes.c_void_p]
+            ctypes.c_void_p, ctypes.c_int32, ctypes.c_double, ctypes.c_double]
         lib.ua_oracle_forward.argtypes = common + [ctypes.c_void_p, ctypes.c_int32]
         lib.ua_oracle_forward.restype = ctypes.c_int
         lib.ua_oracle_rows.argtypes = common + [ctypes.c_void_p, ctypes.c_int64,
@@ -54,6 +56,8 @@ def _load():
         lib.ua_oracle_row_weights.argtypes = common + [ctypes.c_int64, ctypes.c_int32,
                                                        ctypes.c_void_p, ctypes.c_void_p]
         lib.ua_oracle_row_weights.restype = ctypes.c_int
+        lib.ua_oracle_e4m3.argtypes = [ctypes.c_uint32]
+        lib.ua_oracle_e4m3.restype = ctypes.c_double
         _lib = lib
     return _lib
 
@@ -74,6 +78,26 @@ def _bf16_bits(t):
     import torch
     assert t.dtype == torch.bfloat16, t.dtype
     return np.ascontiguousarray(t.detach().cpu().contiguous().view(torch.int16).numpy()).view(np.uint16)
+
+
+def _kv_bits(t):
+    """A K/V cache -> (contiguous numpy codes, is_fp8): bf16 as uint16 bit
+    patterns, fp8 e4m3 (torch float8_e4m3fn, or a uint8 array of codes) as uint8."""
+    if isinstance(t, np.ndarray):
+        if t.dtype == np.uint8:
+            return np.ascontiguousarray(t), True
+        return _bf16_bits(t), False
+    import torch
+    if t.dtype == torch.float8_e4m3fn:
+        return np.ascontiguousarray(t.detach().cpu().contiguous().view(torch.uint8).numpy()), True
+    if t.dtype == torch.uint8:
+        return np.ascontiguousarray(t.detach().cpu().contiguous().numpy()), True
+    return _bf16_bits(t), False
+
+
+def e4m3_value(code):
+    """The oracle's value of one e4m3 code (0..255)."""
+    return float(_load().ua_oracle_e4m3(int(code)))
 
 
 def _i32(t):
@@ -99,10 +123,14 @@ class _Args:
 
     def __init__(self, q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k,
                  scale, causal=True, softcap=0.0, window=0, alibi_slopes=None,
-                 sinks=None):
+                 sinks=None, k_scale=1.0, v_scale=1.0):
         self.q = _bf16_bits(q)
-        self.k = _bf16_bits(k_cache)
-        self.v = _bf16_bits(v_cache)
+        self.k, fp8_k = _kv_bits(k_cache)
+        self.v, fp8_v = _kv_bits(v_cache)
+        assert fp8_k == fp8_v, "K and V caches must share a dtype"
+        self.kv_fp8 = 1 if fp8_k else 0
+        self.k_scale = float(k_scale)
+        self.v_scale = float(v_scale)
         self.bt = _i32(block_table)
         self.cu = _i32(cu_seqlens_q)
         self.su = _i32(seqused_k)
@@ -125,15 +153,17 @@ class _Args:
         return [self.num_seqs, self.hq, self.hk, self.d, self.b, self.num_blocks,
                 _ptr(self.q), _ptr(self.k), _ptr(self.v), _ptr(self.bt), self.bt_stride,
                 _ptr(self.cu), _ptr(self.su), self.scale, self.causal, self.softcap,
-                self.window, _ptr(self.alibi), _ptr(self.sinks)]
+                self.window, _ptr(self.alibi), _ptr(self.sinks), self.kv_fp8,
+                self.k_scale, self.v_scale]
 
 
 def forward(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, scale,
             causal=True, softcap=0.0, window=0, alibi_slopes=None, sinks=None,
-            nthreads=None):
-    """All output rows, fp64 numpy [total_q, H_q, d]."""
+            nthreads=None, k_scale=1.0, v_scale=1.0):
+    """All output rows, fp64 numpy [total_q, H_q, d].  fp8 caches are e4m3
+    codes scaled by k_scale / v_scale."""
     a = _Args(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, scale,
-              causal, softcap, window, alibi_slopes, sinks)
+              causal, softcap, window, alibi_slopes, sinks, k_scale, v_scale)
     out = np.zeros((a.total_q, a.hq, a.d), dtype=np.float64)
     rc = _load().ua_oracle_forward(*a.head(), _ptr(out),
                                    nthreads or default_threads())
@@ -144,10 +174,10 @@ def forward(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, scale,
 
 def rows(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, scale, row_ids,
          causal=True, softcap=0.0, window=0, alibi_slopes=None, sinks=None,
-         nthreads=None):
+         nthreads=None, k_scale=1.0, v_scale=1.0):
     """Selected output rows (row id = token * H_q + head), fp64 numpy [n, d]."""
     a = _Args(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, scale,
-              causal, softcap, window, alibi_slopes, sinks)
+              causal, softcap, window, alibi_slopes, sinks, k_scale, v_scale)
     ids = np.ascontiguousarray(np.asarray(row_ids, dtype=np.int64))
     out = np.zeros((ids.shape[0], a.d), dtype=np.float64)
     rc = _load().ua_oracle_rows(*a.head(), _ptr(ids), ids.shape[0], _ptr(out),
@@ -159,10 +189,10 @@ def rows(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, scale, row_i
 
 def row_weights(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, scale,
                 token, head, causal=True, softcap=0.0, window=0, alibi_slopes=None,
-                sinks=None):
+                sinks=None, k_scale=1.0, v_scale=1.0):
     """(weights [S_k + 1] with the sink's share last, O_i [d]) for one row."""
     a = _Args(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, scale,
-              causal, softcap, window, alibi_slopes, sinks)
+              causal, softcap, window, alibi_slopes, sinks, k_scale, v_scale)
     cu = a.cu
     s = int(np.searchsorted(cu, token, side="right") - 1)
     while s + 1 < len(cu) and cu[s + 1] <= token:
@@ -179,7 +209,8 @@ def row_weights(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, scale
 def forward_workload(w, nthreads=None, row_ids=None):
     """Oracle on a ``paged_varlen_flash_gb300.workloads.Workload`` (host copies)."""
     kw = dict(causal=w.causal, softcap=w.softcap, window=w.window,
-              alibi_slopes=w.alibi_slopes, sinks=w.sinks, nthreads=nthreads)
+              alibi_slopes=w.alibi_slopes, sinks=w.sinks, nthreads=nthreads,
+              k_scale=getattr(w, "k_scale", 1.0), v_scale=getattr(w, "v_scale", 1.0))
     if row_ids is None:
         return forward(w.q, w.k_cache, w.v_cache, w.block_table, w.cu_seqlens_q,
                        w.seqused_k, w.scale, **kw)

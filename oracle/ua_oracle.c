@@ -36,6 +36,12 @@
  *
  * bf16 inputs are widened exactly (a bf16 value is the upper half of an
  * IEEE-754 binary32), and every product and sum is fp64.
+ *
+ * fp8 KV cache (gfx950 page, section 7.3 "fp8 KV cache (bf16-Q + fp8-KV)"):
+ * the cache holds e4m3 codes with one scale per tensor, K_j = e4m3(k) * k_scale
+ * and V_j = e4m3(v) * v_scale, decoded exactly (OCP 8-bit float e4m3: 1 sign,
+ * 4 exponent bits with bias 7, 3 mantissa bits, subnormals at exponent 0, the
+ * all-ones code NaN, no infinities); Q stays bf16.
  */
 #include <math.h>
 #include <pthread.h>
@@ -53,7 +59,10 @@
 typedef struct {
     int32_t num_seqs, hq, hk, d, b;
     int64_t num_blocks;
-    const uint16_t *q, *k, *v;      /* bf16 bit patterns */
+    const uint16_t *q;              /* bf16 bit patterns */
+    const void *k, *v;              /* bf16 bit patterns, or e4m3 codes when kv_fp8 */
+    int32_t kv_fp8;
+    double k_scale, v_scale;        /* applied to decoded e4m3 values */
     const int32_t *block_table;     /* [num_seqs, bt_stride] */
     int32_t bt_stride;
     const int32_t *cu_seqlens_q;    /* [num_seqs + 1] */
@@ -72,6 +81,23 @@ static double widen_bf16(uint16_t h)
     float f;
     memcpy(&f, &u, sizeof f);
     return (double)f;
+}
+
+/* Value of an OCP e4m3 code: (-1)^s (1 + m/8) 2^(e-7), or m/8 2^-6 when e = 0;
+ * exponent 15 with mantissa 7 is NaN. */
+static double decode_e4m3(uint8_t x)
+{
+    const int s = x >> 7, e = (x >> 3) & 15, m = x & 7;
+    if (e == 15 && m == 7) return NAN;
+    const double v = e == 0 ? ldexp((double)m, -9) : ldexp((double)(8 + m), e - 10);
+    return s ? -v : v;
+}
+
+/* Element `idx` of a K or V cache, widened exactly (fp8: times its scale). */
+static double kv_elem(const oracle_problem *P, const void *base, int64_t idx, double scale)
+{
+    if (P->kv_fp8) return decode_e4m3(((const uint8_t *)base)[idx]) * scale;
+    return widen_bf16(((const uint16_t *)base)[idx]);
 }
 
 /* Sequence that owns packed query row `token` (cu_seqlens_q is non-decreasing). */
@@ -134,9 +160,9 @@ static void one_row(const oracle_problem *P, int64_t token, int32_t h, double *o
         vis[j] = (unsigned char)visible;
         if (!visible) { x[j] = -INFINITY; continue; }
         int64_t blk = P->block_table[(int64_t)s * P->bt_stride + j / P->b];
-        const uint16_t *krow = P->k + ((blk * P->b + j % P->b) * P->hk + hkv) * (int64_t)d;
+        const int64_t krow = ((blk * P->b + j % P->b) * P->hk + hkv) * (int64_t)d;
         double dot = 0.0;
-        for (int32_t t = 0; t < d; ++t) dot += widen_bf16(qrow[t]) * widen_bf16(krow[t]);
+        for (int32_t t = 0; t < d; ++t) dot += widen_bf16(qrow[t]) * kv_elem(P, P->k, krow + t, P->k_scale);
         double xj = P->scale * dot;
         if (P->softcap > 0.0) xj = P->softcap * tanh(xj / P->softcap);
         if (P->alibi_slopes) xj += P->alibi_slopes[h] * (double)((int64_t)j - ctx);
@@ -172,9 +198,9 @@ static void one_row(const oracle_problem *P, int64_t token, int32_t h, double *o
     for (int32_t j = 0; j < sk; ++j) {
         if (!vis[j]) continue;
         int64_t blk = P->block_table[(int64_t)s * P->bt_stride + j / P->b];
-        const uint16_t *vrow = P->v + ((blk * P->b + j % P->b) * P->hk + hkv) * (int64_t)d;
+        const int64_t vrow = ((blk * P->b + j % P->b) * P->hk + hkv) * (int64_t)d;
         double wgt = x[j];
-        for (int32_t t = 0; t < d; ++t) out[t] += wgt * widen_bf16(vrow[t]);
+        for (int32_t t = 0; t < d; ++t) out[t] += wgt * kv_elem(P, P->v, vrow + t, P->v_scale);
         if (weights) weights[j] = x[j] / den;
     }
     for (int32_t t = 0; t < d; ++t) out[t] /= den;
@@ -258,7 +284,8 @@ static int run_rows(const oracle_problem *P, const int64_t *rows, int64_t n_rows
  * q [total_q, hq, d], k_cache / v_cache [num_blocks, b, hk, d] (bf16 bits),
  * block_table [num_seqs, bt_stride], cu_seqlens_q [num_seqs + 1],
  * seqused_k [num_seqs]; softcap <= 0 and window <= 0 switch those terms off;
- * alibi_slopes / sinks may be NULL.  Output is fp64.
+ * alibi_slopes / sinks may be NULL; kv_fp8 != 0 reads the caches as e4m3
+ * codes scaled by k_scale / v_scale.  Output is fp64.
  * ------------------------------------------------------------------------- */
 
 #define FILL_PROBLEM()                                                        \
@@ -270,15 +297,17 @@ static int run_rows(const oracle_problem *P, const int64_t *rows, int64_t n_rows
     P.scale = scale; P.causal = causal;                                       \
     P.softcap = softcap > 0.0 ? softcap : 0.0;                                \
     P.window = window > 0 ? window : 0;                                       \
-    P.alibi_slopes = alibi_slopes; P.sinks = sinks;
+    P.alibi_slopes = alibi_slopes; P.sinks = sinks;                           \
+    P.kv_fp8 = kv_fp8 ? 1 : 0; P.k_scale = k_scale; P.v_scale = v_scale;
 
 #define PROBLEM_ARGS                                                          \
     int32_t num_seqs, int32_t hq, int32_t hk, int32_t d, int32_t b,          \
-    int64_t num_blocks, const uint16_t *q, const uint16_t *k_cache,          \
-    const uint16_t *v_cache, const int32_t *block_table, int32_t bt_stride,  \
+    int64_t num_blocks, const uint16_t *q, const void *k_cache,              \
+    const void *v_cache, const int32_t *block_table, int32_t bt_stride,      \
     const int32_t *cu_seqlens_q, const int32_t *seqused_k, double scale,     \
     int32_t causal, double softcap, int32_t window,                          \
-    const double *alibi_slopes, const double *sinks
+    const double *alibi_slopes, const double *sinks, int32_t kv_fp8,         \
+    double k_scale, double v_scale
 
 /* Every output row: out [total_q, hq, d]. */
 int ua_oracle_forward(PROBLEM_ARGS, double *out, int32_t nthreads)
@@ -320,4 +349,10 @@ int ua_oracle_row_weights(PROBLEM_ARGS, int64_t token, int32_t head, double *wei
     one_row(&P, token, head, out_row, weights, x, vis);
     free(x); free(vis);
     return ORACLE_OK;
+}
+
+/* The value of one e4m3 code (exposed for the tests that pin the decoder). */
+double ua_oracle_e4m3(uint32_t code)
+{
+    return decode_e4m3((uint8_t)(code & 0xffu));
 }

@@ -20,6 +20,8 @@ Named workloads (the sizes of the five benchmark configurations):
 * ``wide_mha_alibi``  8 sequences x 4096, 32/32, d = 256, b = 64, shuffled 512-block
                       pool, values 0.5 * N(0,1), causal, ALiBi slopes 2^(-8h/32),
                       h = 1..32.
+* ``decode_fp8``      the ``decode`` lengths and tables with an fp8 e4m3 K/V cache
+                      (one scale per tensor, 1/32; codes of N(0,1) / scale).
 
 Lengths and block tables come from a CPU ``torch.Generator`` seeded with
 ``1000 + config index`` and are therefore identical on every device; the bf16
@@ -28,6 +30,10 @@ rounded to bf16).  Key slots that no sequence uses -- blocks outside every
 table and the tail of each sequence's last block -- are filled with NaN when
 ``poison=True`` so that a kernel reading them shows up as NaN in its output;
 block-table padding past a sequence's last block holds -1.
+
+fp8 caches (``kv_fp8=True``) hold e4m3 codes as uint8: the N(0,1) values are
+divided by the tensor's scale and rounded to e4m3 by PyTorch's
+``float8_e4m3fn`` conversion; their poison is the NaN code 0x7f.
 """
 from __future__ import annotations
 
@@ -40,7 +46,7 @@ import torch
 CONFIG_NAMES = ["tiny", "decode", "chunked", "long_prefill", "wide_mha_alibi"]
 _CONFIG_INDEX = {
     "tiny": 0, "decode": 1, "chunked": 2, "long_prefill": 3,
-    "long_prefill_shuffled": 3, "wide_mha_alibi": 4,
+    "long_prefill_shuffled": 3, "wide_mha_alibi": 4, "decode_fp8": 1,
 }
 
 
@@ -67,6 +73,9 @@ class Workload:
     sinks: Optional[torch.Tensor] = None         # fp32 [hq]
     alibi_slopes: Optional[torch.Tensor] = None  # fp32 [hq]
     meta: dict = field(default_factory=dict)
+    kv_fp8: bool = False              # caches hold e4m3 codes (uint8)
+    k_scale: float = 1.0              # K = e4m3(k) * k_scale when kv_fp8
+    v_scale: float = 1.0
 
     @property
     def num_seqs(self) -> int:
@@ -100,7 +109,8 @@ class Workload:
             list(self.seqlens_q), list(self.seqlens_k), mv(self.q), mv(self.k_cache),
             mv(self.v_cache), mv(self.block_table), mv(self.cu_seqlens_q),
             mv(self.seqused_k), self.scale, self.causal, self.softcap, self.window,
-            mv(self.sinks), mv(self.alibi_slopes), dict(self.meta))
+            mv(self.sinks), mv(self.alibi_slopes), dict(self.meta), self.kv_fp8,
+            self.k_scale, self.v_scale)
 
     # -- counts used for reporting (no attention arithmetic) ------------------
     def visible_pairs(self) -> int:
@@ -117,7 +127,7 @@ class Workload:
 
     def kv_bytes_read(self) -> int:
         """K and V bytes of the used keys, counted once per (sequence, kv head)."""
-        return int(sum(self.seqlens_k)) * self.hk * self.d * 2 * 2
+        return int(sum(self.seqlens_k)) * self.hk * self.d * (1 if self.kv_fp8 else 2) * 2
 
 
 def _gen(seed: int) -> torch.Generator:
@@ -136,7 +146,7 @@ def build(name: str, hq: int, hk: int, d: int, b: int, seqlens_q, seqlens_k,
           seed: int = 0, device="cpu", std: float = 1.0, causal: bool = True,
           softcap: float = 0.0, window: int = 0, sinks: bool = False,
           alibi: bool = False, poison: bool = True, bt_pad: int = 0,
-          values: bool = True) -> Workload:
+          values: bool = True, kv_fp8: bool = False, kv_scale: float = 1.0 / 32) -> Workload:
     """Assemble a workload from explicit lengths.
 
     ``block_ids`` (int, len >= sum of blocks needed) fixes the physical blocks
@@ -176,20 +186,35 @@ def build(name: str, hq: int, hk: int, d: int, b: int, seqlens_q, seqlens_k,
         return x.to(torch.bfloat16)
 
     q = randn(total_q, hq, d) if values else torch.zeros(total_q, hq, d, dtype=torch.bfloat16, device=dev)
-    fill = float("nan") if poison else 0.0
-    k_cache = torch.full((num_blocks, b, hk, d), fill, dtype=torch.bfloat16, device=dev)
-    v_cache = torch.full((num_blocks, b, hk, d), fill, dtype=torch.bfloat16, device=dev)
+
+    def kv_values(*shape):
+        if not kv_fp8:
+            return randn(*shape)
+        x = torch.randn(*shape, generator=vg, device=dev, dtype=torch.float32)
+        x.mul_(std / kv_scale).clamp_(-448.0, 448.0)
+        return x.to(torch.float8_e4m3fn).view(torch.uint8)
+
+    if kv_fp8:
+        nan = 0x7f
+        fill = nan if poison else 0
+        k_cache = torch.full((num_blocks, b, hk, d), fill, dtype=torch.uint8, device=dev)
+        v_cache = torch.full((num_blocks, b, hk, d), fill, dtype=torch.uint8, device=dev)
+    else:
+        nan = float("nan")
+        fill = nan if poison else 0.0
+        k_cache = torch.full((num_blocks, b, hk, d), fill, dtype=torch.bfloat16, device=dev)
+        v_cache = torch.full((num_blocks, b, hk, d), fill, dtype=torch.bfloat16, device=dev)
     if values and need:
         ids = block_ids.to(dev)
-        k_cache.index_copy_(0, ids, randn(need, b, hk, d))
-        v_cache.index_copy_(0, ids, randn(need, b, hk, d))
+        k_cache.index_copy_(0, ids, kv_values(need, b, hk, d))
+        v_cache.index_copy_(0, ids, kv_values(need, b, hk, d))
     if poison:
         for s in range(n):
             tail = seqlens_k[s] % b
             if nblk[s] and tail:
                 last = int(table[s, nblk[s] - 1])
-                k_cache[last, tail:] = float("nan")
-                v_cache[last, tail:] = float("nan")
+                k_cache[last, tail:] = nan
+                v_cache[last, tail:] = nan
 
     sink_t = torch.randn(hq, generator=g, dtype=torch.float32) if sinks else None
     alibi_t = None
@@ -198,7 +223,8 @@ def build(name: str, hq: int, hk: int, d: int, b: int, seqlens_q, seqlens_k,
                                dtype=torch.float32)
     w = Workload(name, hq, hk, d, b, num_blocks, seqlens_q, seqlens_k, q, k_cache,
                  v_cache, table, cu, seqused, float(scale), causal, float(softcap),
-                 int(window), sink_t, alibi_t, {"seed": seed})
+                 int(window), sink_t, alibi_t, {"seed": seed}, bool(kv_fp8),
+                 float(kv_scale) if kv_fp8 else 1.0, float(kv_scale) if kv_fp8 else 1.0)
     if dev.type != "cpu":
         w.block_table = w.block_table.to(dev)
         w.cu_seqlens_q = w.cu_seqlens_q.to(dev)
@@ -218,10 +244,10 @@ def make(name: str, device="cpu", poison: bool = False, values: bool = True) -> 
     common = dict(seed=seed, device=device, poison=poison, values=values)
     if name == "tiny":
         return build(name, 4, 1, 64, 16, [128], [128], 32, 1.0 / 8.0, **common)
-    if name == "decode":
+    if name in ("decode", "decode_fp8"):
         sk = _randint(g, 512, 8192, 64)
         return build(name, 32, 8, 128, 16, [1] * 64, sk, 40000, 1.0 / math.sqrt(128),
-                     **common)
+                     kv_fp8=name == "decode_fp8", **common)
     if name == "chunked":
         ctx = _randint(g, 0, 4096, 16)
         sq = _randint(g, 1, 512, 16)
@@ -241,7 +267,7 @@ def make(name: str, device="cpu", poison: bool = False, values: bool = True) -> 
 def random_small(seed: int, *, num_seqs=3, hq=8, hk=2, d=64, b=16, sq=(1, 40),
                  ctx=(0, 70), causal=True, softcap=0.0, window=0, sinks=False,
                  alibi=False, device="cpu", poison=True, spare_blocks=5,
-                 std=1.0) -> Workload:
+                 std=1.0, kv_fp8=False, kv_scale=1.0 / 32) -> Workload:
     """A small seeded ragged batch for parity sweeps (lengths drawn per seq)."""
     g = _gen(seed)
     seqlens_q = _randint(g, sq[0], sq[1], num_seqs)
@@ -251,7 +277,7 @@ def random_small(seed: int, *, num_seqs=3, hq=8, hk=2, d=64, b=16, sq=(1, 40),
     return build("random_small", hq, hk, d, b, seqlens_q, seqlens_k,
                  need + spare_blocks, 1.0 / math.sqrt(d), seed=seed, device=device,
                  std=std, causal=causal, softcap=softcap, window=window, sinks=sinks,
-                 alibi=alibi, poison=poison, bt_pad=1)
+                 alibi=alibi, poison=poison, bt_pad=1, kv_fp8=kv_fp8, kv_scale=kv_scale)
 
 
 def sample_rows(w: Workload, n: int, seed: int = 0) -> torch.Tensor:

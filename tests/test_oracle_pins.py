@@ -418,3 +418,60 @@ def test_sampled_rows_match_full_forward():
     part = oracle.forward_workload(w, row_ids=ids)
     flat = full.reshape(-1, w.d)
     assert np.array_equal(part, flat[ids.numpy()])
+
+
+# ---------------------------------------------------------------------------
+# fp8 e4m3 KV cache (gfx950 page, section 7.3): decoder, scales.
+# ---------------------------------------------------------------------------
+
+def test_e4m3_decoder_matches_torch_for_every_code():
+    """The oracle's e4m3 decoder equals PyTorch's float8_e4m3fn -> fp32
+    conversion (an independent implementation of the OCP format) on all 256
+    codes, NaN codes included."""
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = np.array([oracle.e4m3_value(c) for c in range(256)])
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(got[ok], ref[ok])
+    assert np.array_equal(np.signbit(got[ok]), np.signbit(ref[ok]))
+    # A few values the format fixes by hand: 1, the largest finite, the
+    # smallest subnormal and the smallest normal.
+    assert oracle.e4m3_value(0x38) == 1.0 and oracle.e4m3_value(0x7E) == 448.0
+    assert oracle.e4m3_value(0x01) == 2.0 ** -9 and oracle.e4m3_value(0x08) == 2.0 ** -6
+
+
+def _decoded_bf16(codes, scale):
+    """e4m3 codes (uint8) -> bf16 tensor of code * scale (exact for these scales)."""
+    return (codes.view(torch.float8_e4m3fn).to(torch.float32) * scale).to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("flags", [dict(), dict(softcap=20.0, sinks=True), dict(alibi=True, window=9)])
+def test_fp8_cache_equals_attention_on_decoded_values(flags):
+    """fp8 K/V with power-of-two scales: every decoded value times its scale is
+    exact in bf16, so the fp8 oracle must equal the bf16 oracle on the decoded
+    caches (pins the decode, the scale on each tensor and the paging)."""
+    w = W.random_small(11, hq=8, hk=2, d=64, kv_fp8=True, kv_scale=0.125, **flags)
+    kw = dict(causal=w.causal, softcap=w.softcap, window=w.window,
+              alibi_slopes=w.alibi_slopes, sinks=w.sinks)
+    got = oracle.forward(w.q, w.k_cache, w.v_cache, w.block_table, w.cu_seqlens_q,
+                         w.seqused_k, w.scale, k_scale=0.125, v_scale=0.25, **kw)
+    kb = _decoded_bf16(w.k_cache, 0.125)
+    vb = _decoded_bf16(w.v_cache, 0.25)
+    want = oracle.forward(w.q, kb, vb, w.block_table, w.cu_seqlens_q, w.seqused_k,
+                          w.scale, **kw)
+    assert not np.isnan(got).any()
+    np.testing.assert_allclose(got, want, rtol=0, atol=1e-12)
+
+
+def test_fp8_scales_fold_into_tau_and_the_output():
+    """k_scale multiplies every logit before the score chain, so it can move into
+    tau; v_scale multiplies every value row, so it scales O."""
+    w = W.random_small(12, hq=4, hk=1, d=64, kv_fp8=True, kv_scale=1.0, softcap=15.0)
+    args = (w.q, w.k_cache, w.v_cache, w.block_table, w.cu_seqlens_q, w.seqused_k)
+    kw = dict(causal=True, softcap=w.softcap)
+    a = oracle.forward(*args, w.scale, k_scale=0.3, v_scale=1.0, **kw)
+    b = oracle.forward(*args, w.scale * 0.3, k_scale=1.0, v_scale=1.0, **kw)
+    np.testing.assert_allclose(a, b, rtol=1e-12, atol=1e-12)
+    c = oracle.forward(*args, w.scale, k_scale=0.3, v_scale=3.0, **kw)
+    np.testing.assert_allclose(c, 3.0 * a, rtol=1e-12, atol=1e-12)
