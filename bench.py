@@ -36,6 +36,8 @@ if ROOT not in sys.path:
 METRIC = "prefill TFLOPS and decode KV-read GB/s on 1×GB300, as % of roofline"
 HEADLINE = "decode"
 SECONDARY = ["chunked", "long_prefill", "wide_mha_alibi"]
+# HBM-bound secondary workloads, reported in GB/s of algorithmic bytes.
+SECONDARY_HBM = ["decode_fp8"]
 L2_FLUSH_BYTES = 256 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
@@ -357,6 +359,22 @@ def run_ours(args):
                 "flops": f_s, "bytes": b_s, "device_error": r["device_error"]}
             del ws
             torch.cuda.empty_cache()
+        for name in SECONDARY_HBM:
+            ws = W.make(name, device=dev)
+            b_s, f_s = workload_units(ws)
+            r = time_ours(ws, max(3, min(args.steps, 20)), max(3, args.warmup), flush=False,
+                          torch=torch, ua=ua)
+            ms = statistics.mean(r["step_ms"])
+            km = statistics.mean(r["kernel_ms"])
+            per_config[name] = {
+                "ms_per_step": round(ms, 4), "gbs": round(b_s / (ms * 1e-3) / 1e9, 1),
+                "kernel_gbs": round(b_s / (km * 1e-3) / 1e9, 1),
+                "frac_of_hbm_peak": round(b_s / (km * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                "kv_tokens_per_s": round(sum(ws.seqlens_k) / (ms * 1e-3), 1),
+                "path": r["path"], "launches_per_step": r["launches"] // max(1, len(r["step_ms"])),
+                "bytes": b_s, "device_error": r["device_error"]}
+            del ws
+            torch.cuda.empty_cache()
     sampler.stop()
 
     cpu = None
@@ -483,7 +501,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default=None,
                     choices=["tiny", "decode", "chunked", "long_prefill", "long_prefill_shuffled",
-                             "wide_mha_alibi"],
+                             "wide_mha_alibi", "decode_fp8"],
                     help="time only this workload and print its own short JSON line "
                          "(for profiling); the default is the full headline run")
     ap.add_argument("--path", default="auto", choices=["auto", "split", "tensor", "decode"],

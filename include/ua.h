@@ -83,7 +83,12 @@ enum {
     UA_DEVERR_TIMEOUT = 1u << 4   /* a bounded on-chip wait gave up; results unspecified */
 };
 
-enum { UA_DTYPE_BF16 = 0 };
+/* Element types.  Q, O: bf16.  K/V caches: bf16, or fp8 e4m3 codes (one byte
+ * each; OCP e4m3: bias 7, subnormals, no infinities, 0x7f / 0xff NaN) with one
+ * scale per tensor, K = code * k_scale, V = code * v_scale (gfx950 page,
+ * section 7.3 "fp8 KV cache (bf16-Q + fp8-KV)").  The fp8 cache is read by
+ * the DECODE_TC path only. */
+enum { UA_DTYPE_BF16 = 0, UA_DTYPE_FP8_E4M3 = 1 };
 
 /* Execution path (gfx950 spec section 6: a path whose query-tile grid fills
  * the device versus split-KV segments plus a reduction).
@@ -119,6 +124,12 @@ typedef struct ua_problem_desc {
     float softcap;              /* c > 0 when UA_FLAG_SOFTCAP, else ignored */
     int32_t window;             /* W >= 1 when UA_FLAG_WINDOW, else ignored */
     uint32_t path;              /* UA_PATH_*: which kernel family serves the calls */
+    int32_t kv_dtype;           /* UA_DTYPE_BF16, or UA_DTYPE_FP8_E4M3 (needs d = 128 and
+                                   path AUTO or DECODE_TC; a call whose shape the
+                                   decode kernel does not take returns
+                                   UA_ERR_UNSUPPORTED) */
+    float k_scale;              /* fp8 caches: K = code * k_scale, > 0; else ignored */
+    float v_scale;              /* fp8 caches: V = code * v_scale, > 0; else ignored */
 } ua_problem_desc;
 
 typedef struct ua_problem ua_problem;
@@ -214,7 +225,8 @@ ua_status ua_set_profile_events(ua_problem *p, void *ev_begin, void *ev_end);
  * library declares statically in device memory: every GPU that loads
  * libua.so holds those 16 MiB until the process exits.  Calls whose partials
  * (total_q * H_q * (d + 2) * 4 bytes per segment) do not fit twice in that
- * array return UA_ERR_UNSUPPORTED and launch nothing.
+ * array return UA_ERR_UNSUPPORTED and launch nothing, as do descriptions
+ * with an fp8 cache (kv_dtype != UA_DTYPE_BF16).
  *
  * device_error: optional caller-owned device int32 that receives the
  * UA_DEVERR_* bits (OR-ed in; the caller clears it).  When NULL the bits go to

@@ -25,6 +25,7 @@ UA_DEVERR_BOUNDS = 1 << 3
 UA_DEVERR_TIMEOUT = 1 << 4
 
 UA_DTYPE_BF16 = 0
+UA_DTYPE_FP8_E4M3 = 1
 
 UA_PATH_AUTO = 0
 UA_PATH_SPLIT_KV = 1
@@ -59,6 +60,9 @@ class ProblemDesc(ctypes.Structure):
         ("softcap", ctypes.c_float),
         ("window", ctypes.c_int32),
         ("path", ctypes.c_uint32),
+        ("kv_dtype", ctypes.c_int32),
+        ("k_scale", ctypes.c_float),
+        ("v_scale", ctypes.c_float),
     ]
 
 
@@ -140,12 +144,13 @@ def flags_of(causal=True, softcap=0.0, alibi=False, window=0, sinks=False):
 
 def ua_problem_create(num_q_heads, num_kv_heads, head_size, block_size, num_blocks,
                       max_num_seqs, max_blocks_per_seq, max_total_q, flags, scale,
-                      softcap=0.0, window=0, path=UA_PATH_AUTO):
+                      softcap=0.0, window=0, path=UA_PATH_AUTO, kv_dtype=UA_DTYPE_BF16,
+                      k_scale=1.0, v_scale=1.0):
     """Returns an opaque problem handle (int); raises UAError on failure."""
     lib = load_library()
     d = ProblemDesc(num_q_heads, num_kv_heads, head_size, block_size, num_blocks,
                     max_num_seqs, max_blocks_per_seq, max_total_q, UA_DTYPE_BF16, flags,
-                    scale, softcap, window, path)
+                    scale, softcap, window, path, kv_dtype, k_scale, v_scale)
     h = ctypes.c_void_p()
     st = lib.ua_problem_create(ctypes.byref(d), ctypes.byref(h))
     if st != UA_OK:
@@ -213,10 +218,11 @@ class Problem:
 
     def __init__(self, num_q_heads, num_kv_heads, head_size, block_size, num_blocks,
                  max_num_seqs, max_blocks_per_seq, max_total_q, flags, scale, softcap=0.0,
-                 window=0, path=UA_PATH_AUTO):
+                 window=0, path=UA_PATH_AUTO, kv_dtype=UA_DTYPE_BF16, k_scale=1.0, v_scale=1.0):
         self.handle = ua_problem_create(num_q_heads, num_kv_heads, head_size, block_size,
                                         num_blocks, max_num_seqs, max_blocks_per_seq,
-                                        max_total_q, flags, scale, softcap, window, path)
+                                        max_total_q, flags, scale, softcap, window, path,
+                                        kv_dtype, k_scale, v_scale)
         self.flags = flags
         self.head_size = head_size
         self.num_q_heads = num_q_heads
@@ -226,9 +232,11 @@ class Problem:
                      path=UA_PATH_AUTO):
         flags = flags_of(w.causal, w.softcap, w.alibi_slopes is not None, w.window,
                          w.sinks is not None) | extra_flags
+        fp8 = getattr(w, "kv_fp8", False)
         return cls(w.hq, w.hk, w.d, w.b, w.num_blocks, max_num_seqs or max(1, w.num_seqs),
                    w.max_blocks_per_seq, max_total_q or max(1, w.total_q), flags, w.scale,
-                   w.softcap, w.window, path)
+                   w.softcap, w.window, path, UA_DTYPE_FP8_E4M3 if fp8 else UA_DTYPE_BF16,
+                   getattr(w, "k_scale", 1.0), getattr(w, "v_scale", 1.0))
 
     def forward(self, q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, num_seqs,
                 total_q, max_seqlen_q, max_seqlen_k, flags, sinks=None, alibi_slopes=None,

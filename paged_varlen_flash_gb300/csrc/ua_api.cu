@@ -47,19 +47,24 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 // swizzle panel), one KV head and `box_rows` consecutive slots of one block.
 // Addresses are formed by the TMA unit in 64 bits, so caches beyond 2 GiB need
 // no special path (the overflow hazard described in gfx950 section 7.2).
+// Tensor map of a paged cache [num_blocks, b, H_k, d]; a box is one
+// 128-byte swizzle panel (64 bf16 or 128 fp8 elements) x 1 head x box_rows
+// slots x 1 block.
 bool encode_cache_map(CUtensorMap* m, const void* base, const ua_problem_desc& d, int box_rows) {
     auto enc = tensor_map_encoder();
     if (!enc) return false;
-    const cuuint64_t es = 2;
+    const bool fp8 = d.kv_dtype == UA_DTYPE_FP8_E4M3;
+    const cuuint64_t es = fp8 ? 1 : 2;
     cuuint64_t dims[4] = {(cuuint64_t)d.head_size, (cuuint64_t)d.num_kv_heads,
                           (cuuint64_t)d.block_size, (cuuint64_t)d.num_blocks};
     cuuint64_t strides[3] = {es * d.head_size, es * d.head_size * d.num_kv_heads,
                              es * d.head_size * d.num_kv_heads * d.block_size};
-    cuuint32_t box[4] = {64, 1, (cuuint32_t)box_rows, 1};
+    cuuint32_t box[4] = {(cuuint32_t)(128 / es), 1, (cuuint32_t)box_rows, 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
-    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides,
-                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = enc(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+                     const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
@@ -133,6 +138,15 @@ ua_status ua_problem_create(const ua_problem_desc* d, ua_problem** out) {
     if ((d->flags & UA_FLAG_WINDOW) && (d->window < 1 || !(d->flags & UA_FLAG_CAUSAL)))
         return UA_ERR_INVALID_ARG;
     if (d->dtype != UA_DTYPE_BF16) return UA_ERR_UNSUPPORTED;
+    if (d->kv_dtype != UA_DTYPE_BF16 && d->kv_dtype != UA_DTYPE_FP8_E4M3) return UA_ERR_INVALID_ARG;
+    if (d->kv_dtype == UA_DTYPE_FP8_E4M3) {
+        if (!(d->k_scale > 0.f) || !std::isfinite(d->k_scale) || !(d->v_scale > 0.f) ||
+            !std::isfinite(d->v_scale))
+            return UA_ERR_INVALID_ARG;
+        // Only the decode tensor-core kernel reads an fp8 cache.
+        if (d->head_size != 128) return UA_ERR_UNSUPPORTED;
+        if (d->path != UA_PATH_AUTO && d->path != UA_PATH_DECODE_TC) return UA_ERR_UNSUPPORTED;
+    }
     if (d->head_size != 64 && d->head_size != 128 && d->head_size != 256) return UA_ERR_UNSUPPORTED;
     if (d->block_size != 16 && d->block_size != 32 && d->block_size != 64) return UA_ERR_UNSUPPORTED;
     if (d->num_blocks > (int64_t(1) << 31) - 1) return UA_ERR_UNSUPPORTED;
@@ -254,6 +268,9 @@ ua_status ua_forward(ua_problem* p, const void* q, const void* k_cache, const vo
     fp.scale = d.scale;
     fp.softcap = d.softcap;
     fp.window = d.window;
+    fp.kv_fp8 = d.kv_dtype == UA_DTYPE_FP8_E4M3 ? 1 : 0;
+    fp.k_scale = fp.kv_fp8 ? d.k_scale : 1.f;
+    fp.v_scale = fp.kv_fp8 ? d.v_scale : 1.f;
 
     if (k_cache != p->map_k_ptr || v_cache != p->map_v_ptr) {
         if (!encode_cache_map(&p->map_k16, k_cache, d, 16) ||
@@ -279,8 +296,8 @@ ua_status ua_forward(ua_problem* p, const void* q, const void* k_cache, const vo
         use_dec = false;
         use_tc = true;
     }
-    if (d.path == UA_PATH_DECODE_TC) {
-        if (!dec_ok) return UA_ERR_UNSUPPORTED;
+    if (d.path == UA_PATH_DECODE_TC || fp.kv_fp8) {
+        if (!dec_ok) return UA_ERR_UNSUPPORTED;   // an fp8 cache is read by this kernel only
         use_dec = true;
         use_tc = false;
     }

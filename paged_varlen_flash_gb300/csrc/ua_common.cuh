@@ -36,6 +36,8 @@ struct FwdParams {
     int32_t splits;                // split-KV segments per row (1 = direct)
     int32_t chunk;                 // keys per segment (multiple of 64)
     int32_t row_tiles;             // row tiles per (sequence, kv head)
+    int32_t kv_fp8;                // caches hold e4m3 codes
+    float k_scale, v_scale;        // fp8 caches: K = code * k_scale, V = code * v_scale
 };
 
 // Per-sequence metadata check.  Returns UA_DEVERR_* bits (0 = well formed) and

@@ -46,37 +46,43 @@ constexpr int kN = 16;          // packed rows per tile (MMA N)
 constexpr int kBN = 128;        // keys per KV tile (MMA M of S^T)
 constexpr int kD = 128;         // head size served by this kernel (MMA M of O^T)
 constexpr int kThreadsD = 224;  // 4 softmax warps, TMA warp, QK^T issuer, P.V issuer
+constexpr int kThreadsF8 = 352; // fp8 caches: + 4 warps turning e4m3 tiles into f16
 constexpr int kWarpTmaD = 4;
 constexpr int kWarpMmaD = 5;    // QK^T issuer (also allocates tensor memory)
 constexpr int kWarpPvD = 6;     // P.V issuer
-constexpr uint32_t kTmemColsD = 64;
 constexpr float kLazyD = 8.0f;
 
 // NSK / NSV: K and V ring depths (a K stage is free once its QK^T ran, a V
-// stage only once its P.V ran, so they may differ).
-template <int NSK, int NSV>
+// stage only once its P.V ran, so they may differ).  F8: the rings hold e4m3
+// tiles (128 keys x 128 one-byte dims); K is turned into f16 in tensor memory
+// (the QK^T A operand), V into an f16 tile in shared memory.
+template <int NSK, int NSV, bool F8>
 struct DCfg {
     static constexpr int kPanels = kD / 64;
     static constexpr int kQPanel = kN * 128;              // 16 rows x 64 dims
     static constexpr int kQBytes = kPanels * kQPanel;
-    static constexpr int kKvPanel = kBN * 128;            // 128 keys x 64 dims
+    static constexpr int kKvPanel = kBN * 128;            // 128 keys x 64 dims (16-bit)
     static constexpr int kKvBytes = kPanels * kKvPanel;
+    static constexpr int kStage = F8 ? kBN * 128 : kKvBytes;   // one TMA ring stage
     static constexpr int kPPanel = kN * 128;              // 16 rows x 64 keys
     static constexpr int kPBuf = (kBN / 64) * kPPanel;    // one P^T tile
     static constexpr int kOffQ = 0;
-    static constexpr int kOffK = 8192;
-    static constexpr int kOffV = kOffK + NSK * kKvBytes;
-    static constexpr int kOffP = kOffV + NSV * kKvBytes;  // two P^T buffers
+    static constexpr int kOffK = F8 ? 4096 : 8192;
+    static constexpr int kOffV = kOffK + NSK * kStage;
+    static constexpr int kOffV16 = kOffV + NSV * kStage;  // F8: the f16 V tile
+    static constexpr int kOffP = kOffV16 + (F8 ? kKvBytes : 0);  // two P^T buffers
     static constexpr int kOffBar = kOffP + 2 * kPBuf;
     // q_full, k_full[NSK], v_full[NSV], k_empty[NSK], v_empty[NSV], s_full[2],
-    // p_full[2], o_done[2], drain[2]
-    static constexpr int kNumBars = 1 + 2 * NSK + 2 * NSV + 8;
+    // p_full[2], o_done[2], drain[2]; F8: kc_full, kc_empty, vc_full, vc_empty
+    static constexpr int kNumBars = 1 + 2 * NSK + 2 * NSV + 8 + (F8 ? 4 : 0);
     static constexpr int kOffRed = kOffBar + kNumBars * 8;    // maxima [2][4][16] fp32
     static constexpr int kOffSum = kOffRed + 2 * 4 * kN * 4;  // row sums [4][16] fp32
     static constexpr int kOffMisc = kOffSum + 4 * kN * 4;
     static constexpr int kSmem = kOffMisc + 16 + 1024;
     static constexpr int kTmemS = 0;    // S^T buffers: columns [0, 16) and [16, 32)
     static constexpr int kTmemO = 32;   // O^T: columns [32, 48)
+    static constexpr int kTmemK = 64;   // F8: f16 K (lane = key, two dims per column)
+    static constexpr uint32_t kTmemCols = F8 ? 128 : 64;
     static_assert(kQBytes <= kOffK, "Q tile");
     static_assert(kSmem <= 232448, "shared memory budget");
 };
@@ -151,11 +157,24 @@ __device__ __forceinline__ float tanh_e2(float x) {
 
 // NR: packed rows the softmax threads track (4, 8 or 16 >= g * S_q); the MMAs
 // always run N = 16 and ignore the padding columns.
-template <int NSK, int NSV, int NR, bool PLAIN>
-__global__ void __launch_bounds__(kThreadsD, 1)
+// e4m3 codes -> f16 (exact): the four bytes of `w` become two f16x2 words
+// (lower byte in the lower half).
+__device__ __forceinline__ void e4m3x4_to_f16x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w));
+}
+
+// F8: K and V caches hold e4m3 codes (gfx950 page, section 7.3): the MMAs run
+// in f16 (every e4m3 value is exact in f16, and so is a bf16 Q of moderate
+// magnitude), k_scale is folded into tau and v_scale into the output scale.
+template <int NSK, int NSV, int NR, bool PLAIN, bool F8>
+__global__ void __launch_bounds__(F8 ? kThreadsF8 : kThreadsD, F8 ? 2 : 1)   // two CTAs per SM
 decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
-    using C = DCfg<NSK, NSV>;
+    using C = DCfg<NSK, NSV, F8>;
+    constexpr int kThreads = F8 ? kThreadsF8 : kThreadsD;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -187,7 +206,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     if (st || k_beg >= k_end) {
         // Malformed lengths (rows written as zeros) or a segment no row sees
         // (an empty partial, m = -inf).
-        for (int e = threadIdx.x; e < nrows * kD; e += kThreadsD) {
+        for (int e = threadIdx.x; e < nrows * kD; e += kThreads) {
             const int r = e / kD, c = e % kD;
             const int64_t row = (q0 + r / g) * p.hq + hkv * g + r % g;
             if (split) {
@@ -214,6 +233,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     const uint32_t p_full0 = s_full0 + 16;
     const uint32_t o_done0 = s_full0 + 32;
     const uint32_t drain = s_full0 + 48;
+    // F8: the f16 K in tensor memory / the f16 V tile written (kc_full, vc_full)
+    // and read by their MMA (kc_empty, vc_empty); single-buffered.
+    const uint32_t kc_full = s_full0 + 64, kc_empty = s_full0 + 72;
+    const uint32_t vc_full = s_full0 + 80, vc_empty = s_full0 + 88;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
     float* red = reinterpret_cast<float*>(smem + C::kOffRed);
@@ -221,13 +244,21 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
+        // A ring stage is released by its MMA (bf16) or by the 128 converting
+        // threads (F8).
         for (int i = 0; i < NSK; ++i) {
             mbar_init(k_full0 + 8 * i, 1);
-            mbar_init(k_empty0 + 8 * i, 1);
+            mbar_init(k_empty0 + 8 * i, F8 ? 128 : 1);
         }
         for (int i = 0; i < NSV; ++i) {
             mbar_init(v_full0 + 8 * i, 1);
-            mbar_init(v_empty0 + 8 * i, 1);
+            mbar_init(v_empty0 + 8 * i, F8 ? 128 : 1);
+        }
+        if (F8) {
+            mbar_init(kc_full, 128);
+            mbar_init(kc_empty, 1);
+            mbar_init(vc_full, 128);
+            mbar_init(vc_empty, 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(s_full0 + 8 * i, 1);
@@ -240,7 +271,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         fence_mbar_init();
     }
     if (warp == kWarpMmaD) {
-        tc::tmem_alloc(smem_u32(tmem_slot), kTmemColsD);
+        tc::tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
         tc::tmem_relinquish();
     }
     tc::fence_before_sync();
@@ -282,7 +313,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             const int key0 = (t_begin + j) * kBN;
             const int blk0 = key0 / b;
             const int nb = min(kBN / b, nblk_seq - blk0);
-            const uint32_t bytes = (uint32_t)nb * b * 128 * C::kPanels;
+            constexpr int kBoxes = F8 ? 1 : C::kPanels;   // 128-byte panels per key row
+            const uint32_t bytes = (uint32_t)nb * b * 128 * kBoxes;
             const int32_t id = id_next;
             if (j + 1 < n_tiles) id_next = tile_id(j + 1);
             if (lane < nb && (id < 0 || (int64_t)id >= p.num_blocks))
@@ -294,8 +326,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             __syncwarp();
             if (lane < nb) {
 #pragma unroll
-                for (int pn = 0; pn < C::kPanels; ++pn)
-                    tma_load_4d(sK + sk_ * C::kKvBytes + pn * C::kKvPanel + lane * b * 128, &tm_k,
+                for (int pn = 0; pn < kBoxes; ++pn)
+                    tma_load_4d(sK + sk_ * C::kStage + pn * C::kKvPanel + lane * b * 128, &tm_k,
                                 pn * 64, hkv, 0, id, k_full0 + 8 * sk_);
             }
             if (j >= NSV && !__all_sync(0xffffffffu, dwait(v_empty0 + 8 * sv_, ((j / NSV) + 1) & 1,
@@ -305,8 +337,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             __syncwarp();
             if (lane < nb) {
 #pragma unroll
-                for (int pn = 0; pn < C::kPanels; ++pn)
-                    tma_load_4d(sV + sv_ * C::kKvBytes + pn * C::kKvPanel + lane * b * 128, &tm_v,
+                for (int pn = 0; pn < kBoxes; ++pn)
+                    tma_load_4d(sV + sv_ * C::kStage + pn * C::kKvPanel + lane * b * 128, &tm_v,
                                 pn * 64, hkv, 0, id, v_full0 + 8 * sv_);
             }
             issued = j + 1;
@@ -326,30 +358,54 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         // S^T(j) = K(j) Q^T once K(j) has landed and the softmax has released
         // S^T buffer (j & 1) (P of tile j - 2 published); warp 6 issues
         // O^T += V(j)^T P^T(j) once P(j) and V(j) are ready.
-        constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(kBN, kN, false, false);
-        constexpr uint32_t idesc_pv = tc::idesc_bf16_f32(kD, kN, true, false);
+        constexpr uint32_t idesc_qk = F8 ? tc::idesc_f16_f32(kBN, kN, false, false)
+                                         : tc::idesc_bf16_f32(kBN, kN, false, false);
+        constexpr uint32_t idesc_pv = F8 ? tc::idesc_f16_f32(kD, kN, true, false)
+                                         : tc::idesc_bf16_f32(kD, kN, true, false);
         auto wwait = [&](uint32_t bar, uint32_t par) {
             return __all_sync(0xffffffffu, dwait(bar, par, abort_flag, p.err));
         };
         if (warp == kWarpMmaD) {
             bool ok = wwait(q_full, 0);
+            if (F8 && ok) {
+                // The MMAs run in f16: convert the bf16 Q tile in place (the
+                // same swizzled positions; every word is two elements).
+                uint32_t* qw = reinterpret_cast<uint32_t*>(smem + C::kOffQ);
+                for (int e = lane; e < C::kQBytes / 4; e += 32) {
+                    const uint32_t w = qw[e];
+                    uint32_t h;
+                    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(bf16_hi(w)), "f"(bf16_lo(w)));
+                    qw[e] = h;
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+            }
             for (int j = 0; ok && j < n_tiles; ++j) {
                 if (j >= 2 && !wwait(p_full0 + 8 * (j & 1), ((j - 2) >> 1) & 1)) break;
                 const int stg = j % NSK;
-                if (!wwait(k_full0 + 8 * stg, (j / NSK) & 1)) break;
+                if constexpr (F8) {
+                    if (!wwait(kc_full, j & 1)) break;
+                } else {
+                    if (!wwait(k_full0 + 8 * stg, (j / NSK) & 1)) break;
+                }
                 tc::fence_after_sync();
                 if (lane == 0) {
-                    const uint32_t kst = sK + stg * C::kKvBytes;
+                    const uint32_t kst = sK + stg * C::kStage;
                     const uint32_t dS = tmem + C::kTmemS + (j & 1) * kN;
 #pragma unroll
                     for (int k = 0; k < kD / 16; ++k) {
                         const int pn = k >> 2, off = (k & 3) * 32;
-                        const uint64_t a = tc::smem_desc_sw128(kst + pn * C::kKvPanel + off, 16, 1024);
                         const uint64_t bq = tc::smem_desc_sw128(sQ + pn * C::kQPanel + off, 16, 1024);
-                        tc::mma_bf16(dS, a, bq, idesc_qk, k > 0 ? 1u : 0u);
+                        if constexpr (F8) {
+                            // A = f16 K from tensor memory: 16 dims per MMA = 8 columns.
+                            tc::mma_bf16_ts(dS, tmem + C::kTmemK + k * 8, bq, idesc_qk, k > 0 ? 1u : 0u);
+                        } else {
+                            const uint64_t a = tc::smem_desc_sw128(kst + pn * C::kKvPanel + off, 16, 1024);
+                            tc::mma_bf16(dS, a, bq, idesc_qk, k > 0 ? 1u : 0u);
+                        }
                     }
                     tc::commit(s_full0 + 8 * (j & 1));
-                    tc::commit(k_empty0 + 8 * stg);
+                    tc::commit(F8 ? kc_empty : k_empty0 + 8 * stg);
                 }
                 __syncwarp();
             }
@@ -357,14 +413,18 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             for (int j = 0; j < n_tiles; ++j) {
                 const int stg = j % NSV;
                 if (!wwait(p_full0 + 8 * (j & 1), (j >> 1) & 1)) break;
-                if (!wwait(v_full0 + 8 * stg, (j / NSV) & 1)) break;
+                if constexpr (F8) {
+                    if (!wwait(vc_full, j & 1)) break;
+                } else {
+                    if (!wwait(v_full0 + 8 * stg, (j / NSV) & 1)) break;
+                }
                 tc::fence_after_sync();
                 const int key0 = (t_begin + j) * kBN;
                 const int nvalid = min(kBN, sk - key0);
-                if (nvalid < kBN) {
+                if (!F8 && nvalid < kBN) {
                     // Keys past S_k: their V rows become zeros so that whatever
                     // the slots hold cannot reach O (0 * NaN is NaN).
-                    uint8_t* vgen = smem + C::kOffV + stg * C::kKvBytes;
+                    uint8_t* vgen = smem + C::kOffV + stg * C::kStage;
                     const int per_panel = (kBN - nvalid) * 8;
                     for (int e = lane; e < per_panel * C::kPanels; e += 32) {
                         const int pn = e / per_panel, rem = e % per_panel;
@@ -375,7 +435,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     __syncwarp();
                 }
                 if (lane == 0) {
-                    const uint32_t vst = sV + stg * C::kKvBytes;
+                    const uint32_t vst = F8 ? smem_u32(smem + C::kOffV16) : sV + stg * C::kStage;
                     const uint32_t pbuf = sP + (j & 1) * C::kPBuf;
 #pragma unroll
                     for (int kk = 0; kk < kBN / 16; ++kk) {
@@ -385,7 +445,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         tc::mma_bf16(tmem + C::kTmemO, a, bp, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
                     }
                     tc::commit(o_done0 + 8 * (j & 1));
-                    tc::commit(v_empty0 + 8 * stg);
+                    tc::commit(F8 ? vc_empty : v_empty0 + 8 * stg);
                 }
                 __syncwarp();
             }
@@ -397,6 +457,67 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             __syncwarp();
             mbar_wait_bounded(dr, 0);
         }
+    } else if (F8 && warp >= 7) {
+        // --------------------- e4m3 -> f16 converters (F8, warps 7-10) ---------------------
+        // Thread (warp, lane) owns key row r of each tile, r = tensor-memory lane
+        // 32 * (warp % 4) + lane: K row r goes to tensor memory (two dims per
+        // column), V row r to the f16 V tile (the swizzled layout a TMA copy of
+        // a bf16 tile would have), zeros for keys past S_k.
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;
+        const uint32_t tk = tmem + ((uint32_t)(quarter * 32) << 16) + C::kTmemK;
+        for (int j = 0; j < n_tiles; ++j) {
+            const int sk_ = j % NSK, sv_ = j % NSV;
+            if (!__all_sync(0xffffffffu, dwait(k_full0 + 8 * sk_, (j / NSK) & 1, abort_flag, p.err))) break;
+            if (j > 0 && !__all_sync(0xffffffffu, dwait(kc_empty, (j - 1) & 1, abort_flag, p.err))) break;
+            tc::fence_after_sync();
+            {
+                const uint8_t* row = smem + C::kOffK + sk_ * C::kStage + r * 128;
+#pragma unroll
+                for (int qq = 0; qq < 4; ++qq) {
+                    uint32_t f[16];
+#pragma unroll
+                    for (int c2 = 0; c2 < 2; ++c2) {
+                        const int c = qq * 2 + c2;   // 16-byte chunk = dims 16c .. 16c + 15
+                        const uint4 w = *reinterpret_cast<const uint4*>(row + ((c ^ (r & 7)) << 4));
+                        e4m3x4_to_f16x2(w.x, f[c2 * 8 + 0], f[c2 * 8 + 1]);
+                        e4m3x4_to_f16x2(w.y, f[c2 * 8 + 2], f[c2 * 8 + 3]);
+                        e4m3x4_to_f16x2(w.z, f[c2 * 8 + 4], f[c2 * 8 + 5]);
+                        e4m3x4_to_f16x2(w.w, f[c2 * 8 + 6], f[c2 * 8 + 7]);
+                    }
+                    tc::st16(tk + qq * 16, f);
+                }
+                tc::wait_st();
+            }
+            tc::fence_before_sync();
+            mbar_arrive(kc_full);
+            mbar_arrive(k_empty0 + 8 * sk_);
+            if (!__all_sync(0xffffffffu, dwait(v_full0 + 8 * sv_, (j / NSV) & 1, abort_flag, p.err))) break;
+            if (j > 0 && !__all_sync(0xffffffffu, dwait(vc_empty, (j - 1) & 1, abort_flag, p.err))) break;
+            {
+                const bool live_key = (t_begin + j) * kBN + r < sk;
+                const uint8_t* row = smem + C::kOffV + sv_ * C::kStage + r * 128;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
+                    if (live_key) {
+                        const uint4 w = *reinterpret_cast<const uint4*>(row + ((c ^ (r & 7)) << 4));
+                        e4m3x4_to_f16x2(w.x, lo.x, lo.y);
+                        e4m3x4_to_f16x2(w.y, lo.z, lo.w);
+                        e4m3x4_to_f16x2(w.z, hi.x, hi.y);
+                        e4m3x4_to_f16x2(w.w, hi.z, hi.w);
+                    }
+                    // dims 16c .. 16c + 15: panel c / 4, 16-byte chunks 2 (c % 4) and 2 (c % 4) + 1
+                    uint8_t* dst = smem + C::kOffV16 + (c >> 2) * C::kKvPanel + r * 128;
+                    const int cc = 2 * (c & 3);
+                    *reinterpret_cast<uint4*>(dst + ((cc ^ (r & 7)) << 4)) = lo;
+                    *reinterpret_cast<uint4*>(dst + (((cc + 1) ^ (r & 7)) << 4)) = hi;
+                }
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(vc_full);
+            mbar_arrive(v_empty0 + 8 * sv_);
+        }
     } else {
         // --------------------------- softmax warps 0-3 ----------------------------
         // Thread t: key t of each KV tile (S^T lane t) and head-dim element t of
@@ -405,7 +526,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
         const bool softcap = (p.flags & UA_FLAG_SOFTCAP) != 0;
         const bool alibi = (p.flags & UA_FLAG_ALIBI) != 0;
-        const float sl2 = p.scale * kLog2e;
+        const float tau = F8 ? p.scale * p.k_scale : p.scale;   // F8: k_scale folded in
+        const float sl2 = tau * kLog2e;
         float m[NR], l[NR];
         // Visible key range [lo, hi] of each packed row (constant per CTA);
         // padding rows get an empty range.
@@ -437,7 +559,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     if constexpr (PLAIN) {
                         v = __uint_as_float(sv[r]) * sl2;
                     } else {
-                        float tt = __uint_as_float(sv[r]) * p.scale;
+                        float tt = __uint_as_float(sv[r]) * tau;
                         if (softcap) tt = p.softcap * tanh_e2(tt / p.softcap);
                         if (alibi) tt += rslope[r] * (float)(key - ctx);
                         v = tt * kLog2e;
@@ -493,7 +615,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     : "r"(e));
                 l[r] = l[r] * alpha[r] + p0;
                 l[r + 1] = l[r + 1] * alpha[r + 1] + p1;
-                pb[r / 2] = pack_bf16x2(p0, p1);
+                pb[r / 2] = F8 ? e : pack_bf16x2(p0, p1);   // the P.V MMA's element type
             }
             // P^T buffer (j & 1) was read by the P.V of tile j - 2; rescaling O
             // needs the P.V of tile j - 1.
@@ -560,7 +682,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     if (r >= nrows) continue;
                     const float L0 = lsum[r] + lsum[kN + r] + lsum[2 * kN + r] + lsum[3 * kN + r];
                     const int64_t row = (q0 + r / g) * p.hq + hkv * g + r % g;
-                    const float ov = __uint_as_float(o[r]);
+                    const float ov = __uint_as_float(o[r]) * (F8 ? p.v_scale : 1.f);
                     if (split) {
                         p.part_o[(row * p.splits + seg) * kD + t] = ov;
                         if (t == 0) {
@@ -594,7 +716,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     __syncthreads();
     if (warp == kWarpMmaD) {
         tc::fence_after_sync();
-        tc::tmem_dealloc(tmem, kTmemColsD);
+        tc::tmem_dealloc(tmem, C::kTmemCols);
     }
 }
 
@@ -627,6 +749,27 @@ void plan_decode_tc(const FwdParams& p, int num_sms, size_t workspace_bytes, Dec
     plan->launches = splits > 1 ? 2 : 1;
 }
 
+namespace {
+
+template <int NSK, int NSV, bool F8>
+cudaError_t launch_decode_t(const CUtensorMap& tq, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                            const FwdParams& p, const DecodePlan& plan, cudaStream_t stream) {
+    using C = DCfg<NSK, NSV, F8>;
+    const bool plain = (p.flags & (UA_FLAG_SOFTCAP | UA_FLAG_ALIBI)) == 0;
+    const int rows = p.g * p.max_seqlen_q;
+    auto kern = rows <= 4 ? (plain ? decode_tc_kernel<NSK, NSV, 4, true, F8> : decode_tc_kernel<NSK, NSV, 4, false, F8>)
+              : rows <= 8 ? (plain ? decode_tc_kernel<NSK, NSV, 8, true, F8> : decode_tc_kernel<NSK, NSV, 8, false, F8>)
+                          : (plain ? decode_tc_kernel<NSK, NSV, 16, true, F8>
+                                   : decode_tc_kernel<NSK, NSV, 16, false, F8>);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    if (e != cudaSuccess) return e;
+    dim3 grid((unsigned)plan.splits, (unsigned)p.hk, (unsigned)p.num_seqs);
+    kern<<<grid, F8 ? kThreadsF8 : kThreadsD, C::kSmem, stream>>>(tq, tm_k, tm_v, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
 cudaError_t launch_decode_tc(const DecodePlan& plan, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                              const FwdParams& p, cudaStream_t stream) {
     // Q map: [total_q, H_q, d]; box = 64 dims x g heads x 16/g positions = 16 rows.
@@ -636,18 +779,11 @@ cudaError_t launch_decode_tc(const DecodePlan& plan, const CUtensorMap& tm_k, co
     cuuint32_t box[3] = {64, (cuuint32_t)p.g, (cuuint32_t)(kN / p.g)};
     if (!encode_bf16_sw128(&tq, p.q, 3, dims, strides, box)) return cudaErrorInvalidValue;
     constexpr int NSK = UA_DEC_NSK, NSV = UA_DEC_NSV;
-    using C = DCfg<NSK, NSV>;
-    const bool plain = (p.flags & (UA_FLAG_SOFTCAP | UA_FLAG_ALIBI)) == 0;
-    const int rows = p.g * p.max_seqlen_q;
-    auto kern = rows <= 4 ? (plain ? decode_tc_kernel<NSK, NSV, 4, true> : decode_tc_kernel<NSK, NSV, 4, false>)
-              : rows <= 8 ? (plain ? decode_tc_kernel<NSK, NSV, 8, true> : decode_tc_kernel<NSK, NSV, 8, false>)
-                          : (plain ? decode_tc_kernel<NSK, NSV, 16, true>
-                                   : decode_tc_kernel<NSK, NSV, 16, false>);
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
-    if (e != cudaSuccess) return e;
-    dim3 grid((unsigned)plan.splits, (unsigned)p.hk, (unsigned)p.num_seqs);
-    kern<<<grid, kThreadsD, C::kSmem, stream>>>(tq, tm_k, tm_v, p);
-    return cudaGetLastError();
+    // fp8 tiles carry half the bytes, so each CTA needs twice the tiles in
+    // flight to keep the same HBM rate: two staging stages per operand (the
+    // e4m3 stages are half the size, so two CTAs still share an SM).
+    return p.kv_fp8 ? launch_decode_t<2, 2, true>(tq, tm_k, tm_v, p, plan, stream)
+                    : launch_decode_t<NSK, NSV, false>(tq, tm_k, tm_v, p, plan, stream);
 }
 
 }  // namespace ua

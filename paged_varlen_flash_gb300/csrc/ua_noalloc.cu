@@ -114,7 +114,7 @@ extern "C" ua_status ua_forward_noalloc(const ua_problem_desc* d, const void* q,
         return UA_ERR_INVALID_ARG;
     if ((d->flags & UA_FLAG_WINDOW) && (d->window < 1 || !(d->flags & UA_FLAG_CAUSAL)))
         return UA_ERR_INVALID_ARG;
-    if (d->dtype != UA_DTYPE_BF16 || (d->head_size != 64 && d->head_size != 128 &&
+    if (d->dtype != UA_DTYPE_BF16 || d->kv_dtype != UA_DTYPE_BF16 || (d->head_size != 64 && d->head_size != 128 &&
                                       d->head_size != 256) ||
         (d->block_size != 16 && d->block_size != 32 && d->block_size != 64) ||
         d->num_blocks > (int64_t(1) << 31) - 1)
