@@ -47,7 +47,8 @@ def _load():
         common = [ctypes.c_int32] * 5 + [ctypes.c_int64] + [ctypes.c_void_p] * 4 + [
             ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_double,
             ctypes.c_int32, ctypes.c_double, ctypes.c_int32, ctypes.c_void_p,
-            ctypes.c_void_p, ctypes.c_int32, ctypes.c_double, ctypes.c_double]
+            ctypes.c_void_p, ctypes.c_int32, ctypes.c_double, ctypes.c_double,
+            ctypes.c_void_p, ctypes.c_int64]
         lib.ua_oracle_forward.argtypes = common + [ctypes.c_void_p, ctypes.c_int32]
         lib.ua_oracle_forward.restype = ctypes.c_int
         lib.ua_oracle_rows.argtypes = common + [ctypes.c_void_p, ctypes.c_int64,
@@ -123,8 +124,12 @@ class _Args:
 
     def __init__(self, q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k,
                  scale, causal=True, softcap=0.0, window=0, alibi_slopes=None,
-                 sinks=None, k_scale=1.0, v_scale=1.0):
+                 sinks=None, k_scale=1.0, v_scale=1.0, qq_bias=None):
         self.q = _bf16_bits(q)
+        self.qq = _f64_or_none(qq_bias)
+        if self.qq is not None:
+            assert self.qq.ndim == 2
+            self.qq = np.ascontiguousarray(self.qq)
         self.k, fp8_k = _kv_bits(k_cache)
         self.v, fp8_v = _kv_bits(v_cache)
         assert fp8_k == fp8_v, "K and V caches must share a dtype"
@@ -154,16 +159,18 @@ class _Args:
                 _ptr(self.q), _ptr(self.k), _ptr(self.v), _ptr(self.bt), self.bt_stride,
                 _ptr(self.cu), _ptr(self.su), self.scale, self.causal, self.softcap,
                 self.window, _ptr(self.alibi), _ptr(self.sinks), self.kv_fp8,
-                self.k_scale, self.v_scale]
+                self.k_scale, self.v_scale, _ptr(self.qq),
+                self.qq.shape[1] if self.qq is not None else 0]
 
 
 def forward(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, scale,
             causal=True, softcap=0.0, window=0, alibi_slopes=None, sinks=None,
-            nthreads=None, k_scale=1.0, v_scale=1.0):
+            nthreads=None, k_scale=1.0, v_scale=1.0, qq_bias=None):
     """All output rows, fp64 numpy [total_q, H_q, d].  fp8 caches are e4m3
-    codes scaled by k_scale / v_scale."""
+    codes scaled by k_scale / v_scale; qq_bias [>= S_q, stride] is the
+    query-section bias shared by all sequences and heads."""
     a = _Args(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, scale,
-              causal, softcap, window, alibi_slopes, sinks, k_scale, v_scale)
+              causal, softcap, window, alibi_slopes, sinks, k_scale, v_scale, qq_bias)
     out = np.zeros((a.total_q, a.hq, a.d), dtype=np.float64)
     rc = _load().ua_oracle_forward(*a.head(), _ptr(out),
                                    nthreads or default_threads())
@@ -174,10 +181,10 @@ def forward(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, scale,
 
 def rows(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, scale, row_ids,
          causal=True, softcap=0.0, window=0, alibi_slopes=None, sinks=None,
-         nthreads=None, k_scale=1.0, v_scale=1.0):
+         nthreads=None, k_scale=1.0, v_scale=1.0, qq_bias=None):
     """Selected output rows (row id = token * H_q + head), fp64 numpy [n, d]."""
     a = _Args(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, scale,
-              causal, softcap, window, alibi_slopes, sinks, k_scale, v_scale)
+              causal, softcap, window, alibi_slopes, sinks, k_scale, v_scale, qq_bias)
     ids = np.ascontiguousarray(np.asarray(row_ids, dtype=np.int64))
     out = np.zeros((ids.shape[0], a.d), dtype=np.float64)
     rc = _load().ua_oracle_rows(*a.head(), _ptr(ids), ids.shape[0], _ptr(out),
@@ -189,10 +196,10 @@ def rows(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, scale, row_i
 
 def row_weights(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, scale,
                 token, head, causal=True, softcap=0.0, window=0, alibi_slopes=None,
-                sinks=None, k_scale=1.0, v_scale=1.0):
+                sinks=None, k_scale=1.0, v_scale=1.0, qq_bias=None):
     """(weights [S_k + 1] with the sink's share last, O_i [d]) for one row."""
     a = _Args(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, scale,
-              causal, softcap, window, alibi_slopes, sinks, k_scale, v_scale)
+              causal, softcap, window, alibi_slopes, sinks, k_scale, v_scale, qq_bias)
     cu = a.cu
     s = int(np.searchsorted(cu, token, side="right") - 1)
     while s + 1 < len(cu) and cu[s + 1] <= token:
@@ -210,7 +217,8 @@ def forward_workload(w, nthreads=None, row_ids=None):
     """Oracle on a ``paged_varlen_flash_gb300.workloads.Workload`` (host copies)."""
     kw = dict(causal=w.causal, softcap=w.softcap, window=w.window,
               alibi_slopes=w.alibi_slopes, sinks=w.sinks, nthreads=nthreads,
-              k_scale=getattr(w, "k_scale", 1.0), v_scale=getattr(w, "v_scale", 1.0))
+              k_scale=getattr(w, "k_scale", 1.0), v_scale=getattr(w, "v_scale", 1.0),
+              qq_bias=getattr(w, "qq_bias", None))
     if row_ids is None:
         return forward(w.q, w.k_cache, w.v_cache, w.block_table, w.cu_seqlens_q,
                        w.seqused_k, w.scale, **kw)

@@ -15,6 +15,7 @@
  *   x_j   = tau * <Q_i, K_j>                                   (step 1, scale)
  *   x_j   = c * tanh(x_j / c)              if SOFTCAP          (step 2)
  *   x_j  += slope_h * (j - ctx)            if ALIBI            (step 3)
+ *   x_j  += bias[i][j - ctx]  for j >= ctx  if QQ-BIAS          (step 4)
  *   j visible iff (not CAUSAL or j <= i + ctx)                 (step 5)
  *             and (not WINDOW or j >= i + ctx - W + 1)         (step 6)
  *   den   = sum_{j visible} e^{x_j}  (+ e^{sink_h} if SINKS)   (step 7)
@@ -36,6 +37,10 @@
  *
  * bf16 inputs are widened exactly (a bf16 value is the upper half of an
  * IEEE-754 binary32), and every product and sum is fp64.
+ *
+ * The QQ-bias (step 4, "inside the query section") is one fp64 matrix shared by
+ * every sequence and head, indexed by the local query index i and the key's
+ * offset j - ctx inside the chunk; keys before the chunk (j < ctx) get none.
  *
  * fp8 KV cache (gfx950 page, section 7.3 "fp8 KV cache (bf16-Q + fp8-KV)"):
  * the cache holds e4m3 codes with one scale per tensor, K_j = e4m3(k) * k_scale
@@ -73,6 +78,8 @@ typedef struct {
     int32_t window;                 /* 0 = off */
     const double *alibi_slopes;     /* [hq] or NULL */
     const double *sinks;            /* [hq] or NULL */
+    const double *qq_bias;          /* [>= S_q][qq_stride] or NULL */
+    int64_t qq_stride;
 } oracle_problem;
 
 static double widen_bf16(uint16_t h)
@@ -166,6 +173,7 @@ static void one_row(const oracle_problem *P, int64_t token, int32_t h, double *o
         double xj = P->scale * dot;
         if (P->softcap > 0.0) xj = P->softcap * tanh(xj / P->softcap);
         if (P->alibi_slopes) xj += P->alibi_slopes[h] * (double)((int64_t)j - ctx);
+        if (P->qq_bias && (int64_t)j >= ctx) xj += P->qq_bias[i * P->qq_stride + ((int64_t)j - ctx)];
         x[j] = xj;
         if (xj > m) m = xj;
     }
@@ -285,7 +293,8 @@ static int run_rows(const oracle_problem *P, const int64_t *rows, int64_t n_rows
  * block_table [num_seqs, bt_stride], cu_seqlens_q [num_seqs + 1],
  * seqused_k [num_seqs]; softcap <= 0 and window <= 0 switch those terms off;
  * alibi_slopes / sinks may be NULL; kv_fp8 != 0 reads the caches as e4m3
- * codes scaled by k_scale / v_scale.  Output is fp64.
+ * codes scaled by k_scale / v_scale; qq_bias (or NULL) is the query-section
+ * bias, row i at qq_bias + i * qq_stride.  Output is fp64.
  * ------------------------------------------------------------------------- */
 
 #define FILL_PROBLEM()                                                        \
@@ -298,7 +307,8 @@ static int run_rows(const oracle_problem *P, const int64_t *rows, int64_t n_rows
     P.softcap = softcap > 0.0 ? softcap : 0.0;                                \
     P.window = window > 0 ? window : 0;                                       \
     P.alibi_slopes = alibi_slopes; P.sinks = sinks;                           \
-    P.kv_fp8 = kv_fp8 ? 1 : 0; P.k_scale = k_scale; P.v_scale = v_scale;
+    P.kv_fp8 = kv_fp8 ? 1 : 0; P.k_scale = k_scale; P.v_scale = v_scale;      \
+    P.qq_bias = qq_bias; P.qq_stride = qq_stride;
 
 #define PROBLEM_ARGS                                                          \
     int32_t num_seqs, int32_t hq, int32_t hk, int32_t d, int32_t b,          \
@@ -307,7 +317,7 @@ static int run_rows(const oracle_problem *P, const int64_t *rows, int64_t n_rows
     const int32_t *cu_seqlens_q, const int32_t *seqused_k, double scale,     \
     int32_t causal, double softcap, int32_t window,                          \
     const double *alibi_slopes, const double *sinks, int32_t kv_fp8,         \
-    double k_scale, double v_scale
+    double k_scale, double v_scale, const double *qq_bias, int64_t qq_stride
 
 /* Every output row: out [total_q, hq, d]. */
 int ua_oracle_forward(PROBLEM_ARGS, double *out, int32_t nthreads)

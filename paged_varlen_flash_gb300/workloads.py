@@ -76,6 +76,7 @@ class Workload:
     kv_fp8: bool = False              # caches hold e4m3 codes (uint8)
     k_scale: float = 1.0              # K = e4m3(k) * k_scale when kv_fp8
     v_scale: float = 1.0
+    qq_bias: Optional[torch.Tensor] = None   # fp32 [max S_q, max S_q] query-section bias
 
     @property
     def num_seqs(self) -> int:
@@ -110,7 +111,7 @@ class Workload:
             mv(self.v_cache), mv(self.block_table), mv(self.cu_seqlens_q),
             mv(self.seqused_k), self.scale, self.causal, self.softcap, self.window,
             mv(self.sinks), mv(self.alibi_slopes), dict(self.meta), self.kv_fp8,
-            self.k_scale, self.v_scale)
+            self.k_scale, self.v_scale, mv(self.qq_bias))
 
     # -- counts used for reporting (no attention arithmetic) ------------------
     def visible_pairs(self) -> int:
@@ -146,7 +147,8 @@ def build(name: str, hq: int, hk: int, d: int, b: int, seqlens_q, seqlens_k,
           seed: int = 0, device="cpu", std: float = 1.0, causal: bool = True,
           softcap: float = 0.0, window: int = 0, sinks: bool = False,
           alibi: bool = False, poison: bool = True, bt_pad: int = 0,
-          values: bool = True, kv_fp8: bool = False, kv_scale: float = 1.0 / 32) -> Workload:
+          values: bool = True, kv_fp8: bool = False, kv_scale: float = 1.0 / 32,
+          qq_bias: bool = False) -> Workload:
     """Assemble a workload from explicit lengths.
 
     ``block_ids`` (int, len >= sum of blocks needed) fixes the physical blocks
@@ -221,10 +223,14 @@ def build(name: str, hq: int, hk: int, d: int, b: int, seqlens_q, seqlens_k,
     if alibi:
         alibi_t = torch.tensor([2.0 ** (-8.0 * h / hq) for h in range(1, hq + 1)],
                                dtype=torch.float32)
+    qq_t = None
+    if qq_bias:
+        mq = max(max(seqlens_q, default=1), 1)
+        qq_t = torch.randn(mq, mq, generator=g, dtype=torch.float32)
     w = Workload(name, hq, hk, d, b, num_blocks, seqlens_q, seqlens_k, q, k_cache,
                  v_cache, table, cu, seqused, float(scale), causal, float(softcap),
                  int(window), sink_t, alibi_t, {"seed": seed}, bool(kv_fp8),
-                 float(kv_scale) if kv_fp8 else 1.0, float(kv_scale) if kv_fp8 else 1.0)
+                 float(kv_scale) if kv_fp8 else 1.0, float(kv_scale) if kv_fp8 else 1.0, qq_t)
     if dev.type != "cpu":
         w.block_table = w.block_table.to(dev)
         w.cu_seqlens_q = w.cu_seqlens_q.to(dev)
@@ -233,6 +239,8 @@ def build(name: str, hq: int, hk: int, d: int, b: int, seqlens_q, seqlens_k,
             w.sinks = w.sinks.to(dev)
         if w.alibi_slopes is not None:
             w.alibi_slopes = w.alibi_slopes.to(dev)
+        if w.qq_bias is not None:
+            w.qq_bias = w.qq_bias.to(dev)
     return w
 
 
@@ -267,7 +275,7 @@ def make(name: str, device="cpu", poison: bool = False, values: bool = True) -> 
 def random_small(seed: int, *, num_seqs=3, hq=8, hk=2, d=64, b=16, sq=(1, 40),
                  ctx=(0, 70), causal=True, softcap=0.0, window=0, sinks=False,
                  alibi=False, device="cpu", poison=True, spare_blocks=5,
-                 std=1.0, kv_fp8=False, kv_scale=1.0 / 32) -> Workload:
+                 std=1.0, kv_fp8=False, kv_scale=1.0 / 32, qq_bias=False) -> Workload:
     """A small seeded ragged batch for parity sweeps (lengths drawn per seq)."""
     g = _gen(seed)
     seqlens_q = _randint(g, sq[0], sq[1], num_seqs)
@@ -277,7 +285,8 @@ def random_small(seed: int, *, num_seqs=3, hq=8, hk=2, d=64, b=16, sq=(1, 40),
     return build("random_small", hq, hk, d, b, seqlens_q, seqlens_k,
                  need + spare_blocks, 1.0 / math.sqrt(d), seed=seed, device=device,
                  std=std, causal=causal, softcap=softcap, window=window, sinks=sinks,
-                 alibi=alibi, poison=poison, bt_pad=1, kv_fp8=kv_fp8, kv_scale=kv_scale)
+                 alibi=alibi, poison=poison, bt_pad=1, kv_fp8=kv_fp8, kv_scale=kv_scale,
+                 qq_bias=qq_bias)
 
 
 def sample_rows(w: Workload, n: int, seed: int = 0) -> torch.Tensor:

@@ -475,3 +475,62 @@ def test_fp8_scales_fold_into_tau_and_the_output():
     np.testing.assert_allclose(a, b, rtol=1e-12, atol=1e-12)
     c = oracle.forward(*args, w.scale, k_scale=0.3, v_scale=3.0, **kw)
     np.testing.assert_allclose(c, 3.0 * a, rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# QQ-bias (gfx950 page, section 1 step 4): s_j += bias[i, j - ctx] for keys
+# inside the query section (j >= ctx), after softcap / ALiBi, before the masks.
+# ---------------------------------------------------------------------------
+
+def _constant_key_workload(sq, sk, causal=True, softcap=0.0, seed=21):
+    """Constant keys (every logit equal) and position-tag values."""
+    w = _blank(sq, sk, causal=causal, seed=seed, softcap=softcap)
+    g = torch.Generator().manual_seed(seed + 1)
+    w.q = torch.randn(w.total_q, w.hq, w.d, generator=g).to(torch.bfloat16)
+    c = torch.randn(w.hk, w.d, generator=g)
+    scatter_logical(w, [c.expand(k, w.hk, w.d).clone() for k in sk],
+                    [position_tags(k, w.hk, w.d) for k in sk])
+    return w
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_qq_bias_closed_form_on_constant_keys(causal):
+    """Equal logits: key j of row i gets weight e^{bias[i, j - ctx]} inside the
+    query section and 1 before it, so O is the weighted mean of the visible
+    position tags -- pins the (i, j - ctx) indexing, the section boundary and
+    the natural-log domain."""
+    sq, sk = [6, 1, 9], [20, 5, 9]
+    w = _constant_key_workload(sq, sk, causal=causal)
+    g = torch.Generator().manual_seed(3)
+    bias = torch.randn(12, 12, generator=g, dtype=torch.float64)
+    bias[2, 1] = -math.inf     # drops one key of local row 2 exactly
+    out = _run(w, qq_bias=bias)
+    bnp = bias.numpy()
+    for tok, (s, i, ctx) in enumerate(token_of_row(w)):
+        lo, hi = _visible_range(i, ctx, sk[s], causal, 0)
+        js = np.arange(lo, hi + 1, dtype=np.int64)
+        wt = np.array([math.exp(bnp[i, j - ctx]) if j >= ctx else 1.0 for j in js])
+        for h in range(w.hq):
+            tags = tag_values(js, h // w.g)
+            for k in range(4):
+                want = float(np.sum(wt * np.asarray(tags[k], dtype=np.float64)) / np.sum(wt))
+                assert abs(out[tok, h, k] - want) < 1e-12
+
+
+def test_qq_bias_zero_is_no_bias_and_it_is_added_after_softcap():
+    w = _constant_key_workload([7, 3], [12, 3], softcap=0.5)
+    base = _run(w)
+    np.testing.assert_array_equal(_run(w, qq_bias=np.zeros((8, 8))), base)
+    # A bias of 2 in the query section multiplies those keys' weights by e^2
+    # whatever the cap; had the bias gone through tanh, the cap of 0.5 would
+    # have flattened it to at most e^0.5.
+    wts = oracle.row_weights(w.q, w.k_cache, w.v_cache, w.block_table, w.cu_seqlens_q,
+                             w.seqused_k, w.scale, token=4, head=1, softcap=0.5)[0]
+    wtb = oracle.row_weights(w.q, w.k_cache, w.v_cache, w.block_table, w.cu_seqlens_q,
+                             w.seqused_k, w.scale, token=4, head=1, softcap=0.5,
+                             qq_bias=np.full((8, 8), 2.0))[0]
+    ctx = 12 - 7
+    manual = wts[:-1].copy()
+    manual[ctx:] *= math.exp(2.0)
+    manual /= manual.sum()
+    np.testing.assert_allclose(wtb[:-1], manual, rtol=1e-12, atol=1e-15)
