@@ -10,11 +10,12 @@
  *
  * with the score transform applied in this fixed order (gfx950 "Unified paged
  * attention on gfx950, from the math up", section 1 "What unified attention
- * computes", steps 1-3 and 5-7):
+ * computes", steps 1-7):
  *
  *     x_j  = tau * <Q_i, K_j>                            scale
  *     x_j  = c * tanh(x_j / c)            UA_FLAG_SOFTCAP
  *     x_j += slope_h * (j - ctx)          UA_FLAG_ALIBI
+ *     x_j += B[i][j - ctx] for j >= ctx   UA_FLAG_QQ_BIAS (see ua_set_qq_bias)
  *     drop j > i + ctx                    UA_FLAG_CAUSAL
  *     drop j < i + ctx - W + 1            UA_FLAG_WINDOW (requires CAUSAL)
  *     sink_h joins the denominator        UA_FLAG_SINKS (no value row)
@@ -69,7 +70,8 @@ enum {
     UA_FLAG_SOFTCAP = 1u << 1,
     UA_FLAG_ALIBI = 1u << 2,
     UA_FLAG_WINDOW = 1u << 3,
-    UA_FLAG_SINKS = 1u << 4
+    UA_FLAG_SINKS = 1u << 4,
+    UA_FLAG_QQ_BIAS = 1u << 5
 };
 
 /* Bits of the device error word. */
@@ -200,6 +202,25 @@ int32_t ua_last_launch_count(const ua_problem *p);
 const char *ua_last_path(const ua_problem *p);
 
 /*
+ * Query-query bias (gfx950 page, section 1, step 4): with UA_FLAG_QQ_BIAS a
+ * call adds B[i][j - ctx] to the score of query row i (the row's index inside
+ * its sequence's query chunk, 0 <= i < S_q) and key j, for the keys of the
+ * query section (ctx <= j < S_k), after softcap and ALiBi and before the
+ * masks.  Keys of the context (j < ctx) get no bias.  B is one fp32 matrix in
+ * natural-log units, shared by every sequence and every query head; its
+ * element (a, c) is bias[a * row_stride + c].
+ *
+ * bias: device pointer, owned by the caller, read by every later call that
+ *       passes UA_FLAG_QQ_BIAS until it is replaced; NULL clears it.
+ * n:    rows and columns of B that may be read; a call with the flag needs
+ *       max_seqlen_q <= n (else UA_ERR_INVALID_ARG, nothing launched).
+ * row_stride: elements between rows, >= n.
+ * The problem must have been created with UA_FLAG_QQ_BIAS in its flags.
+ * Returns UA_ERR_INVALID_ARG for n < 1 or row_stride < n with a non-NULL bias.
+ */
+ua_status ua_set_qq_bias(ua_problem *p, const float *bias, int64_t n, int64_t row_stride);
+
+/*
  * Profiling hook: when both events are non-null, every later forward call
  * records `ev_begin` on its stream immediately before launching its dominant
  * kernel (the attention kernel, not the split combine) and `ev_end`
@@ -226,7 +247,8 @@ ua_status ua_set_profile_events(ua_problem *p, void *ev_begin, void *ev_end);
  * libua.so holds those 16 MiB until the process exits.  Calls whose partials
  * (total_q * H_q * (d + 2) * 4 bytes per segment) do not fit twice in that
  * array return UA_ERR_UNSUPPORTED and launch nothing, as do descriptions
- * with an fp8 cache (kv_dtype != UA_DTYPE_BF16).
+ * with an fp8 cache (kv_dtype != UA_DTYPE_BF16) or with UA_FLAG_QQ_BIAS
+ * (the bias matrix is bound to a ua_problem).
  *
  * device_error: optional caller-owned device int32 that receives the
  * UA_DEVERR_* bits (OR-ed in; the caller clears it).  When NULL the bits go to

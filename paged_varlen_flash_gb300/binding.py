@@ -17,6 +17,7 @@ UA_FLAG_SOFTCAP = 1 << 1
 UA_FLAG_ALIBI = 1 << 2
 UA_FLAG_WINDOW = 1 << 3
 UA_FLAG_SINKS = 1 << 4
+UA_FLAG_QQ_BIAS = 1 << 5
 
 UA_DEVERR_CONTEXT = 1 << 0
 UA_DEVERR_BLOCK_ID = 1 << 1
@@ -94,6 +95,8 @@ def load_library():
     lib.ua_last_launch_count.restype = i32
     lib.ua_last_path.argtypes = [vp]
     lib.ua_last_path.restype = ctypes.c_char_p
+    lib.ua_set_qq_bias.argtypes = [vp, vp, ctypes.c_int64, ctypes.c_int64]
+    lib.ua_set_qq_bias.restype = ctypes.c_int
     lib.ua_set_profile_events.argtypes = [vp, vp, vp]
     lib.ua_set_profile_events.restype = ctypes.c_int
     lib.ua_destroy.argtypes = [vp]
@@ -127,7 +130,7 @@ def _stream(stream):
     return stream.cuda_stream
 
 
-def flags_of(causal=True, softcap=0.0, alibi=False, window=0, sinks=False):
+def flags_of(causal=True, softcap=0.0, alibi=False, window=0, sinks=False, qq_bias=False):
     f = 0
     if causal:
         f |= UA_FLAG_CAUSAL
@@ -139,6 +142,8 @@ def flags_of(causal=True, softcap=0.0, alibi=False, window=0, sinks=False):
         f |= UA_FLAG_WINDOW
     if sinks:
         f |= UA_FLAG_SINKS
+    if qq_bias:
+        f |= UA_FLAG_QQ_BIAS
     return f
 
 
@@ -199,6 +204,13 @@ def ua_forward_noalloc(desc, q, k_cache, v_cache, block_table, cu_seqlens_q, seq
               _ptr(device_error), _stream(stream))
 
 
+def ua_set_qq_bias(problem, bias, n, row_stride):
+    """Bind the query-query bias matrix (device fp32, element (a, c) at
+    a * row_stride + c) to a problem; ``bias=None`` clears it.  Returns the
+    status code without raising."""
+    return load_library().ua_set_qq_bias(problem, _ptr(bias), n, row_stride)
+
+
 def ua_check_device_error(problem, stream=None):
     """Synchronise the stream and return (and clear) the device error word."""
     code = ctypes.c_int32(0)
@@ -231,7 +243,7 @@ class Problem:
     def for_workload(cls, w, max_total_q=None, max_num_seqs=None, extra_flags=0,
                      path=UA_PATH_AUTO):
         flags = flags_of(w.causal, w.softcap, w.alibi_slopes is not None, w.window,
-                         w.sinks is not None) | extra_flags
+                         w.sinks is not None, getattr(w, "qq_bias", None) is not None) | extra_flags
         fp8 = getattr(w, "kv_fp8", False)
         return cls(w.hq, w.hk, w.d, w.b, w.num_blocks, max_num_seqs or max(1, w.num_seqs),
                    w.max_blocks_per_seq, max_total_q or max(1, w.total_q), flags, w.scale,
@@ -253,11 +265,28 @@ class Problem:
 
     def forward_workload(self, w, out=None, stream=None):
         """Forward on a device-resident ``workloads.Workload``."""
+        qq = getattr(w, "qq_bias", None)
         flags = flags_of(w.causal, w.softcap, w.alibi_slopes is not None, w.window,
-                         w.sinks is not None)
+                         w.sinks is not None, qq is not None)
+        if qq is not None:
+            self.set_qq_bias(qq)
         return self.forward(w.q, w.k_cache, w.v_cache, w.block_table, w.cu_seqlens_q,
                             w.seqused_k, w.num_seqs, w.total_q, w.max_seqlen_q,
                             w.max_seqlen_k, flags, w.sinks, w.alibi_slopes, out, stream)
+
+    def set_qq_bias(self, bias):
+        """Bind a device fp32 matrix [n, >= n] (unit inner stride) as the
+        query-query bias of later calls with UA_FLAG_QQ_BIAS; None clears it.
+        The problem keeps a reference so the memory outlives its use."""
+        if bias is None:
+            st = ua_set_qq_bias(self.handle, None, 0, 0)
+        else:
+            if bias.dim() != 2 or bias.stride(1) != 1 or bias.shape[1] < bias.shape[0]:
+                raise ValueError("qq bias must be [n, >= n] with unit inner stride")
+            st = ua_set_qq_bias(self.handle, bias, bias.shape[0], bias.stride(0))
+        if st != UA_OK:
+            raise UAError(st, "ua_set_qq_bias")
+        self._qq_bias = bias
 
     def check_device_error(self, stream=None):
         return ua_check_device_error(self.handle, stream)

@@ -87,6 +87,10 @@ struct ua_problem {
     int32_t* st_su = nullptr;
     float* st_sinks = nullptr;
     float* st_alibi = nullptr;
+    // query-query bias set by ua_set_qq_bias (caller-owned device memory)
+    const float* qq_bias = nullptr;
+    int64_t qq_n = 0;
+    int64_t qq_stride = 0;
     // tensor maps of the most recent caches (re-encoded when the pointers change)
     const void* map_k_ptr = nullptr;
     const void* map_v_ptr = nullptr;
@@ -125,7 +129,7 @@ ua_status ua_problem_create(const ua_problem_desc* d, ua_problem** out) {
     if (!d || !out) return UA_ERR_INVALID_ARG;
     *out = nullptr;
     const uint32_t known = UA_FLAG_CAUSAL | UA_FLAG_SOFTCAP | UA_FLAG_ALIBI | UA_FLAG_WINDOW |
-                           UA_FLAG_SINKS;
+                           UA_FLAG_SINKS | UA_FLAG_QQ_BIAS;
     if (d->num_q_heads <= 0 || d->num_kv_heads <= 0 || d->num_q_heads % d->num_kv_heads != 0)
         return UA_ERR_INVALID_ARG;
     if (d->num_blocks <= 0 || d->max_num_seqs <= 0 || d->max_blocks_per_seq <= 0 ||
@@ -203,6 +207,21 @@ int32_t ua_last_launch_count(const ua_problem* p) { return p ? p->last_launches 
 
 const char* ua_last_path(const ua_problem* p) { return p ? p->last_path : "none"; }
 
+ua_status ua_set_qq_bias(ua_problem* p, const float* bias, int64_t n, int64_t row_stride) {
+    if (!p || !(p->desc.flags & UA_FLAG_QQ_BIAS)) return UA_ERR_INVALID_ARG;
+    if (!bias) {
+        p->qq_bias = nullptr;
+        p->qq_n = p->qq_stride = 0;
+        return UA_OK;
+    }
+    if (n < 1 || row_stride < n || (reinterpret_cast<uintptr_t>(bias) & 3u) != 0)
+        return UA_ERR_INVALID_ARG;
+    p->qq_bias = bias;
+    p->qq_n = n;
+    p->qq_stride = row_stride;
+    return UA_OK;
+}
+
 ua_status ua_set_profile_events(ua_problem* p, void* ev_begin, void* ev_end) {
     if (!p || ((ev_begin == nullptr) != (ev_end == nullptr))) return UA_ERR_INVALID_ARG;
     p->prof_begin = reinterpret_cast<cudaEvent_t>(ev_begin);
@@ -228,6 +247,8 @@ ua_status ua_forward(ua_problem* p, const void* q, const void* k_cache, const vo
     if ((flags & UA_FLAG_WINDOW) && !(flags & UA_FLAG_CAUSAL)) return UA_ERR_INVALID_ARG;
     if (((flags & UA_FLAG_SINKS) != 0) != (sinks != nullptr)) return UA_ERR_INVALID_ARG;
     if (((flags & UA_FLAG_ALIBI) != 0) != (alibi_slopes != nullptr)) return UA_ERR_INVALID_ARG;
+    if ((flags & UA_FLAG_QQ_BIAS) && (!p->qq_bias || (int64_t)max_seqlen_q > p->qq_n))
+        return UA_ERR_INVALID_ARG;
     if (num_seqs == 0 || total_q == 0) return UA_OK;
     if (!q || !k_cache || !v_cache || !block_table || !cu_seqlens_q || !seqused_k || !out)
         return UA_ERR_INVALID_ARG;
@@ -271,6 +292,10 @@ ua_status ua_forward(ua_problem* p, const void* q, const void* k_cache, const vo
     fp.kv_fp8 = d.kv_dtype == UA_DTYPE_FP8_E4M3 ? 1 : 0;
     fp.k_scale = fp.kv_fp8 ? d.k_scale : 1.f;
     fp.v_scale = fp.kv_fp8 ? d.v_scale : 1.f;
+    if (flags & UA_FLAG_QQ_BIAS) {
+        fp.qq_bias = p->qq_bias;
+        fp.qq_stride = p->qq_stride;
+    }
 
     if (k_cache != p->map_k_ptr || v_cache != p->map_v_ptr) {
         if (!encode_cache_map(&p->map_k16, k_cache, d, 16) ||

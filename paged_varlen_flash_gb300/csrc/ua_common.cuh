@@ -18,6 +18,7 @@ struct FwdParams {
     const int32_t* seqused_k;      // [num_seqs]
     const float* sinks;            // [hq] or null
     const float* alibi;            // [hq] or null
+    const float* qq_bias;          // query-query bias B, element (a, c) at a * qq_stride + c, or null
     __nv_bfloat16* out;            // [total_q, hq, d]
     float* part_o;                 // [total_q * hq, splits, d] split partials
     float* part_ml;                // [total_q * hq, splits, 2] (m in log2 units, l)
@@ -38,6 +39,7 @@ struct FwdParams {
     int32_t row_tiles;             // row tiles per (sequence, kv head)
     int32_t kv_fp8;                // caches hold e4m3 codes
     float k_scale, v_scale;        // fp8 caches: K = code * k_scale, V = code * v_scale
+    int64_t qq_stride;             // row stride of qq_bias
 };
 
 // Per-sequence metadata check.  Returns UA_DEVERR_* bits (0 = well formed) and

@@ -526,6 +526,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
         const bool softcap = (p.flags & UA_FLAG_SOFTCAP) != 0;
         const bool alibi = (p.flags & UA_FLAG_ALIBI) != 0;
+        const bool qq = (p.flags & UA_FLAG_QQ_BIAS) != 0;
         const float tau = F8 ? p.scale * p.k_scale : p.scale;   // F8: k_scale folded in
         const float sl2 = tau * kLog2e;
         float m[NR], l[NR];
@@ -562,6 +563,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         float tt = __uint_as_float(sv[r]) * tau;
                         if (softcap) tt = p.softcap * tanh_e2(tt / p.softcap);
                         if (alibi) tt += rslope[r] * (float)(key - ctx);
+                        // Query section of row r (position r / g); keys past
+                        // the row's last visible key read nothing.
+                        if (qq && key >= ctx && key <= rhi[r])
+                            tt += __ldg(p.qq_bias + (int64_t)(r / g) * p.qq_stride + (key - ctx));
                         v = tt * kLog2e;
                     }
                     x[r] = (key >= rlo[r] && key <= rhi[r]) ? v : -INFINITY;
@@ -755,7 +760,7 @@ template <int NSK, int NSV, bool F8>
 cudaError_t launch_decode_t(const CUtensorMap& tq, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                             const FwdParams& p, const DecodePlan& plan, cudaStream_t stream) {
     using C = DCfg<NSK, NSV, F8>;
-    const bool plain = (p.flags & (UA_FLAG_SOFTCAP | UA_FLAG_ALIBI)) == 0;
+    const bool plain = (p.flags & (UA_FLAG_SOFTCAP | UA_FLAG_ALIBI | UA_FLAG_QQ_BIAS)) == 0;
     const int rows = p.g * p.max_seqlen_q;
     auto kern = rows <= 4 ? (plain ? decode_tc_kernel<NSK, NSV, 4, true, F8> : decode_tc_kernel<NSK, NSV, 4, false, F8>)
               : rows <= 8 ? (plain ? decode_tc_kernel<NSK, NSV, 8, true, F8> : decode_tc_kernel<NSK, NSV, 8, false, F8>)

@@ -105,11 +105,12 @@ extern "C" ua_status ua_forward_noalloc(const ua_problem_desc* d, const void* q,
                                         int32_t* device_error, void* stream) {
     if (!d) return UA_ERR_INVALID_ARG;
     const uint32_t known = UA_FLAG_CAUSAL | UA_FLAG_SOFTCAP | UA_FLAG_ALIBI | UA_FLAG_WINDOW |
-                           UA_FLAG_SINKS;
+                           UA_FLAG_SINKS | UA_FLAG_QQ_BIAS;
     if (d->num_q_heads <= 0 || d->num_kv_heads <= 0 || d->num_q_heads % d->num_kv_heads != 0 ||
         d->num_blocks <= 0 || d->max_blocks_per_seq <= 0 || (d->flags & ~known) ||
         !(d->scale > 0.f) || !std::isfinite(d->scale))
         return UA_ERR_INVALID_ARG;
+    if (d->flags & UA_FLAG_QQ_BIAS) return UA_ERR_UNSUPPORTED;   // the bias is bound to a ua_problem
     if ((d->flags & UA_FLAG_SOFTCAP) && !(d->softcap > 0.f && std::isfinite(d->softcap)))
         return UA_ERR_INVALID_ARG;
     if ((d->flags & UA_FLAG_WINDOW) && (d->window < 1 || !(d->flags & UA_FLAG_CAUSAL)))

@@ -408,6 +408,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         const float sl2 = p.scale * kLog2e;
         const float slope = alibi ? __ldg(p.alibi + head) : 0.f;
         const float inv_cap = softcap ? 1.0f / p.softcap : 0.f;
+        // The row's line of the query-query bias (none for padding rows).
+        const float* qrow = ((p.flags & UA_FLAG_QQ_BIAS) && row_valid)
+                                ? p.qq_bias + (int64_t)i * p.qq_stride
+                                : nullptr;
         const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16);
         float* red = reinterpret_cast<float*>(smem + C::kOffRed);
         // Keys every row of the tile sees: [kfree_lo, kfree_hi].
@@ -438,6 +442,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     // ALiBi: one int -> float conversion per tile; the per-key
                     // offsets are compile-time constants.
                     const float abias = slope * (float)(key0 - ctx);
+                    // Query-query bias on the query-section keys up to the
+                    // row's last visible key (so j - ctx < S_q).
+                    const bool qtile = qrow != nullptr && key0 + CPT > ctx && key0 <= hi;
 #pragma unroll
                     for (int c = 0; c < CPT / 32; ++c)
 #pragma unroll
@@ -445,6 +452,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                             float t = __uint_as_float(sr[c][e]) * p.scale;
                             if (softcap) t = p.softcap * tanh_via_exp2(t * inv_cap);
                             if (alibi) t += abias + slope * (float)(c * 32 + e);
+                            if (qtile) {
+                                const int kc = key0 - ctx + c * 32 + e;
+                                if (kc >= 0 && kc <= hi - ctx) t += __ldg(qrow + kc);
+                            }
                             sr[c][e] = __float_as_uint(t * kLog2e);
                         }
                 }
@@ -720,7 +731,7 @@ cudaError_t launch_prefill(const PrefillPlan& plan, const CUtensorMap& tm_k, con
     if (plan.num_tiles <= 0) return cudaSuccess;
     if (prefill_pair_supported(p.d))
         return launch_prefill_pair(tq, tm_k, tm_v, p, (plan.num_tiles + 1) / 2, stream);
-    const bool plain = (p.flags & (UA_FLAG_SOFTCAP | UA_FLAG_ALIBI)) == 0;
+    const bool plain = (p.flags & (UA_FLAG_SOFTCAP | UA_FLAG_ALIBI | UA_FLAG_QQ_BIAS)) == 0;
     if (p.d != 256) return cudaErrorInvalidValue;
     return plain ? launch_t<256, 64, 2, 2, 2, true, UA_PF256_CL>(tq, tm_k, tm_v, p, plan.num_tiles, stream)
                  : launch_t<256, 64, 2, 2, 2, false, UA_PF256_CL>(tq, tm_k, tm_v, p, plan.num_tiles, stream);

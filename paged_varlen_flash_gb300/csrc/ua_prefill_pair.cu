@@ -392,6 +392,10 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         const bool valid = (x == 0 || has_b) && pos <= last;
         const int hi = causal ? min(pos + ctx, sk - 1) : sk - 1;
         const int lo = window ? max(0, pos + ctx - p.window + 1) : 0;
+        // The row's line of the query-query bias (none for padding rows).
+        const float* qrow = ((p.flags & UA_FLAG_QQ_BIAS) && valid)
+                                ? p.qq_bias + (int64_t)pos * p.qq_stride
+                                : nullptr;
         // Keys every row of the tile sees: [kfree_lo, kfree_hi].
         const int kfree_hi = causal ? min(first + ctx, sk - 1) : sk - 1;
         const int kfree_lo = window ? max(0, last + ctx - p.window + 1) : 0;
@@ -436,6 +440,9 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                     // ALiBi: one int -> float conversion per tile; the per-key
                     // offsets are compile-time constants.
                     const float abias = slope * (float)(key0 - ctx);
+                    // Query-query bias on the query-section keys up to the
+                    // row's last visible key (so j - ctx < S_q).
+                    const bool qtile = qrow != nullptr && key0 + kBN > ctx && key0 <= hi;
 #pragma unroll
                     for (int c = 0; c < kBN / 32; ++c)
 #pragma unroll
@@ -443,6 +450,10 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                             float t = __uint_as_float(sr[c][e]) * p.scale;
                             if (softcap) t = p.softcap * tanh_via_exp2(t * inv_cap);
                             if (alibi) t += abias + slope * (float)(c * 32 + e);
+                            if (qtile) {
+                                const int kc = key0 - ctx + c * 32 + e;
+                                if (kc >= 0 && kc <= hi - ctx) t += __ldg(qrow + kc);
+                            }
                             sr[c][e] = __float_as_uint(t * kLog2e);
                         }
                 }
@@ -624,7 +635,7 @@ bool prefill_pair_supported(int d) { return d == 64 || d == 128; }
 
 cudaError_t launch_prefill_pair(const CUtensorMap& tq, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                                 const FwdParams& p, int pairs, cudaStream_t stream) {
-    const bool plain = (p.flags & (UA_FLAG_SOFTCAP | UA_FLAG_ALIBI)) == 0;
+    const bool plain = (p.flags & (UA_FLAG_SOFTCAP | UA_FLAG_ALIBI | UA_FLAG_QQ_BIAS)) == 0;
     switch (p.d) {
         case 64:
             return plain ? launch_pair_t<64, 4, 4, true>(tq, tm_k, tm_v, p, pairs, stream)

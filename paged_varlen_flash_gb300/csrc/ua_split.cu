@@ -207,6 +207,7 @@ split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
     float* p_s = reinterpret_cast<float*>(smem + L::kPOff) + warp * kSub * ROWS;
     const bool softcap = (p.flags & UA_FLAG_SOFTCAP) != 0;
     const bool alibi = (p.flags & UA_FLAG_ALIBI) != 0;
+    const bool qq = (p.flags & UA_FLAG_QQ_BIAS) != 0;
     const float qk_scale_log2 = p.scale * kLog2e;
     bool timed_out = false;
     int fail_it = 0;
@@ -248,10 +249,14 @@ split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
         for (int r = 0; r < ROWS; ++r) {
             acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], 16);
             float x2;
-            if (softcap || alibi) {
+            if (softcap || alibi || qq) {
                 float t = acc[r] * p.scale;
                 if (softcap) t = p.softcap * tanh_exp2(t / p.softcap);
                 if (alibi) t += __ldg(p.alibi + row_h[r]) * (float)(j - ctx);
+                // Query section only; row_hi < S_k keeps j - ctx < S_q, and
+                // padding rows (row_hi = -1) read nothing.
+                if (qq && j >= ctx && j <= row_hi[r])
+                    t += __ldg(p.qq_bias + (row_tok[r] - q0) * p.qq_stride + (j - ctx));
                 x2 = t * kLog2e;
             } else {
                 x2 = acc[r] * qk_scale_log2;

@@ -92,3 +92,17 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(binding, "_LIB_PATH", str(tmp_path / "nope.so"))
     with pytest.raises(RuntimeError, match="not built"):
         binding.load_library()
+
+
+def test_qq_bias_setter_checks_its_arguments_on_the_host(lib):
+    # No problem handle: rejected before anything else is looked at.
+    assert lib.ua_set_qq_bias(None, None, 0, 0) == 1
+    assert ua.UA_FLAG_QQ_BIAS == 1 << 5
+
+
+def test_noalloc_rejects_the_qq_bias_flag_before_any_device_work(lib):
+    d = _desc(flags=ua.UA_FLAG_CAUSAL | ua.UA_FLAG_QQ_BIAS)
+    st = ua.ua_forward_noalloc(d, None, None, None, None, None, None, 1, 1, 1, 1,
+                               ua.UA_FLAG_CAUSAL | ua.UA_FLAG_QQ_BIAS, None, None, None,
+                               stream=0)
+    assert st == 2
