@@ -106,6 +106,13 @@ enum { UA_DTYPE_BF16 = 0, UA_DTYPE_FP8_E4M3 = 1 };
  * A forced path that does not apply returns UA_ERR_UNSUPPORTED. */
 enum { UA_PATH_AUTO = 0, UA_PATH_SPLIT_KV = 1, UA_PATH_TENSOR_CORE = 2, UA_PATH_DECODE_TC = 3 };
 
+/* Storage of the per-segment o partials that a KV-split call writes and the
+ * combine kernel reads (gfx950 spec section 5; storing them in bf16 halves
+ * their bytes and stores, as the pages' sparse decode kernel does).  m and l
+ * stay fp32 either way; bf16 rounds each partial o element once (relative
+ * error <= 2^-9 of that element). */
+enum { UA_PARTIALS_F32 = 0, UA_PARTIALS_BF16 = 1 };
+
 /*
  * Static description of a problem family (UnifiedAttentionProblem in the
  * gfx950 spec: one flag per bias/mask term, section 1 last paragraph and
@@ -132,6 +139,7 @@ typedef struct ua_problem_desc {
                                    UA_ERR_UNSUPPORTED) */
     float k_scale;              /* fp8 caches: K = code * k_scale, > 0; else ignored */
     float v_scale;              /* fp8 caches: V = code * v_scale, > 0; else ignored */
+    int32_t split_partials;     /* UA_PARTIALS_F32 (0, the default) or UA_PARTIALS_BF16 */
 } ua_problem_desc;
 
 typedef struct ua_problem ua_problem;

@@ -13,7 +13,7 @@ from .binding import (  # noqa: F401
     UA_FLAG_QQ_BIAS,
     UA_DEVERR_BLOCK_ID, UA_DEVERR_BOUNDS, UA_DEVERR_CONTEXT, UA_DEVERR_CU_SEQLENS,
     UA_DEVERR_TIMEOUT, UA_PATH_AUTO, UA_PATH_SPLIT_KV, UA_PATH_TENSOR_CORE, UA_PATH_DECODE_TC,
-    UA_DTYPE_BF16, UA_DTYPE_FP8_E4M3,
+    UA_DTYPE_BF16, UA_DTYPE_FP8_E4M3, UA_PARTIALS_F32, UA_PARTIALS_BF16,
     UAError, Problem, flags_of, lib_path, load_library,
     ua_check_device_error, ua_destroy, ua_forward, ua_forward_host, ua_forward_noalloc,
     ua_problem_create, ua_set_qq_bias,

@@ -18,6 +18,8 @@ UA_FLAG_ALIBI = 1 << 2
 UA_FLAG_WINDOW = 1 << 3
 UA_FLAG_SINKS = 1 << 4
 UA_FLAG_QQ_BIAS = 1 << 5
+UA_PARTIALS_F32 = 0
+UA_PARTIALS_BF16 = 1
 
 UA_DEVERR_CONTEXT = 1 << 0
 UA_DEVERR_BLOCK_ID = 1 << 1
@@ -64,6 +66,7 @@ class ProblemDesc(ctypes.Structure):
         ("kv_dtype", ctypes.c_int32),
         ("k_scale", ctypes.c_float),
         ("v_scale", ctypes.c_float),
+        ("split_partials", ctypes.c_int32),
     ]
 
 
@@ -150,12 +153,12 @@ def flags_of(causal=True, softcap=0.0, alibi=False, window=0, sinks=False, qq_bi
 def ua_problem_create(num_q_heads, num_kv_heads, head_size, block_size, num_blocks,
                       max_num_seqs, max_blocks_per_seq, max_total_q, flags, scale,
                       softcap=0.0, window=0, path=UA_PATH_AUTO, kv_dtype=UA_DTYPE_BF16,
-                      k_scale=1.0, v_scale=1.0):
+                      k_scale=1.0, v_scale=1.0, split_partials=UA_PARTIALS_F32):
     """Returns an opaque problem handle (int); raises UAError on failure."""
     lib = load_library()
     d = ProblemDesc(num_q_heads, num_kv_heads, head_size, block_size, num_blocks,
                     max_num_seqs, max_blocks_per_seq, max_total_q, UA_DTYPE_BF16, flags,
-                    scale, softcap, window, path, kv_dtype, k_scale, v_scale)
+                    scale, softcap, window, path, kv_dtype, k_scale, v_scale, split_partials)
     h = ctypes.c_void_p()
     st = lib.ua_problem_create(ctypes.byref(d), ctypes.byref(h))
     if st != UA_OK:
@@ -230,25 +233,26 @@ class Problem:
 
     def __init__(self, num_q_heads, num_kv_heads, head_size, block_size, num_blocks,
                  max_num_seqs, max_blocks_per_seq, max_total_q, flags, scale, softcap=0.0,
-                 window=0, path=UA_PATH_AUTO, kv_dtype=UA_DTYPE_BF16, k_scale=1.0, v_scale=1.0):
+                 window=0, path=UA_PATH_AUTO, kv_dtype=UA_DTYPE_BF16, k_scale=1.0, v_scale=1.0,
+                 split_partials=UA_PARTIALS_F32):
         self.handle = ua_problem_create(num_q_heads, num_kv_heads, head_size, block_size,
                                         num_blocks, max_num_seqs, max_blocks_per_seq,
                                         max_total_q, flags, scale, softcap, window, path,
-                                        kv_dtype, k_scale, v_scale)
+                                        kv_dtype, k_scale, v_scale, split_partials)
         self.flags = flags
         self.head_size = head_size
         self.num_q_heads = num_q_heads
 
     @classmethod
     def for_workload(cls, w, max_total_q=None, max_num_seqs=None, extra_flags=0,
-                     path=UA_PATH_AUTO):
+                     path=UA_PATH_AUTO, split_partials=UA_PARTIALS_F32):
         flags = flags_of(w.causal, w.softcap, w.alibi_slopes is not None, w.window,
                          w.sinks is not None, getattr(w, "qq_bias", None) is not None) | extra_flags
         fp8 = getattr(w, "kv_fp8", False)
         return cls(w.hq, w.hk, w.d, w.b, w.num_blocks, max_num_seqs or max(1, w.num_seqs),
                    w.max_blocks_per_seq, max_total_q or max(1, w.total_q), flags, w.scale,
                    w.softcap, w.window, path, UA_DTYPE_FP8_E4M3 if fp8 else UA_DTYPE_BF16,
-                   getattr(w, "k_scale", 1.0), getattr(w, "v_scale", 1.0))
+                   getattr(w, "k_scale", 1.0), getattr(w, "v_scale", 1.0), split_partials)
 
     def forward(self, q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, num_seqs,
                 total_q, max_seqlen_q, max_seqlen_k, flags, sinks=None, alibi_slopes=None,

@@ -155,6 +155,8 @@ ua_status ua_problem_create(const ua_problem_desc* d, ua_problem** out) {
     if (d->block_size != 16 && d->block_size != 32 && d->block_size != 64) return UA_ERR_UNSUPPORTED;
     if (d->num_blocks > (int64_t(1) << 31) - 1) return UA_ERR_UNSUPPORTED;
     if (d->path > UA_PATH_DECODE_TC) return UA_ERR_INVALID_ARG;
+    if (d->split_partials != UA_PARTIALS_F32 && d->split_partials != UA_PARTIALS_BF16)
+        return UA_ERR_INVALID_ARG;
 
     ua_problem* p = new (std::nothrow) ua_problem();
     if (!p) return UA_ERR_OUT_OF_MEMORY;
@@ -292,6 +294,7 @@ ua_status ua_forward(ua_problem* p, const void* q, const void* k_cache, const vo
     fp.kv_fp8 = d.kv_dtype == UA_DTYPE_FP8_E4M3 ? 1 : 0;
     fp.k_scale = fp.kv_fp8 ? d.k_scale : 1.f;
     fp.v_scale = fp.kv_fp8 ? d.v_scale : 1.f;
+    fp.part_bf16 = d.split_partials == UA_PARTIALS_BF16 ? 1 : 0;
     if (flags & UA_FLAG_QQ_BIAS) {
         fp.qq_bias = p->qq_bias;
         fp.qq_stride = p->qq_stride;

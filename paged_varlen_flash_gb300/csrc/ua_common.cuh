@@ -40,6 +40,7 @@ struct FwdParams {
     int32_t kv_fp8;                // caches hold e4m3 codes
     float k_scale, v_scale;        // fp8 caches: K = code * k_scale, V = code * v_scale
     int64_t qq_stride;             // row stride of qq_bias
+    int32_t part_bf16;             // part_o holds bf16 (same element indexing) instead of fp32
 };
 
 // Per-sequence metadata check.  Returns UA_DEVERR_* bits (0 = well formed) and
@@ -62,6 +63,44 @@ __device__ __forceinline__ uint32_t seq_status(const FwdParams& p, int s, int& s
         (int64_t)sk > (int64_t)p.bt_stride * p.b)
         st |= UA_DEVERR_BOUNDS;
     return st;
+}
+
+// Split partials of o: fp32, or bf16 when p.part_bf16 (half the bytes, same
+// element index; m and l stay fp32).
+__device__ __forceinline__ void part_store(const FwdParams& p, int64_t idx, float v) {
+    if (p.part_bf16)
+        reinterpret_cast<__nv_bfloat16*>(p.part_o)[idx] = __float2bfloat16_rn(v);
+    else
+        p.part_o[idx] = v;
+}
+
+__device__ __forceinline__ float part_load(const FwdParams& p, int64_t idx) {
+    return p.part_bf16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p.part_o)[idx])
+                       : p.part_o[idx];
+}
+
+// 32 consecutive elements from fp32 bit patterns; idx is a multiple of 32.
+__device__ __forceinline__ void part_store32(const FwdParams& p, int64_t idx, const uint32_t* o) {
+    if (p.part_bf16) {
+        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.part_o) + idx);
+#pragma unroll
+        for (int e = 0; e < 32; e += 8) {
+            uint32_t w[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(o[e + 2 * k]),
+                                                               __uint_as_float(o[e + 2 * k + 1]));
+                w[k] = *reinterpret_cast<const uint32_t*>(&h);
+            }
+            dst[e / 8] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+    } else {
+        float4* dst = reinterpret_cast<float4*>(p.part_o + idx);
+#pragma unroll
+        for (int e = 0; e < 32; e += 4)
+            dst[e / 4] = make_float4(__uint_as_float(o[e]), __uint_as_float(o[e + 1]),
+                                     __uint_as_float(o[e + 2]), __uint_as_float(o[e + 3]));
+    }
 }
 
 // Number of split segments sequence s uses (the split kernel and the combine

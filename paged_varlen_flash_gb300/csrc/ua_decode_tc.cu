@@ -689,7 +689,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     const int64_t row = (q0 + r / g) * p.hq + hkv * g + r % g;
                     const float ov = __uint_as_float(o[r]) * (F8 ? p.v_scale : 1.f);
                     if (split) {
-                        p.part_o[(row * p.splits + seg) * kD + t] = ov;
+                        part_store(p, (row * p.splits + seg) * kD + t, ov);
                         if (t == 0) {
                             p.part_ml[(row * p.splits + seg) * 2 + 0] = m[r];
                             p.part_ml[(row * p.splits + seg) * 2 + 1] = L0;

@@ -111,6 +111,8 @@ extern "C" ua_status ua_forward_noalloc(const ua_problem_desc* d, const void* q,
         !(d->scale > 0.f) || !std::isfinite(d->scale))
         return UA_ERR_INVALID_ARG;
     if (d->flags & UA_FLAG_QQ_BIAS) return UA_ERR_UNSUPPORTED;   // the bias is bound to a ua_problem
+    if (d->split_partials != UA_PARTIALS_F32 && d->split_partials != UA_PARTIALS_BF16)
+        return UA_ERR_INVALID_ARG;
     if ((d->flags & UA_FLAG_SOFTCAP) && !(d->softcap > 0.f && std::isfinite(d->softcap)))
         return UA_ERR_INVALID_ARG;
     if ((d->flags & UA_FLAG_WINDOW) && (d->window < 1 || !(d->flags & UA_FLAG_CAUSAL)))
@@ -192,6 +194,7 @@ extern "C" ua_status ua_forward_noalloc(const ua_problem_desc* d, const void* q,
 
     ua::FwdParams fp;
     std::memset(&fp, 0, sizeof fp);
+    fp.part_bf16 = d->split_partials == UA_PARTIALS_BF16 ? 1 : 0;
     fp.q = static_cast<const __nv_bfloat16*>(q);
     fp.block_table = block_table;
     fp.cu_seqlens_q = cu_seqlens_q;

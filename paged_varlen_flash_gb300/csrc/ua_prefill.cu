@@ -584,7 +584,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 #pragma unroll
                 for (int o = 1; o < SPLIT; ++o) L += red[((half + o) % SPLIT) * kRows + r];
                 const int64_t row = (q0 + i) * p.hq + head;
-                float* po = p.part_o + (row * p.splits + seg) * D + half * OPT;
+                const int64_t po = (row * p.splits + seg) * D + half * OPT;
                 if (row_valid && half == 0) {
                     p.part_ml[(row * p.splits + seg) * 2 + 0] = m;
                     p.part_ml[(row * p.splits + seg) * 2 + 1] = L;
@@ -594,13 +594,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     uint32_t o[32];
                     tc::ld32(trow + C::kTmemO + half * OPT + c * 32, o);
                     tc::wait_ld();
-                    if (row_valid) {
-#pragma unroll
-                        for (int e = 0; e < 32; e += 4)
-                            *reinterpret_cast<float4*>(po + c * 32 + e) =
-                                make_float4(__uint_as_float(o[e]), __uint_as_float(o[e + 1]),
-                                            __uint_as_float(o[e + 2]), __uint_as_float(o[e + 3]));
-                    }
+                    if (row_valid) part_store32(p, po + c * 32, o);
                 }
             } else if (all_done && live && !split) {
                 tc::fence_after_sync();

@@ -581,12 +581,7 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 tc::wait_ld();
                 if (!valid) continue;
                 if (split) {
-                    float* po = p.part_o + (row * p.splits + seg) * D + c * 32;
-#pragma unroll
-                    for (int e = 0; e < 32; e += 4)
-                        *reinterpret_cast<float4*>(po + e) =
-                            make_float4(__uint_as_float(o[e]), __uint_as_float(o[e + 1]),
-                                        __uint_as_float(o[e + 2]), __uint_as_float(o[e + 3]));
+                    part_store32(p, (row * p.splits + seg) * D + c * 32, o);
                 } else {
                     __nv_bfloat16* orow = p.out + row * (int64_t)D + c * 32;
 #pragma unroll

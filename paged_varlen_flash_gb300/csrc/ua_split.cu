@@ -368,7 +368,7 @@ split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
         }
         const int64_t row_id = row_tok[r] * p.hq + row_h[r];
         if constexpr (SPLIT) {
-            p.part_o[(row_id * p.splits + seg) * D + dd] = O;
+            part_store(p, (row_id * p.splits + seg) * D + dd, O);
             if (dd == 0) {
                 p.part_ml[(row_id * p.splits + seg) * 2 + 0] = M;
                 p.part_ml[(row_id * p.splits + seg) * 2 + 1] = Lsum;
@@ -430,9 +430,9 @@ __global__ void __launch_bounds__(256) combine_kernel(const FwdParams p) {
             if (mk == -INFINITY) continue;  // empty segment: its o is never read
             const float a = fast_exp2(mk - M);
             Lsum = fmaf(a, ml[2 * k + 1], Lsum);
-            const float* po = p.part_o + (row * p.splits + k) * D + lane * DPL;
+            const int64_t po = (row * p.splits + k) * D + lane * DPL;
 #pragma unroll
-            for (int t = 0; t < DPL; ++t) o[t] = fmaf(a, po[t], o[t]);
+            for (int t = 0; t < DPL; ++t) o[t] = fmaf(a, part_load(p, po + t), o[t]);
         }
     }
     bool zero = false;

@@ -69,6 +69,7 @@ def _desc(**over):
     (dict(head_size=96), 2),
     (dict(block_size=8), 2),
     (dict(dtype=1), 2),
+    (dict(split_partials=2), 1),                    # unknown partials type
 ])
 def test_descriptor_validation_before_any_device_work(lib, over, status):
     h = ctypes.c_void_p()
