@@ -11,7 +11,8 @@ torch CPU arrays into that library.
 Parity status: every term of the definition is pinned by the closed-form and
 invariant tests in ``tests/test_oracle_pins.py`` (the e4m3 decoder of the fp8
 KV cache against PyTorch's float8_e4m3fn conversion for all 256 codes, and
-fp8 attention against the same attention on the decoded values); the one
+fp8 attention against the same attention on the decoded values; the sparse
+top-k mode against the dense definition on full and permuted lists); the one
 part left unpinned is the absolute accuracy of libm's ``tanh`` inside the
 softcap term, which is far below any tolerance used against the GPU.
 """
@@ -48,7 +49,7 @@ def _load():
             ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_double,
             ctypes.c_int32, ctypes.c_double, ctypes.c_int32, ctypes.c_void_p,
             ctypes.c_void_p, ctypes.c_int32, ctypes.c_double, ctypes.c_double,
-            ctypes.c_void_p, ctypes.c_int64]
+            ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64]
         lib.ua_oracle_forward.argtypes = common + [ctypes.c_void_p, ctypes.c_int32]
         lib.ua_oracle_forward.restype = ctypes.c_int
         lib.ua_oracle_rows.argtypes = common + [ctypes.c_void_p, ctypes.c_int64,
@@ -124,8 +125,17 @@ class _Args:
 
     def __init__(self, q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k,
                  scale, causal=True, softcap=0.0, window=0, alibi_slopes=None,
-                 sinks=None, k_scale=1.0, v_scale=1.0, qq_bias=None):
+                 sinks=None, k_scale=1.0, v_scale=1.0, qq_bias=None, topk_idx=None,
+                 topk_len=None):
         self.q = _bf16_bits(q)
+        self.topk_idx = self.topk_len = None
+        self.topk_stride = 0
+        if topk_idx is not None:
+            self.topk_idx = _i32(topk_idx)
+            assert self.topk_idx.ndim == 2
+            self.topk_stride = self.topk_idx.shape[1]
+            self.topk_len = _i32(topk_len)
+            assert self.topk_len.shape == (self.topk_idx.shape[0],)
         self.qq = _f64_or_none(qq_bias)
         if self.qq is not None:
             assert self.qq.ndim == 2
@@ -160,17 +170,22 @@ class _Args:
                 _ptr(self.cu), _ptr(self.su), self.scale, self.causal, self.softcap,
                 self.window, _ptr(self.alibi), _ptr(self.sinks), self.kv_fp8,
                 self.k_scale, self.v_scale, _ptr(self.qq),
-                self.qq.shape[1] if self.qq is not None else 0]
+                self.qq.shape[1] if self.qq is not None else 0,
+                _ptr(self.topk_idx), _ptr(self.topk_len), self.topk_stride]
 
 
 def forward(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, scale,
             causal=True, softcap=0.0, window=0, alibi_slopes=None, sinks=None,
-            nthreads=None, k_scale=1.0, v_scale=1.0, qq_bias=None):
+            nthreads=None, k_scale=1.0, v_scale=1.0, qq_bias=None, topk_idx=None,
+            topk_len=None):
     """All output rows, fp64 numpy [total_q, H_q, d].  fp8 caches are e4m3
     codes scaled by k_scale / v_scale; qq_bias [>= S_q, stride] is the
-    query-section bias shared by all sequences and heads."""
+    query-section bias shared by all sequences and heads; topk_idx
+    [total_q, K] with topk_len [total_q] gives each query token its own key
+    list (sparse top-k mode; entries outside [0, S_k) are padding)."""
     a = _Args(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, scale,
-              causal, softcap, window, alibi_slopes, sinks, k_scale, v_scale, qq_bias)
+              causal, softcap, window, alibi_slopes, sinks, k_scale, v_scale, qq_bias,
+              topk_idx, topk_len)
     out = np.zeros((a.total_q, a.hq, a.d), dtype=np.float64)
     rc = _load().ua_oracle_forward(*a.head(), _ptr(out),
                                    nthreads or default_threads())
@@ -181,10 +196,12 @@ def forward(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, scale,
 
 def rows(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, scale, row_ids,
          causal=True, softcap=0.0, window=0, alibi_slopes=None, sinks=None,
-         nthreads=None, k_scale=1.0, v_scale=1.0, qq_bias=None):
+         nthreads=None, k_scale=1.0, v_scale=1.0, qq_bias=None, topk_idx=None,
+         topk_len=None):
     """Selected output rows (row id = token * H_q + head), fp64 numpy [n, d]."""
     a = _Args(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, scale,
-              causal, softcap, window, alibi_slopes, sinks, k_scale, v_scale, qq_bias)
+              causal, softcap, window, alibi_slopes, sinks, k_scale, v_scale, qq_bias,
+              topk_idx, topk_len)
     ids = np.ascontiguousarray(np.asarray(row_ids, dtype=np.int64))
     out = np.zeros((ids.shape[0], a.d), dtype=np.float64)
     rc = _load().ua_oracle_rows(*a.head(), _ptr(ids), ids.shape[0], _ptr(out),
@@ -196,16 +213,19 @@ def rows(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, scale, row_i
 
 def row_weights(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, scale,
                 token, head, causal=True, softcap=0.0, window=0, alibi_slopes=None,
-                sinks=None, k_scale=1.0, v_scale=1.0, qq_bias=None):
-    """(weights [S_k + 1] with the sink's share last, O_i [d]) for one row."""
+                sinks=None, k_scale=1.0, v_scale=1.0, qq_bias=None, topk_idx=None,
+                topk_len=None):
+    """(weights [n + 1] with the sink's share last, O_i [d]) for one row; n is
+    S_k, or the row's top-k list length in the sparse mode."""
     a = _Args(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, scale,
-              causal, softcap, window, alibi_slopes, sinks, k_scale, v_scale, qq_bias)
+              causal, softcap, window, alibi_slopes, sinks, k_scale, v_scale, qq_bias,
+              topk_idx, topk_len)
     cu = a.cu
     s = int(np.searchsorted(cu, token, side="right") - 1)
     while s + 1 < len(cu) and cu[s + 1] <= token:
         s += 1
-    sk = int(a.su[s])
-    w = np.zeros(sk + 1, dtype=np.float64)
+    n = int(a.su[s]) if a.topk_idx is None else int(a.topk_len[token])
+    w = np.zeros(n + 1, dtype=np.float64)
     o = np.zeros(a.d, dtype=np.float64)
     rc = _load().ua_oracle_row_weights(*a.head(), int(token), int(head), _ptr(w), _ptr(o))
     if rc != 0:
@@ -218,7 +238,8 @@ def forward_workload(w, nthreads=None, row_ids=None):
     kw = dict(causal=w.causal, softcap=w.softcap, window=w.window,
               alibi_slopes=w.alibi_slopes, sinks=w.sinks, nthreads=nthreads,
               k_scale=getattr(w, "k_scale", 1.0), v_scale=getattr(w, "v_scale", 1.0),
-              qq_bias=getattr(w, "qq_bias", None))
+              qq_bias=getattr(w, "qq_bias", None), topk_idx=getattr(w, "topk_idx", None),
+              topk_len=getattr(w, "topk_len", None))
     if row_ids is None:
         return forward(w.q, w.k_cache, w.v_cache, w.block_table, w.cu_seqlens_q,
                        w.seqused_k, w.scale, **kw)

@@ -42,6 +42,15 @@
  * every sequence and head, indexed by the local query index i and the key's
  * offset j - ctx inside the chunk; keys before the chunk (j < ctx) get none.
  *
+ * Sparse top-k mode ("[Triton/Gluon] [GFX950] Sparse paged attention and
+ * Sparse MLA", the token-granular top-k gather of its sparse decode): each
+ * query token t carries its own list of key positions topk_idx[t][0 .. n_t-1]
+ * (n_t = topk_len[t]) into its sequence's paged cache, and the row attends to
+ * the listed keys instead of to all S_k of them: the sum above runs over the
+ * list entries e with j = topk_idx[t][e], every entry with the same score
+ * chain and masks as key j.  Entries outside [0, S_k) are padding (not keys).
+ * An entry listed twice counts twice (a plain sum over the list).
+ *
  * fp8 KV cache (gfx950 page, section 7.3 "fp8 KV cache (bf16-Q + fp8-KV)"):
  * the cache holds e4m3 codes with one scale per tensor, K_j = e4m3(k) * k_scale
  * and V_j = e4m3(v) * v_scale, decoded exactly (OCP 8-bit float e4m3: 1 sign,
@@ -80,6 +89,9 @@ typedef struct {
     const double *sinks;            /* [hq] or NULL */
     const double *qq_bias;          /* [>= S_q][qq_stride] or NULL */
     int64_t qq_stride;
+    const int32_t *topk_idx;        /* [total_q][topk_stride] key positions, or NULL */
+    const int32_t *topk_len;        /* [total_q] list lengths (with topk_idx) */
+    int64_t topk_stride;
 } oracle_problem;
 
 static double widen_bf16(uint16_t h)
@@ -126,6 +138,12 @@ static int validate(const oracle_problem *P)
     if (P->window < 0 || P->softcap < 0.0) return ORACLE_ERR_ARG;
     if (P->window > 0 && !P->causal) return ORACLE_ERR_ARG;
     if (P->cu_seqlens_q[0] != 0) return ORACLE_ERR_CU;
+    if (P->topk_idx) {
+        if (!P->topk_len || P->topk_stride < 1) return ORACLE_ERR_ARG;
+        const int64_t total_q = P->num_seqs > 0 ? P->cu_seqlens_q[P->num_seqs] : 0;
+        for (int64_t t = 0; t < total_q; ++t)
+            if (P->topk_len[t] < 0 || P->topk_len[t] > P->topk_stride) return ORACLE_ERR_ARG;
+    }
     for (int32_t s = 0; s < P->num_seqs; ++s) {
         int32_t sq = P->cu_seqlens_q[s + 1] - P->cu_seqlens_q[s];
         int32_t sk = P->seqused_k[s];
@@ -141,10 +159,23 @@ static int validate(const oracle_problem *P)
     return ORACLE_OK;
 }
 
+/* Number of keys row `token` ranges over: S_k, or its list length. */
+static int64_t row_keys(const oracle_problem *P, int64_t token, int32_t sk)
+{
+    return P->topk_idx ? P->topk_len[token] : sk;
+}
+
+/* Key position of the row's e-th key: e itself, or the e-th list entry. */
+static int64_t key_at(const oracle_problem *P, int64_t token, int64_t e)
+{
+    return P->topk_idx ? P->topk_idx[token * P->topk_stride + e] : e;
+}
+
 /*
- * One output row.  `x` and `w` are caller scratch of length >= S_k.
- * If `weights` is non-NULL it receives the S_k softmax weights followed by the
- * sink's weight (0 when SINKS is off); masked keys get weight 0.
+ * One output row.  `x` and `vis` are caller scratch of length >= the row's
+ * key count n (S_k, or its top-k list length).  If `weights` is non-NULL it
+ * receives the n softmax weights followed by the sink's weight (0 when SINKS
+ * is off); masked keys get weight 0.
  */
 static void one_row(const oracle_problem *P, int64_t token, int32_t h, double *out,
                     double *weights, double *x, unsigned char *vis)
@@ -159,22 +190,24 @@ static void one_row(const oracle_problem *P, int64_t token, int32_t h, double *o
     const int32_t d = P->d;
     const uint16_t *qrow = P->q + (token * P->hq + h) * (int64_t)d;
 
+    const int64_t n = row_keys(P, token, sk);
     double m = -INFINITY;
-    for (int32_t j = 0; j < sk; ++j) {
-        int visible = 1;
-        if (P->causal && (int64_t)j > i + ctx) visible = 0;
-        if (P->window > 0 && (int64_t)j < i + ctx - P->window + 1) visible = 0;
-        vis[j] = (unsigned char)visible;
-        if (!visible) { x[j] = -INFINITY; continue; }
+    for (int64_t e = 0; e < n; ++e) {
+        const int64_t j = key_at(P, token, e);
+        int visible = j >= 0 && j < sk;
+        if (P->causal && j > i + ctx) visible = 0;
+        if (P->window > 0 && j < i + ctx - P->window + 1) visible = 0;
+        vis[e] = (unsigned char)visible;
+        if (!visible) { x[e] = -INFINITY; continue; }
         int64_t blk = P->block_table[(int64_t)s * P->bt_stride + j / P->b];
         const int64_t krow = ((blk * P->b + j % P->b) * P->hk + hkv) * (int64_t)d;
         double dot = 0.0;
         for (int32_t t = 0; t < d; ++t) dot += widen_bf16(qrow[t]) * kv_elem(P, P->k, krow + t, P->k_scale);
         double xj = P->scale * dot;
         if (P->softcap > 0.0) xj = P->softcap * tanh(xj / P->softcap);
-        if (P->alibi_slopes) xj += P->alibi_slopes[h] * (double)((int64_t)j - ctx);
-        if (P->qq_bias && (int64_t)j >= ctx) xj += P->qq_bias[i * P->qq_stride + ((int64_t)j - ctx)];
-        x[j] = xj;
+        if (P->alibi_slopes) xj += P->alibi_slopes[h] * (double)(j - ctx);
+        if (P->qq_bias && j >= ctx) xj += P->qq_bias[i * P->qq_stride + (j - ctx)];
+        x[e] = xj;
         if (xj > m) m = xj;
     }
     const int have_sink = P->sinks != NULL;
@@ -183,36 +216,36 @@ static void one_row(const oracle_problem *P, int64_t token, int32_t h, double *o
 
     for (int32_t t = 0; t < d; ++t) out[t] = 0.0;
     if (weights)
-        for (int32_t j = 0; j <= sk; ++j) weights[j] = 0.0;
+        for (int64_t e = 0; e <= n; ++e) weights[e] = 0.0;
 
     if (m == INFINITY) {
         /* A +inf sink takes all of the probability mass and has no value row. */
-        if (weights) weights[sk] = 1.0;
+        if (weights) weights[n] = 1.0;
         return;
     }
     if (m == -INFINITY) return; /* nothing visible, no sink: den = 0, O = 0 */
 
     double den = 0.0;
-    for (int32_t j = 0; j < sk; ++j) {
-        if (!vis[j]) continue;
-        double e = exp(x[j] - m);
-        x[j] = e;
-        den += e;
+    for (int64_t e = 0; e < n; ++e) {
+        if (!vis[e]) continue;
+        x[e] = exp(x[e] - m);
+        den += x[e];
     }
     double e_sink = have_sink ? exp(sink - m) : 0.0;
     den += e_sink;
     if (!(den > 0.0)) return;
 
-    for (int32_t j = 0; j < sk; ++j) {
-        if (!vis[j]) continue;
+    for (int64_t e = 0; e < n; ++e) {
+        if (!vis[e]) continue;
+        const int64_t j = key_at(P, token, e);
         int64_t blk = P->block_table[(int64_t)s * P->bt_stride + j / P->b];
         const int64_t vrow = ((blk * P->b + j % P->b) * P->hk + hkv) * (int64_t)d;
-        double wgt = x[j];
+        double wgt = x[e];
         for (int32_t t = 0; t < d; ++t) out[t] += wgt * kv_elem(P, P->v, vrow + t, P->v_scale);
-        if (weights) weights[j] = x[j] / den;
+        if (weights) weights[e] = x[e] / den;
     }
     for (int32_t t = 0; t < d; ++t) out[t] /= den;
-    if (weights) weights[sk] = e_sink / den;
+    if (weights) weights[n] = e_sink / den;
 }
 
 typedef struct {
@@ -267,6 +300,10 @@ static int run_rows(const oracle_problem *P, const int64_t *rows, int64_t n_rows
     int32_t max_sk = 0;
     for (int32_t s = 0; s < P->num_seqs; ++s)
         if (P->seqused_k[s] > max_sk) max_sk = P->seqused_k[s];
+    if (P->topk_idx && P->topk_stride > max_sk) {
+        if (P->topk_stride > INT32_MAX - 1) return ORACLE_ERR_ARG;
+        max_sk = (int32_t)P->topk_stride;
+    }
 
     job_t J;
     J.P = P; J.rows = rows; J.n_rows = n_rows; J.out = out; J.max_sk = max_sk;
@@ -294,7 +331,9 @@ static int run_rows(const oracle_problem *P, const int64_t *rows, int64_t n_rows
  * seqused_k [num_seqs]; softcap <= 0 and window <= 0 switch those terms off;
  * alibi_slopes / sinks may be NULL; kv_fp8 != 0 reads the caches as e4m3
  * codes scaled by k_scale / v_scale; qq_bias (or NULL) is the query-section
- * bias, row i at qq_bias + i * qq_stride.  Output is fp64.
+ * bias, row i at qq_bias + i * qq_stride; topk_idx (or NULL) switches to the
+ * sparse top-k mode: token t's list at topk_idx + t * topk_stride, of
+ * topk_len[t] <= topk_stride entries.  Output is fp64.
  * ------------------------------------------------------------------------- */
 
 #define FILL_PROBLEM()                                                        \
@@ -308,7 +347,8 @@ static int run_rows(const oracle_problem *P, const int64_t *rows, int64_t n_rows
     P.window = window > 0 ? window : 0;                                       \
     P.alibi_slopes = alibi_slopes; P.sinks = sinks;                           \
     P.kv_fp8 = kv_fp8 ? 1 : 0; P.k_scale = k_scale; P.v_scale = v_scale;      \
-    P.qq_bias = qq_bias; P.qq_stride = qq_stride;
+    P.qq_bias = qq_bias; P.qq_stride = qq_stride;                             \
+    P.topk_idx = topk_idx; P.topk_len = topk_len; P.topk_stride = topk_stride;
 
 #define PROBLEM_ARGS                                                          \
     int32_t num_seqs, int32_t hq, int32_t hk, int32_t d, int32_t b,          \
@@ -317,7 +357,8 @@ static int run_rows(const oracle_problem *P, const int64_t *rows, int64_t n_rows
     const int32_t *cu_seqlens_q, const int32_t *seqused_k, double scale,     \
     int32_t causal, double softcap, int32_t window,                          \
     const double *alibi_slopes, const double *sinks, int32_t kv_fp8,         \
-    double k_scale, double v_scale, const double *qq_bias, int64_t qq_stride
+    double k_scale, double v_scale, const double *qq_bias, int64_t qq_stride,   \
+    const int32_t *topk_idx, const int32_t *topk_len, int64_t topk_stride
 
 /* Every output row: out [total_q, hq, d]. */
 int ua_oracle_forward(PROBLEM_ARGS, double *out, int32_t nthreads)
@@ -340,8 +381,9 @@ int ua_oracle_rows(PROBLEM_ARGS, const int64_t *rows, int64_t n_rows, double *ou
 }
 
 /*
- * Softmax weights of one row: weights [seqused_k[s] + 1], the last entry being
- * the sink's share (0 when SINKS is off).  out_row [d] receives O_i.
+ * Softmax weights of one row: weights [n + 1] for its n keys (S_k, or its
+ * top-k list length), the last entry being the sink's share (0 when SINKS is
+ * off).  out_row [d] receives O_i.
  */
 int ua_oracle_row_weights(PROBLEM_ARGS, int64_t token, int32_t head, double *weights,
                           double *out_row)
@@ -353,8 +395,9 @@ int ua_oracle_row_weights(PROBLEM_ARGS, int64_t token, int32_t head, double *wei
     int64_t total_q = num_seqs > 0 ? cu_seqlens_q[num_seqs] : 0;
     if (token < 0 || token >= total_q || head < 0 || head >= hq) return ORACLE_ERR_ARG;
     int32_t sk = seqused_k[owner_seq(&P, token)];
-    double *x = (double *)malloc(sizeof(double) * (size_t)(sk + 1));
-    unsigned char *vis = (unsigned char *)malloc((size_t)sk + 1);
+    const int64_t n = row_keys(&P, token, sk);
+    double *x = (double *)malloc(sizeof(double) * (size_t)(n + 1));
+    unsigned char *vis = (unsigned char *)malloc((size_t)n + 1);
     if (!x || !vis) { free(x); free(vis); return ORACLE_ERR_NOMEM; }
     one_row(&P, token, head, out_row, weights, x, vis);
     free(x); free(vis);

@@ -22,6 +22,11 @@ Named workloads (the sizes of the five benchmark configurations):
                       h = 1..32.
 * ``decode_fp8``      the ``decode`` lengths and tables with an fp8 e4m3 K/V cache
                       (one scale per tensor, 1/32; codes of N(0,1) / scale).
+* ``decode_topk``     sparse top-k decode: 256 sequences, S_q = 1,
+                      S_k ~ U{4096..16384}, H_q/H_k = 16/1, d = 128, b = 64,
+                      pool 48,000 blocks, causal; each query token attends to
+                      its own list of 2048 distinct key positions drawn
+                      uniformly from its context (random order).
 
 Lengths and block tables come from a CPU ``torch.Generator`` seeded with
 ``1000 + config index`` and are therefore identical on every device; the bf16
@@ -46,7 +51,7 @@ import torch
 CONFIG_NAMES = ["tiny", "decode", "chunked", "long_prefill", "wide_mha_alibi"]
 _CONFIG_INDEX = {
     "tiny": 0, "decode": 1, "chunked": 2, "long_prefill": 3,
-    "long_prefill_shuffled": 3, "wide_mha_alibi": 4, "decode_fp8": 1,
+    "long_prefill_shuffled": 3, "wide_mha_alibi": 4, "decode_fp8": 1, "decode_topk": 5,
 }
 
 
@@ -77,6 +82,8 @@ class Workload:
     k_scale: float = 1.0              # K = e4m3(k) * k_scale when kv_fp8
     v_scale: float = 1.0
     qq_bias: Optional[torch.Tensor] = None   # fp32 [max S_q, max S_q] query-section bias
+    topk_idx: Optional[torch.Tensor] = None  # int32 [total_q, K] key positions per query token
+    topk_len: Optional[torch.Tensor] = None  # int32 [total_q] list lengths
 
     @property
     def num_seqs(self) -> int:
@@ -111,7 +118,7 @@ class Workload:
             mv(self.v_cache), mv(self.block_table), mv(self.cu_seqlens_q),
             mv(self.seqused_k), self.scale, self.causal, self.softcap, self.window,
             mv(self.sinks), mv(self.alibi_slopes), dict(self.meta), self.kv_fp8,
-            self.k_scale, self.v_scale, mv(self.qq_bias))
+            self.k_scale, self.v_scale, mv(self.qq_bias), mv(self.topk_idx), mv(self.topk_len))
 
     # -- counts used for reporting (no attention arithmetic) ------------------
     def visible_pairs(self) -> int:
@@ -127,8 +134,48 @@ class Workload:
         return total
 
     def kv_bytes_read(self) -> int:
-        """K and V bytes of the used keys, counted once per (sequence, kv head)."""
-        return int(sum(self.seqlens_k)) * self.hk * self.d * (1 if self.kv_fp8 else 2) * 2
+        """K and V bytes of the used keys, counted once per (sequence, kv head);
+        with top-k lists, once per listed key of each query token."""
+        keys = int(sum(self.seqlens_k))
+        if self.topk_len is not None:
+            keys = int(self.topk_len.to(torch.int64).sum())
+        return keys * self.hk * self.d * (1 if self.kv_fp8 else 2) * 2
+
+
+def topk_lists(seqlens_q, seqlens_k, k: int, seed: int, *, causal: bool = True,
+               ragged: bool = False, junk: float = 0.0):
+    """Per query token, up to ``k`` distinct key positions drawn uniformly
+    (random order) from the keys it may see: [0, i + ctx] when causal, else
+    [0, S_k).  ``ragged`` draws each list's length uniformly in [0, k] (capped
+    by the keys available).  ``junk`` replaces that fraction of the entries by
+    positions that are not keys of the row: -1, S_k or beyond, and (causal)
+    keys past i + ctx.  Unused list slots hold -1.  Returns int32
+    ([total_q, k] positions, [total_q] lengths), CPU."""
+    g = _gen(seed)
+    rows, lens = [], []
+    for sq, sk in zip(seqlens_q, seqlens_k):
+        ctx = sk - sq
+        for i in range(sq):
+            avail = (i + ctx + 1) if causal else sk
+            n = min(k, avail)
+            if ragged:
+                n = min(n, int(torch.randint(0, k + 1, (1,), generator=g)))
+            row = torch.full((k,), -1, dtype=torch.int32)
+            pos = torch.randperm(avail, generator=g)[:n].to(torch.int32)
+            if junk > 0 and n > 0:
+                bad = torch.rand(n, generator=g) < junk
+                kind = torch.randint(0, 3, (n,), generator=g)
+                # kind 2: the first key the causal mask hides, else S_k itself
+                hidden = i + ctx + 1 if causal and i + ctx + 1 < sk else sk
+                alt = torch.where(kind == 0, torch.full_like(pos, -1),
+                                  torch.where(kind == 1, torch.full_like(pos, sk + 3),
+                                              torch.full_like(pos, hidden)))
+                pos = torch.where(bad, alt, pos)
+            row[:n] = pos
+            rows.append(row)
+            lens.append(n)
+    idx = torch.stack(rows) if rows else torch.zeros((0, k), dtype=torch.int32)
+    return idx, torch.tensor(lens, dtype=torch.int32)
 
 
 def _gen(seed: int) -> torch.Generator:
@@ -269,24 +316,37 @@ def make(name: str, device="cpu", poison: bool = False, values: bool = True) -> 
     if name == "wide_mha_alibi":
         return build(name, 32, 32, 256, 64, [4096] * 8, [4096] * 8, 512,
                      1.0 / math.sqrt(256), std=0.5, alibi=True, **common)
+    if name == "decode_topk":
+        sk = _randint(g, 4096, 16384, 256)
+        w = build(name, 16, 1, 128, 64, [1] * 256, sk, 48000, 1.0 / math.sqrt(128), **common)
+        idx, lens = topk_lists(w.seqlens_q, w.seqlens_k, 2048, seed + 1)
+        w.topk_idx, w.topk_len = idx.to(w.q.device), lens.to(w.q.device)
+        return w
     raise KeyError(name)
 
 
 def random_small(seed: int, *, num_seqs=3, hq=8, hk=2, d=64, b=16, sq=(1, 40),
                  ctx=(0, 70), causal=True, softcap=0.0, window=0, sinks=False,
                  alibi=False, device="cpu", poison=True, spare_blocks=5,
-                 std=1.0, kv_fp8=False, kv_scale=1.0 / 32, qq_bias=False) -> Workload:
-    """A small seeded ragged batch for parity sweeps (lengths drawn per seq)."""
+                 std=1.0, kv_fp8=False, kv_scale=1.0 / 32, qq_bias=False, topk=0,
+                 topk_ragged=False, topk_junk=0.0) -> Workload:
+    """A small seeded ragged batch for parity sweeps (lengths drawn per seq);
+    ``topk`` > 0 attaches per-token key lists of that capacity (``topk_lists``)."""
     g = _gen(seed)
     seqlens_q = _randint(g, sq[0], sq[1], num_seqs)
     ctxs = _randint(g, ctx[0], ctx[1], num_seqs)
     seqlens_k = [q + c for q, c in zip(seqlens_q, ctxs)]
     need = sum((k + b - 1) // b for k in seqlens_k)
-    return build("random_small", hq, hk, d, b, seqlens_q, seqlens_k,
-                 need + spare_blocks, 1.0 / math.sqrt(d), seed=seed, device=device,
-                 std=std, causal=causal, softcap=softcap, window=window, sinks=sinks,
-                 alibi=alibi, poison=poison, bt_pad=1, kv_fp8=kv_fp8, kv_scale=kv_scale,
-                 qq_bias=qq_bias)
+    w = build("random_small", hq, hk, d, b, seqlens_q, seqlens_k,
+              need + spare_blocks, 1.0 / math.sqrt(d), seed=seed, device=device,
+              std=std, causal=causal, softcap=softcap, window=window, sinks=sinks,
+              alibi=alibi, poison=poison, bt_pad=1, kv_fp8=kv_fp8, kv_scale=kv_scale,
+              qq_bias=qq_bias)
+    if topk:
+        idx, lens = topk_lists(seqlens_q, seqlens_k, topk, seed + 7919, causal=causal,
+                               ragged=topk_ragged, junk=topk_junk)
+        w.topk_idx, w.topk_len = idx.to(w.q.device), lens.to(w.q.device)
+    return w
 
 
 def sample_rows(w: Workload, n: int, seed: int = 0) -> torch.Tensor:

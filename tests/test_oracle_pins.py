@@ -534,3 +534,134 @@ def test_qq_bias_zero_is_no_bias_and_it_is_added_after_softcap():
     manual[ctx:] *= math.exp(2.0)
     manual /= manual.sum()
     np.testing.assert_allclose(wtb[:-1], manual, rtol=1e-12, atol=1e-15)
+
+
+# ---------------------------------------------------------------------------
+# Sparse top-k mode ("[Triton/Gluon] [GFX950] Sparse paged attention and Sparse
+# MLA": each query token attends to its own list of key positions).
+# ---------------------------------------------------------------------------
+
+def _full_lists(w, permute_seed=None):
+    """Every key of each token's sequence, in order (or permuted per token)."""
+    kmax = max(w.seqlens_k)
+    rows, lens = [], []
+    g = torch.Generator().manual_seed(permute_seed or 0)
+    for s, i, ctx in token_of_row(w):
+        sk = w.seqlens_k[s]
+        pos = torch.arange(sk, dtype=torch.int32)
+        if permute_seed is not None:
+            pos = pos[torch.randperm(sk, generator=g)]
+        row = torch.full((kmax,), -1, dtype=torch.int32)
+        row[:sk] = pos
+        rows.append(row)
+        lens.append(sk)
+    return torch.stack(rows), torch.tensor(lens, dtype=torch.int32)
+
+
+@pytest.mark.parametrize("flags", [{}, dict(softcap=5.0, alibi=True, sinks=True, window=13),
+                                   dict(causal=False, qq_bias=True), dict(sinks=True, qq_bias=True)])
+def test_topk_list_of_every_key_in_order_is_the_dense_definition(flags):
+    """A list holding keys 0 .. S_k-1 in order takes exactly the dense row's
+    sum in the dense row's order: identical outputs, so the list mode applies
+    the same score chain and masks with j = the listed position."""
+    w = _flagged_random(60, **flags)
+    qq = {"qq_bias": w.qq_bias} if w.qq_bias is not None else {}
+    idx, lens = _full_lists(w)
+    assert np.array_equal(_run(w, topk_idx=idx, topk_len=lens, **qq), _run(w, **qq))
+
+
+def test_topk_list_order_does_not_matter():
+    """A per-token permutation of the full list changes only the summation
+    order: catches a weight or value taken from the entry index instead of the
+    listed position."""
+    w = _flagged_random(61, softcap=5.0, alibi=True, sinks=True)
+    idx, lens = _full_lists(w, permute_seed=62)
+    got = _run(w, topk_idx=idx, topk_len=lens)
+    assert np.max(np.abs(got - _run(w))) < 1e-12
+
+
+def test_topk_closed_form_on_constant_keys_with_padding_and_duplicates():
+    """Constant keys: O = mean of the position tags over the list entries that
+    are keys of the row (0 <= j < S_k and j <= i + ctx), counted as listed; -1,
+    S_k and causally hidden entries drop out; an empty list gives O = 0."""
+    sq, sk = [3, 1, 5], [40, 17, 12]
+    w = _constant_key_workload(sq, sk, seed=63)
+    g = torch.Generator().manual_seed(64)
+    K = 24
+    rows, lens = [], []
+    for s, i, ctx in token_of_row(w):
+        hi = i + ctx
+        n = int(torch.randint(0, K + 1, (1,), generator=g))
+        ent = torch.randint(-2, sk[s] + 3, (n,), generator=g).to(torch.int32)
+        if n >= 2:
+            ent[1] = ent[0]                       # one duplicate
+        if n >= 3:
+            ent[2] = min(hi + 1, sk[s])           # hidden by the causal mask or past S_k
+        row = torch.full((K,), -1, dtype=torch.int32)
+        row[:n] = ent
+        rows.append(row)
+        lens.append(n)
+    idx, lens_t = torch.stack(rows), torch.tensor(lens, dtype=torch.int32)
+    idx[0, :] = -1                                # token 0: an empty list ...
+    lens_t[0] = K                                 # ... of K padding entries
+    out = _run(w, topk_idx=idx, topk_len=lens_t)
+    for tok, (s, i, ctx) in enumerate(token_of_row(w)):
+        ent = idx[tok, :int(lens_t[tok])].numpy().astype(np.int64)
+        keep = ent[(ent >= 0) & (ent < sk[s]) & (ent <= i + ctx)]
+        for h in range(w.hq):
+            if keep.size == 0:
+                assert np.all(out[tok, h] == 0)
+                continue
+            tags = tag_values(keep, h // w.g)
+            for k in range(4):
+                assert abs(out[tok, h, k] - np.mean(tags[k])) < 1e-12
+
+
+def test_topk_single_entry_returns_that_value_row_and_window_list_equals_window():
+    """One listed key -> O = its V row; the list [i+ctx-W+1 .. i+ctx] equals
+    the dense call with window W (same key set)."""
+    sq, sk = [4, 2], [30, 9]
+    w = _blank(sq, sk, seed=65)
+    _random_kv(w, 66)
+    W_ = 6
+    one, win, lens1, lensw = [], [], [], []
+    for s, i, ctx in token_of_row(w):
+        j = (7 * i + 3) % (i + ctx + 1)
+        r1 = torch.full((W_,), -1, dtype=torch.int32)
+        r1[0] = j
+        one.append(r1)
+        lens1.append(1)
+        lo = max(0, i + ctx - W_ + 1)
+        rw = torch.full((W_,), -1, dtype=torch.int32)
+        rw[:i + ctx - lo + 1] = torch.arange(lo, i + ctx + 1, dtype=torch.int32)
+        win.append(rw)
+        lensw.append(i + ctx - lo + 1)
+    out1 = _run(w, topk_idx=torch.stack(one), topk_len=torch.tensor(lens1, dtype=torch.int32))
+    for tok, (s, i, ctx) in enumerate(token_of_row(w)):
+        j = (7 * i + 3) % (i + ctx + 1)
+        for h in range(w.hq):
+            assert decode_tag(out1[tok, h]) == (j, h // w.g)
+    outw = _run(w, topk_idx=torch.stack(win), topk_len=torch.tensor(lensw, dtype=torch.int32))
+    assert np.max(np.abs(outw - _run(w, window=W_))) < 1e-12
+
+
+def test_topk_weights_follow_the_list():
+    w = _flagged_random(67, sinks=True)
+    idx, lens = W.topk_lists(w.seqlens_q, w.seqlens_k, 12, 68, ragged=True, junk=0.3)
+    got = _run(w, topk_idx=idx, topk_len=lens)
+    for tok in range(0, w.total_q, 5):
+        wt, o = oracle.row_weights(w.q, w.k_cache, w.v_cache, w.block_table, w.cu_seqlens_q,
+                                   w.seqused_k, w.scale, tok, 2, sinks=w.sinks,
+                                   topk_idx=idx, topk_len=lens)
+        n = int(lens[tok])
+        assert wt.shape == (n + 1,)
+        assert abs(wt.sum() - 1.0) < 1e-12
+        assert np.max(np.abs(o - got[tok, 2])) < 1e-12
+
+
+def test_topk_rejects_a_list_longer_than_its_capacity():
+    w = _flagged_random(69)
+    idx, lens = W.topk_lists(w.seqlens_q, w.seqlens_k, 8, 70)
+    lens[1] = 9
+    with pytest.raises(oracle.OracleError):
+        _run(w, topk_idx=idx, topk_len=lens)
