@@ -179,6 +179,37 @@ ua_status ua_forward(ua_problem *p, const void *q, const void *k_cache, const vo
                      void *stream);
 
 /*
+ * ua_forward_topk -- sparse top-k decode ("[Triton/Gluon] [GFX950] Sparse
+ * paged attention and Sparse MLA", its token-granular top-k gather): each
+ * query token t attends to its own list of key positions instead of to all
+ * S_k keys of its sequence,
+ *
+ *     O_(t,h) = sum_e softmax(x)_e V_(j_e),  j_e = topk_idx[t][e], e < topk_len[t],
+ *
+ * where x_e is the score chain above evaluated for key j_e (the masks, ALiBi
+ * and QQ-bias use the listed position j_e).  Entries outside [0, S_k) are
+ * padding (-1 by convention) and are not keys; an entry listed twice counts
+ * twice.  Same arguments as ua_forward plus:
+ *   topk_idx     int32 [total_q, topk_stride] device, the lists (row t = token t)
+ *   topk_len     int32 [total_q] device, list lengths in [0, topk_stride];
+ *                a length outside it sets UA_DEVERR_BOUNDS and writes the
+ *                token's rows as 0
+ *   topk_stride  > 0, entries per list row
+ * A listed key in a block whose id is out of range is dropped and sets
+ * UA_DEVERR_BLOCK_ID.  Needs d = 128, 16 % g == 0, a bf16 cache, path AUTO
+ * or DECODE_TC and num_blocks * b * H_k < 2^31 (else UA_ERR_UNSUPPORTED).
+ * The lists are split into segments of 128-entry tiles per token (one CTA
+ * each, merged by the combine kernel), counted from each token's own length.
+ */
+ua_status ua_forward_topk(ua_problem *p, const void *q, const void *k_cache, const void *v_cache,
+                          const int32_t *block_table, const int32_t *cu_seqlens_q,
+                          const int32_t *seqused_k, int32_t num_seqs, int64_t total_q,
+                          int32_t max_seqlen_q, int32_t max_seqlen_k, const int32_t *topk_idx,
+                          const int32_t *topk_len, int32_t topk_stride, uint32_t flags,
+                          const float *sinks, const float *alibi_slopes, void *out,
+                          void *stream);
+
+/*
  * Same computation with the per-step inputs and the output in HOST memory:
  * q_host, block_table_host, cu_seqlens_q_host, seqused_k_host, sinks_host and
  * alibi_host are copied to problem-owned device staging buffers (allocated on

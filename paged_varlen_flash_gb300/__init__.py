@@ -16,5 +16,6 @@ from .binding import (  # noqa: F401
     UA_DTYPE_BF16, UA_DTYPE_FP8_E4M3, UA_PARTIALS_F32, UA_PARTIALS_BF16,
     UAError, Problem, flags_of, lib_path, load_library,
     ua_check_device_error, ua_destroy, ua_forward, ua_forward_host, ua_forward_noalloc,
+    ua_forward_topk,
     ua_problem_create, ua_set_qq_bias,
     ua_status_string)

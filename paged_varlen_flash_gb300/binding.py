@@ -98,6 +98,9 @@ def load_library():
     lib.ua_last_launch_count.restype = i32
     lib.ua_last_path.argtypes = [vp]
     lib.ua_last_path.restype = ctypes.c_char_p
+    lib.ua_forward_topk.argtypes = [vp] * 7 + [i32, ctypes.c_int64, i32, i32, vp, vp, i32,
+                                               ctypes.c_uint32, vp, vp, vp, vp]
+    lib.ua_forward_topk.restype = ctypes.c_int
     lib.ua_set_qq_bias.argtypes = [vp, vp, ctypes.c_int64, ctypes.c_int64]
     lib.ua_set_qq_bias.restype = ctypes.c_int
     lib.ua_set_profile_events.argtypes = [vp, vp, vp]
@@ -175,6 +178,18 @@ def ua_forward(problem, q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_
         problem, _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
         _ptr(cu_seqlens_q), _ptr(seqused_k), num_seqs, total_q, max_seqlen_q,
         max_seqlen_k, flags, _ptr(sinks), _ptr(alibi_slopes), _ptr(out), _stream(stream))
+
+
+def ua_forward_topk(problem, q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k,
+                    num_seqs, total_q, max_seqlen_q, max_seqlen_k, topk_idx, topk_len,
+                    topk_stride, flags, sinks, alibi_slopes, out, stream=None):
+    """Enqueue a sparse top-k forward (device tensors; topk_idx int32
+    [total_q, topk_stride], topk_len int32 [total_q]).  Returns the status."""
+    return load_library().ua_forward_topk(
+        problem, _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+        _ptr(cu_seqlens_q), _ptr(seqused_k), num_seqs, total_q, max_seqlen_q,
+        max_seqlen_k, _ptr(topk_idx), _ptr(topk_len), topk_stride, flags, _ptr(sinks),
+        _ptr(alibi_slopes), _ptr(out), _stream(stream))
 
 
 def ua_forward_host(problem, q_host, k_cache, v_cache, block_table_host, cu_seqlens_q_host,
@@ -267,13 +282,35 @@ class Problem:
             raise UAError(st, "ua_forward")
         return out
 
+    def forward_topk(self, q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k,
+                     num_seqs, total_q, max_seqlen_q, max_seqlen_k, topk_idx, topk_len, flags,
+                     sinks=None, alibi_slopes=None, out=None, stream=None):
+        if out is None:
+            import torch
+            out = torch.empty_like(q)
+        if topk_idx.dim() != 2 or topk_idx.stride(1) != 1:
+            raise ValueError("topk_idx must be [total_q, K] with unit inner stride")
+        st = ua_forward_topk(self.handle, q, k_cache, v_cache, block_table, cu_seqlens_q,
+                             seqused_k, num_seqs, total_q, max_seqlen_q, max_seqlen_k, topk_idx,
+                             topk_len, topk_idx.stride(0), flags, sinks, alibi_slopes, out,
+                             stream)
+        if st != UA_OK:
+            raise UAError(st, "ua_forward_topk")
+        return out
+
     def forward_workload(self, w, out=None, stream=None):
-        """Forward on a device-resident ``workloads.Workload``."""
+        """Forward on a device-resident ``workloads.Workload`` (through
+        ``ua_forward_topk`` when it carries top-k lists)."""
         qq = getattr(w, "qq_bias", None)
         flags = flags_of(w.causal, w.softcap, w.alibi_slopes is not None, w.window,
                          w.sinks is not None, qq is not None)
         if qq is not None:
             self.set_qq_bias(qq)
+        if getattr(w, "topk_idx", None) is not None:
+            return self.forward_topk(w.q, w.k_cache, w.v_cache, w.block_table, w.cu_seqlens_q,
+                                     w.seqused_k, w.num_seqs, w.total_q, w.max_seqlen_q,
+                                     w.max_seqlen_k, w.topk_idx, w.topk_len, flags, w.sinks,
+                                     w.alibi_slopes, out, stream)
         return self.forward(w.q, w.k_cache, w.v_cache, w.block_table, w.cu_seqlens_q,
                             w.seqused_k, w.num_seqs, w.total_q, w.max_seqlen_q,
                             w.max_seqlen_k, flags, w.sinks, w.alibi_slopes, out, stream)

@@ -16,6 +16,7 @@
 #include "ua_decode_tc.h"
 #include "ua_prefill.h"
 #include "ua_split.h"
+#include "ua_topk.h"
 
 namespace {
 
@@ -97,6 +98,9 @@ struct ua_problem {
     CUtensorMap map_k16, map_v16;       // 16-slot boxes (split path)
     CUtensorMap map_kp, map_vp;         // prefill-path boxes
     int map_p_rows = 0;
+    const void* map_g_k_ptr = nullptr;  // row-gather views of the caches (top-k calls)
+    const void* map_g_v_ptr = nullptr;
+    CUtensorMap map_kg, map_vg;
     int last_launches = 0;
     const char* last_path = "none";
     cudaEvent_t prof_begin = nullptr;
@@ -231,11 +235,19 @@ ua_status ua_set_profile_events(ua_problem* p, void* ev_begin, void* ev_end) {
     return UA_OK;
 }
 
-ua_status ua_forward(ua_problem* p, const void* q, const void* k_cache, const void* v_cache,
-                     const int32_t* block_table, const int32_t* cu_seqlens_q,
-                     const int32_t* seqused_k, int32_t num_seqs, int64_t total_q,
-                     int32_t max_seqlen_q, int32_t max_seqlen_k, uint32_t flags,
-                     const float* sinks, const float* alibi_slopes, void* out, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Host checks shared by the forward entry points, then the kernel parameters.
+// Returns UA_OK with *skip set when the call has nothing to compute.
+ua_status prepare_call(ua_problem* p, const void* q, const void* k_cache, const void* v_cache,
+                       const int32_t* block_table, const int32_t* cu_seqlens_q,
+                       const int32_t* seqused_k, int32_t num_seqs, int64_t total_q,
+                       int32_t max_seqlen_q, int32_t max_seqlen_k, uint32_t flags,
+                       const float* sinks, const float* alibi_slopes, void* out,
+                       ua::FwdParams* fpp, bool* skip) {
+    *skip = false;
     if (!p) return UA_ERR_INVALID_ARG;
     p->last_launches = 0;
     p->last_path = "none";
@@ -251,7 +263,10 @@ ua_status ua_forward(ua_problem* p, const void* q, const void* k_cache, const vo
     if (((flags & UA_FLAG_ALIBI) != 0) != (alibi_slopes != nullptr)) return UA_ERR_INVALID_ARG;
     if ((flags & UA_FLAG_QQ_BIAS) && (!p->qq_bias || (int64_t)max_seqlen_q > p->qq_n))
         return UA_ERR_INVALID_ARG;
-    if (num_seqs == 0 || total_q == 0) return UA_OK;
+    if (num_seqs == 0 || total_q == 0) {
+        *skip = true;
+        return UA_OK;
+    }
     if (!q || !k_cache || !v_cache || !block_table || !cu_seqlens_q || !seqused_k || !out)
         return UA_ERR_INVALID_ARG;
     auto misaligned = [](const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) != 0; };
@@ -263,10 +278,7 @@ ua_status ua_forward(ua_problem* p, const void* q, const void* k_cache, const vo
         if (max_seqlen_q > 1) return UA_ERR_INVALID_ARG;
     }
 
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    const int g = d.num_q_heads / d.num_kv_heads;
-
-    ua::FwdParams fp;
+    ua::FwdParams& fp = *fpp;
     std::memset(&fp, 0, sizeof fp);
     fp.q = static_cast<const __nv_bfloat16*>(q);
     fp.block_table = block_table;
@@ -284,7 +296,7 @@ ua_status ua_forward(ua_problem* p, const void* q, const void* k_cache, const vo
     fp.max_seqlen_k = max_seqlen_k;
     fp.hq = d.num_q_heads;
     fp.hk = d.num_kv_heads;
-    fp.g = g;
+    fp.g = d.num_q_heads / d.num_kv_heads;
     fp.d = d.head_size;
     fp.b = d.block_size;
     fp.flags = flags;
@@ -299,6 +311,28 @@ ua_status ua_forward(ua_problem* p, const void* q, const void* k_cache, const vo
         fp.qq_bias = p->qq_bias;
         fp.qq_stride = p->qq_stride;
     }
+    return UA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+ua_status ua_forward(ua_problem* p, const void* q, const void* k_cache, const void* v_cache,
+                     const int32_t* block_table, const int32_t* cu_seqlens_q,
+                     const int32_t* seqused_k, int32_t num_seqs, int64_t total_q,
+                     int32_t max_seqlen_q, int32_t max_seqlen_k, uint32_t flags,
+                     const float* sinks, const float* alibi_slopes, void* out, void* stream) {
+    ua::FwdParams fp;
+    bool skip = false;
+    ua_status rs = prepare_call(p, q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k,
+                                num_seqs, total_q, max_seqlen_q, max_seqlen_k, flags, sinks,
+                                alibi_slopes, out, &fp, &skip);
+    if (rs != UA_OK || skip) return rs;
+    const ua_problem_desc& d = p->desc;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const int g = fp.g;
+    max_seqlen_k = fp.max_seqlen_k;
 
     if (k_cache != p->map_k_ptr || v_cache != p->map_v_ptr) {
         if (!encode_cache_map(&p->map_k16, k_cache, d, 16) ||
@@ -440,6 +474,70 @@ ua_status ua_forward(ua_problem* p, const void* q, const void* k_cache, const vo
     } else {
         p->last_path = "split_kv_direct";
     }
+    return UA_OK;
+}
+
+ua_status ua_forward_topk(ua_problem* p, const void* q, const void* k_cache, const void* v_cache,
+                          const int32_t* block_table, const int32_t* cu_seqlens_q,
+                          const int32_t* seqused_k, int32_t num_seqs, int64_t total_q,
+                          int32_t max_seqlen_q, int32_t max_seqlen_k, const int32_t* topk_idx,
+                          const int32_t* topk_len, int32_t topk_stride, uint32_t flags,
+                          const float* sinks, const float* alibi_slopes, void* out, void* stream) {
+    ua::FwdParams fp;
+    bool skip = false;
+    ua_status rs = prepare_call(p, q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k,
+                                num_seqs, total_q, max_seqlen_q, max_seqlen_k, flags, sinks,
+                                alibi_slopes, out, &fp, &skip);
+    if (rs != UA_OK) return rs;
+    if (topk_stride < 1) return UA_ERR_INVALID_ARG;
+    if (skip) return UA_OK;
+    if (!topk_idx || !topk_len) return UA_ERR_INVALID_ARG;
+    const ua_problem_desc& d = p->desc;
+    if (d.kv_dtype != UA_DTYPE_BF16) return UA_ERR_UNSUPPORTED;
+    if (d.path != UA_PATH_AUTO && d.path != UA_PATH_DECODE_TC) return UA_ERR_UNSUPPORTED;
+    fp.topk_idx = topk_idx;
+    fp.topk_len = topk_len;
+    fp.topk_stride = topk_stride;
+    if (!ua::topk_shape_ok(fp)) return UA_ERR_UNSUPPORTED;
+    if (k_cache != p->map_g_k_ptr || v_cache != p->map_g_v_ptr) {
+        if (!ua::encode_gather_map(&p->map_kg, k_cache, d.num_blocks, d.block_size, d.num_kv_heads,
+                                   d.head_size) ||
+            !ua::encode_gather_map(&p->map_vg, v_cache, d.num_blocks, d.block_size, d.num_kv_heads,
+                                   d.head_size)) {
+            p->map_g_k_ptr = p->map_g_v_ptr = nullptr;
+            // Either the cache's rows overflow the gather's 32-bit row index
+            // or the encoder failed.
+            if ((int64_t)d.num_blocks * d.block_size * d.num_kv_heads > 0x7fffffffLL)
+                return UA_ERR_UNSUPPORTED;
+            std::snprintf(g_cuda_err, sizeof g_cuda_err, "cuTensorMapEncodeTiled failed");
+            return UA_ERR_CUDA;
+        }
+        p->map_g_k_ptr = k_cache;
+        p->map_g_v_ptr = v_cache;
+    }
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    ua::TopkPlan plan;
+    ua::plan_topk(fp, p->num_sms, p->ws_bytes, &plan);
+    fp.splits = plan.splits;
+    fp.chunk = plan.chunk;
+    fp.part_o = p->d_ws;
+    fp.part_ml = p->d_ws + (size_t)total_q * d.num_q_heads * plan.splits * d.head_size;
+    prof_mark(p, true, st);
+    cudaError_t e = ua::launch_topk(plan, p->map_kg, p->map_vg, fp, st);
+    prof_mark(p, false, st);
+    if (e != cudaSuccess) {
+        note_cuda(e, "top-k kernel launch");
+        return UA_ERR_CUDA;
+    }
+    if (plan.splits > 1) {
+        e = ua::launch_combine(fp, st);
+        if (e != cudaSuccess) {
+            note_cuda(e, "combine kernel launch");
+            return UA_ERR_CUDA;
+        }
+    }
+    p->last_launches = plan.launches;
+    p->last_path = plan.splits > 1 ? "topk_tc+combine" : "topk_tc";
     return UA_OK;
 }
 

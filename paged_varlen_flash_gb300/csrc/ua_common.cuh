@@ -41,6 +41,9 @@ struct FwdParams {
     float k_scale, v_scale;        // fp8 caches: K = code * k_scale, V = code * v_scale
     int64_t qq_stride;             // row stride of qq_bias
     int32_t part_bf16;             // part_o holds bf16 (same element indexing) instead of fp32
+    const int32_t* topk_idx;       // [total_q, topk_stride] key positions per query token, or null
+    const int32_t* topk_len;       // [total_q] list lengths (with topk_idx)
+    int32_t topk_stride;
 };
 
 // Per-sequence metadata check.  Returns UA_DEVERR_* bits (0 = well formed) and
@@ -63,6 +66,22 @@ __device__ __forceinline__ uint32_t seq_status(const FwdParams& p, int s, int& s
         (int64_t)sk > (int64_t)p.bt_stride * p.b)
         st |= UA_DEVERR_BOUNDS;
     return st;
+}
+
+// Top-k calls: the list length of query token `token`, or -1 when it lies
+// outside [0, topk_stride] (a malformed list; the token's rows are written as 0).
+__device__ __forceinline__ int topk_length(const FwdParams& p, int64_t token) {
+    const int n = __ldg(p.topk_len + token);
+    return (n < 0 || n > p.topk_stride) ? -1 : n;
+}
+
+// Segments the token's list is split into (the top-k kernel and the combine
+// kernel must agree): one per `chunk` entries, at least one.
+__device__ __forceinline__ int topk_segments(const FwdParams& p, uint32_t st, int64_t token) {
+    const int n = topk_length(p, token);
+    if (st != 0 || n <= 0) return 1;
+    const int k = (n + p.chunk - 1) / p.chunk;
+    return k < p.splits ? k : p.splits;
 }
 
 // Split partials of o: fp32, or bf16 when p.part_bf16 (half the bytes, same

@@ -129,6 +129,19 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int3
         : "memory");
 }
 
+// Row gather from a 2-D tensor map whose box is {cols, 1}: rows r0..r3 (each
+// `cols` wide from column c0) land as four consecutive box rows at dst, with
+// the map's swizzle, completion signalled on `bar` (tx bytes).
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const void* tmap, int32_t c0, int32_t r0,
+                                            int32_t r1, int32_t r2, int32_t r3, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
+        "r"(bar)
+        : "memory");
+}
+
 // ---- bf16 ------------------------------------------------------------------
 __device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }

@@ -416,7 +416,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const FwdParams p) {
     const uint32_t st = seq_status(p, lo, sq, sk, q0);
     if (st & UA_DEVERR_CU_SEQLENS) return;
     if (token < q0 || token >= q0 + sq) return;
-    const int n = seq_segments(p, st, sk);
+    const int n = p.topk_len ? topk_segments(p, st, token) : seq_segments(p, st, sk);
     const float* ml = p.part_ml + row * p.splits * 2;
     float M = -INFINITY;
     for (int k = 0; k < n; ++k) M = fmaxf(M, ml[2 * k]);

@@ -1,0 +1,628 @@
+// ua_topk.cu -- sparse top-k decode on the tcgen05 tensor cores: every query
+// token attends to its own list of key positions in its sequence's paged
+// cache (the token-granular top-k gather of "[Triton/Gluon] [GFX950] Sparse
+// paged attention and Sparse MLA"), not to all of its S_k keys.
+//
+// One CTA serves one (query token, KV head, list segment); its rows are the g
+// query heads of that KV head (g <= 16).  The products are laid out as in the
+// decode kernel, keys on the MMA M dimension:
+//
+//     S^T [128 listed keys x 16 rows] = K_gathered [128 x d] * Q^T [d x 16]
+//     O^T [d x 16 rows]              += V_gathered^T [d x 128] * P^T [128 x 16]
+//
+// The K and V tiles are gathered row by row with TMA tile::gather4 loads from
+// a 2-D view of each cache ([num_blocks * b * H_k rows, d columns], box = one
+// 128-byte panel of one row): a lane of the producer warp looks up four list
+// entries, maps each through the block table to its cache row and issues one
+// gather per 64-dim panel, so the 128 rows of a tile land in the same
+// swizzled layout a paged TMA box would give.  Entries that are not keys of
+// the row (padding, out of range, hidden by the causal mask or the window,
+// or in a bad block) gather row 0 instead, their scores are masked, and the
+// P.V issuer zeroes their V rows before the MMA (a masked weight of 0 times
+// whatever row 0 holds must stay 0).
+//
+// The softmax is the decode kernel's: base 2, lazy re-anchor, fp32 (m, l),
+// P in bf16, O^T rescaled in tensor memory; the score chain (scale, softcap,
+// ALiBi, QQ-bias, masks) uses the listed position j of each key (gfx950
+// "Unified paged attention on gfx950, from the math up", section 1).  Long
+// lists are split into segments of whole 128-entry tiles whose partials the
+// combine kernel merges (section 5); the number of segments is taken per
+// token from its own list length, and surplus CTAs return at once.
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+
+#include "ua_common.cuh"
+#include "ua_decode_common.cuh"
+#include "ua_ptx.cuh"
+#include "ua_tc.cuh"
+#include "ua_tmap.h"
+#include "ua_topk.h"
+
+#ifndef UA_TOPK_NS
+#define UA_TOPK_NS 1
+#endif
+#ifndef UA_TOPK_MIN_TILES
+#define UA_TOPK_MIN_TILES 4
+#endif
+
+namespace ua {
+namespace {
+
+constexpr int kN = 16;          // rows per tile (MMA N): the g heads of one token, padded
+constexpr int kBN = 128;        // list entries per tile (MMA M of S^T)
+constexpr int kD = 128;         // head size
+constexpr int kThreads = 224;   // 4 softmax warps, gather warp, QK^T issuer, P.V issuer
+constexpr int kWarpTma = 4;
+constexpr int kWarpMma = 5;     // QK^T issuer (also allocates tensor memory)
+constexpr int kWarpPv = 6;      // P.V issuer
+constexpr float kLazy = 8.0f;
+
+template <int NS>
+struct TCfg {
+    static constexpr int kPanels = kD / 64;
+    static constexpr int kQPanel = kN * 128;              // 16 rows x 64 dims
+    static constexpr int kQBytes = kPanels * kQPanel;
+    static constexpr int kKvPanel = kBN * 128;            // 128 rows x 64 dims
+    static constexpr int kKvBytes = kPanels * kKvPanel;
+    static constexpr int kPPanel = kN * 128;              // 16 rows x 64 keys
+    static constexpr int kPBuf = (kBN / 64) * kPPanel;    // one P^T tile
+    static constexpr int kOffQ = 0;
+    static constexpr int kOffK = 4096;
+    static constexpr int kOffV = kOffK + NS * kKvBytes;
+    static constexpr int kOffP = kOffV + NS * kKvBytes;   // two P^T buffers
+    static constexpr int kOffBar = kOffP + 2 * kPBuf;
+    // q_full, k_full[NS], v_full[NS], k_empty[NS], v_empty[NS], s_full[2],
+    // p_full[2], o_done[2], drain[2]
+    static constexpr int kNumBars = 1 + 4 * NS + 8;
+    static constexpr int kOffRed = kOffBar + kNumBars * 8;    // maxima [2][4][16] fp32
+    static constexpr int kOffSum = kOffRed + 2 * 4 * kN * 4;  // row sums [4][16] fp32
+    static constexpr int kOffMask = kOffSum + 4 * kN * 4;     // key masks [2][4] words
+    static constexpr int kOffMisc = kOffMask + 2 * 4 * 4;
+    static constexpr int kSmem = kOffMisc + 16 + 1024;
+    static constexpr int kTmemS = 0;    // S^T buffers: columns [0, 16) and [16, 32)
+    static constexpr int kTmemO = 32;   // O^T: columns [32, 48)
+    static constexpr uint32_t kTmemCols = 64;
+    static_assert(kQBytes <= kOffK, "Q tile");
+    static_assert(kSmem <= 232448, "shared memory budget");
+};
+
+// The cache row (2-D view [num_blocks * b * H_k, d]) of listed key j, or -1
+// when j is not a key of the sequence or its block id is out of range.
+__device__ __forceinline__ int32_t cache_row(const FwdParams& p, const int32_t* bt, int j, int sk,
+                                             int hkv, bool& bad_block) {
+    if (j < 0 || j >= sk) return -1;
+    const int32_t blk = __ldg(bt + j / p.b);
+    if (blk < 0 || (int64_t)blk >= p.num_blocks) {
+        bad_block = true;
+        return -1;
+    }
+    return (int32_t)(((int64_t)blk * p.b + j % p.b) * p.hk + hkv);
+}
+
+// NR: rows the softmax threads track (4, 8 or 16 >= g); the MMAs always run
+// N = 16 and ignore the padding columns.
+template <int NS, int NR, bool PLAIN>
+__global__ void __launch_bounds__(kThreads, 1)
+topk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+            const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+    using C = TCfg<NS>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int64_t token = blockIdx.x;
+    const int hkv = blockIdx.y;
+    const int seg = blockIdx.z;
+    const bool split = p.splits > 1;
+    const int g = p.g;
+    const int nrows = g;
+
+    // Owning sequence: the last s with cu_seqlens_q[s] <= token.
+    int lo = 0, hi = p.num_seqs - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if ((int64_t)__ldg(p.cu_seqlens_q + mid) <= token) lo = mid; else hi = mid - 1;
+    }
+    const int s = lo;
+    int sq, sk;
+    int64_t q0;
+    uint32_t st = seq_status(p, s, sq, sk, q0);
+    if (st && token == q0 && hkv == 0 && seg == 0 && threadIdx.x == 0) atomicOr(p.err, (int)st);
+    if (st & UA_DEVERR_CU_SEQLENS) return;
+    if (token < q0 || token >= q0 + sq) return;   // a row outside every sequence
+    const int len = topk_length(p, token);
+    if (len < 0) {
+        if (hkv == 0 && seg == 0 && threadIdx.x == 0) atomicOr(p.err, (int)UA_DEVERR_BOUNDS);
+        st |= UA_DEVERR_BOUNDS;
+    }
+    if (seg >= (split ? topk_segments(p, st, token) : 1)) return;
+    const int i = (int)(token - q0);
+    const int ctx = sk - sq;
+    const bool causal = (p.flags & UA_FLAG_CAUSAL) != 0;
+    const bool window = (p.flags & UA_FLAG_WINDOW) != 0;
+    const int e_beg = split ? seg * p.chunk : 0;
+    const int e_end = split ? min(len, e_beg + p.chunk) : len;
+    if (st || e_beg >= e_end) {
+        // A malformed sequence or list (rows written as zeros), or an empty
+        // list (no key, no value: O = 0; split: an empty partial, m = -inf).
+        for (int e = threadIdx.x; e < nrows * kD; e += kThreads) {
+            const int r = e / kD, c = e % kD;
+            const int64_t row = token * p.hq + hkv * g + r;
+            if (split) {
+                if (c == 0) {
+                    p.part_ml[(row * p.splits + seg) * 2 + 0] = -INFINITY;
+                    p.part_ml[(row * p.splits + seg) * 2 + 1] = 0.f;
+                }
+            } else {
+                p.out[row * kD + c] = __float2bfloat16_rn(0.f);
+            }
+        }
+        return;
+    }
+    const int n_tiles = (e_end - e_beg + kBN - 1) / kBN;
+    const int32_t* lst = p.topk_idx + token * p.topk_stride;
+    const int32_t* bt = p.block_table + (int64_t)s * p.bt_stride;
+
+    uint64_t* bm = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+    const uint32_t q_full = smem_u32(&bm[0]);
+    const uint32_t k_full0 = smem_u32(&bm[1]);
+    const uint32_t v_full0 = smem_u32(&bm[1 + NS]);
+    const uint32_t k_empty0 = smem_u32(&bm[1 + 2 * NS]);
+    const uint32_t v_empty0 = smem_u32(&bm[1 + 3 * NS]);
+    const uint32_t s_full0 = smem_u32(&bm[1 + 4 * NS]);
+    const uint32_t p_full0 = s_full0 + 16;
+    const uint32_t o_done0 = s_full0 + 32;
+    const uint32_t drain = s_full0 + 48;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
+    float* red = reinterpret_cast<float*>(smem + C::kOffRed);
+    float* lsum = reinterpret_cast<float*>(smem + C::kOffSum);
+    uint32_t* kmask = reinterpret_cast<uint32_t*>(smem + C::kOffMask);
+
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        for (int k = 0; k < NS; ++k) {
+            mbar_init(k_full0 + 8 * k, 1);
+            mbar_init(v_full0 + 8 * k, 1);
+            mbar_init(k_empty0 + 8 * k, 1);
+            mbar_init(v_empty0 + 8 * k, 1);
+        }
+        for (int k = 0; k < 2; ++k) {
+            mbar_init(s_full0 + 8 * k, 1);
+            mbar_init(p_full0 + 8 * k, 128);
+            mbar_init(o_done0 + 8 * k, 1);
+        }
+        mbar_init(drain, 1);
+        mbar_init(drain + 8, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == kWarpMma) {
+        tc::tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t sQ = smem_u32(smem + C::kOffQ);
+    const uint32_t sK = smem_u32(smem + C::kOffK);
+    const uint32_t sV = smem_u32(smem + C::kOffV);
+    const uint32_t sP = smem_u32(smem + C::kOffP);
+
+    if (warp == kWarpTma) {
+        // ------------------------------ gather producer ------------------------------
+        // Lane l owns list entries 4l .. 4l+3 of each tile: it maps them to cache
+        // rows (one tile ahead, so the list and block-table loads overlap the
+        // current tile's waits) and issues one four-row gather per panel.
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_q);
+            tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_v);
+            mbar_arrive_expect_tx(q_full, C::kQBytes);
+#pragma unroll
+            for (int pn = 0; pn < C::kPanels; ++pn)
+                tma_load_3d(sQ + pn * C::kQPanel, &tm_q, pn * 64, hkv * g, (int)token, q_full);
+        }
+        bool bad_block = false;
+        auto tile_rows = [&](int j, int32_t (&rw)[4]) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int e = e_beg + j * kBN + 4 * lane + k;
+                const int32_t r = e < e_end ? cache_row(p, bt, __ldg(lst + e), sk, hkv, bad_block) : -1;
+                rw[k] = r < 0 ? 0 : r;
+            }
+        };
+        int32_t nxt[4];
+        tile_rows(0, nxt);
+        int issued = 0;
+        for (int j = 0; j < n_tiles; ++j) {
+            const int stg = j % NS;
+            int32_t cur[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) cur[k] = nxt[k];
+            if (j + 1 < n_tiles) tile_rows(j + 1, nxt);
+            if (j >= NS && !__all_sync(0xffffffffu, dwait(k_empty0 + 8 * stg, ((j / NS) + 1) & 1,
+                                                          abort_flag, p.err)))
+                break;
+            if (lane == 0) mbar_arrive_expect_tx(k_full0 + 8 * stg, C::kKvBytes);
+            __syncwarp();
+#pragma unroll
+            for (int pn = 0; pn < C::kPanels; ++pn)
+                tma_gather4(sK + stg * C::kKvBytes + pn * C::kKvPanel + lane * 4 * 128, &tm_k, pn * 64,
+                            cur[0], cur[1], cur[2], cur[3], k_full0 + 8 * stg);
+            if (j >= NS && !__all_sync(0xffffffffu, dwait(v_empty0 + 8 * stg, ((j / NS) + 1) & 1,
+                                                          abort_flag, p.err)))
+                break;
+            if (lane == 0) mbar_arrive_expect_tx(v_full0 + 8 * stg, C::kKvBytes);
+            __syncwarp();
+#pragma unroll
+            for (int pn = 0; pn < C::kPanels; ++pn)
+                tma_gather4(sV + stg * C::kKvBytes + pn * C::kKvPanel + lane * 4 * 128, &tm_v, pn * 64,
+                            cur[0], cur[1], cur[2], cur[3], v_full0 + 8 * stg);
+            issued = j + 1;
+        }
+        if (__any_sync(0xffffffffu, bad_block) && lane == 0) atomicOr(p.err, (int)UA_DEVERR_BLOCK_ID);
+        if (*abort_flag && lane == 0) {
+            // Let every copy this warp issued land before the CTA ends.
+            for (int j = max(0, issued - NS); j < issued; ++j) {
+                mbar_wait_bounded(k_full0 + 8 * (j % NS), (j / NS) & 1);
+                mbar_wait_bounded(v_full0 + 8 * (j % NS), (j / NS) & 1);
+            }
+        }
+        __syncwarp();
+    } else if (warp == kWarpMma || warp == kWarpPv) {
+        // ---------------------- MMA issuers (one thread each) ----------------------
+        constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(kBN, kN, false, false);
+        constexpr uint32_t idesc_pv = tc::idesc_bf16_f32(kD, kN, true, false);
+        auto wwait = [&](uint32_t bar, uint32_t par) {
+            return __all_sync(0xffffffffu, dwait(bar, par, abort_flag, p.err));
+        };
+        if (warp == kWarpMma) {
+            bool ok = wwait(q_full, 0);
+            for (int j = 0; ok && j < n_tiles; ++j) {
+                // S^T buffer (j & 1) is free once P of tile j - 2 is published.
+                if (j >= 2 && !wwait(p_full0 + 8 * (j & 1), ((j - 2) >> 1) & 1)) break;
+                const int stg = j % NS;
+                if (!wwait(k_full0 + 8 * stg, (j / NS) & 1)) break;
+                tc::fence_after_sync();
+                if (lane == 0) {
+                    const uint32_t kst = sK + stg * C::kKvBytes;
+                    const uint32_t dS = tmem + C::kTmemS + (j & 1) * kN;
+#pragma unroll
+                    for (int k = 0; k < kD / 16; ++k) {
+                        const int pn = k >> 2, off = (k & 3) * 32;
+                        const uint64_t bq = tc::smem_desc_sw128(sQ + pn * C::kQPanel + off, 16, 1024);
+                        const uint64_t a = tc::smem_desc_sw128(kst + pn * C::kKvPanel + off, 16, 1024);
+                        tc::mma_bf16(dS, a, bq, idesc_qk, k > 0 ? 1u : 0u);
+                    }
+                    tc::commit(s_full0 + 8 * (j & 1));
+                    tc::commit(k_empty0 + 8 * stg);
+                }
+                __syncwarp();
+            }
+        } else {
+            for (int j = 0; j < n_tiles; ++j) {
+                const int stg = j % NS;
+                if (!wwait(p_full0 + 8 * (j & 1), (j >> 1) & 1)) break;
+                if (!wwait(v_full0 + 8 * stg, (j / NS) & 1)) break;
+                tc::fence_after_sync();
+                // V rows of entries that are not keys of the row become zeros
+                // (their weight is 0, but 0 times a NaN in the gathered row is NaN).
+                const uint32_t* mk = kmask + (j & 1) * 4;
+                const uint32_t full = mk[0] & mk[1] & mk[2] & mk[3];
+                if (full != 0xffffffffu) {
+                    uint8_t* vst = smem + C::kOffV + stg * C::kKvBytes;
+#pragma unroll 1
+                    for (int q = 0; q < 4; ++q) {
+                        if ((mk[q] >> lane) & 1u) continue;
+                        const int row = q * 32 + lane;
+#pragma unroll
+                        for (int pn = 0; pn < C::kPanels; ++pn) {
+                            uint4* dst = reinterpret_cast<uint4*>(vst + pn * C::kKvPanel + row * 128);
+#pragma unroll
+                            for (int c = 0; c < 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
+                        }
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                }
+                if (lane == 0) {
+                    const uint32_t vst = sV + stg * C::kKvBytes;
+                    const uint32_t pbuf = sP + (j & 1) * C::kPBuf;
+#pragma unroll
+                    for (int kk = 0; kk < kBN / 16; ++kk) {
+                        const uint64_t a = tc::smem_desc_sw128(vst + kk * 16 * 128, C::kKvPanel, 1024);
+                        const uint64_t bp =
+                            tc::smem_desc_sw128(pbuf + (kk >> 2) * C::kPPanel + (kk & 3) * 32, 16, 1024);
+                        tc::mma_bf16(tmem + C::kTmemO, a, bp, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    tc::commit(o_done0 + 8 * (j & 1));
+                    tc::commit(v_empty0 + 8 * stg);
+                }
+                __syncwarp();
+            }
+        }
+        if (*abort_flag) {
+            // No MMA this thread issued may still run when tensor memory is freed.
+            const uint32_t dr = drain + 8 * (warp - kWarpMma);
+            if (lane == 0) tc::commit(dr);
+            __syncwarp();
+            mbar_wait_bounded(dr, 0);
+        }
+    } else {
+        // --------------------------- softmax warps 0-3 ----------------------------
+        // Thread t: list entry t of each tile (S^T lane t) and head-dim element t
+        // of the output (O^T lane t).  Every row of the CTA is the same query
+        // token, so an entry is a key of all rows or of none.
+        const int t = threadIdx.x;
+        const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
+        const bool softcap = (p.flags & UA_FLAG_SOFTCAP) != 0;
+        const bool alibi = (p.flags & UA_FLAG_ALIBI) != 0;
+        const float* qrow = (p.flags & UA_FLAG_QQ_BIAS) ? p.qq_bias + (int64_t)i * p.qq_stride : nullptr;
+        const float sl2 = p.scale * kLog2e;
+        const int khi = causal ? i + ctx : sk - 1;                 // last visible position
+        const int klo = window ? i + ctx - p.window + 1 : 0;       // first visible position
+        float m[NR], l[NR], rslope[NR];
+#pragma unroll
+        for (int r = 0; r < NR; ++r) {
+            m[r] = -INFINITY;
+            l[r] = 0.f;
+            rslope[r] = (!PLAIN && alibi && r < nrows) ? __ldg(p.alibi + hkv * g + r) : 0.f;
+        }
+        bool ok = true;
+        for (int j = 0; j < n_tiles; ++j) {
+            // The entry's listed position and whether it is a key of the row;
+            // loaded before the wait so the two dependent loads overlap it.
+            const int e = e_beg + j * kBN + t;
+            int jp = -1;
+            bool valid = false;
+            if (e < e_end) {
+                jp = __ldg(lst + e);
+                bool bad = false;
+                valid = cache_row(p, bt, jp, sk, hkv, bad) >= 0 && jp <= khi && jp >= klo;
+            }
+            const bool got = __all_sync(0xffffffffu, dwait(s_full0 + 8 * (j & 1), (j >> 1) & 1,
+                                                           abort_flag, p.err));
+            float x[NR];
+            if (got) {
+                tc::fence_after_sync();
+                uint32_t sv[kN];
+                ld16(tl + C::kTmemS + (j & 1) * kN, sv);
+                tc::wait_ld();
+#pragma unroll
+                for (int r = 0; r < NR; ++r) {
+                    float v;
+                    if constexpr (PLAIN) {
+                        v = __uint_as_float(sv[r]) * sl2;
+                    } else {
+                        float tt = __uint_as_float(sv[r]) * p.scale;
+                        if (softcap) tt = p.softcap * tanh_e2(tt / p.softcap);
+                        if (alibi) tt += rslope[r] * (float)(jp - ctx);
+                        if (qrow && valid && jp >= ctx) tt += __ldg(qrow + (jp - ctx));
+                        v = tt * kLog2e;
+                    }
+                    x[r] = (valid && r < nrows) ? v : -INFINITY;
+                }
+            } else {
+#pragma unroll
+                for (int r = 0; r < NR; ++r) x[r] = -INFINITY;
+            }
+            // Per-row maxima over this warp's 32 entries, then over the 4 warps.
+#pragma unroll
+            for (int r = 0; r < NR; ++r) {
+                if (r < nrows) {
+                    const float w = warp_max_f32(x[r]);
+                    if (lane == 0) red[((j & 1) * 4 + warp) * kN + r] = w;
+                }
+            }
+            const uint32_t vmask = __ballot_sync(0xffffffffu, valid);
+            if (!dbar_and(1, 128, got)) {
+                ok = false;
+                break;
+            }
+            float alpha[NR];
+            bool any_re = false;
+#pragma unroll
+            for (int r = 0; r < NR; ++r) {
+                alpha[r] = 1.f;
+                if (r < nrows) {
+                    const float* rr = red + (j & 1) * 4 * kN + r;
+                    const float tmax = fmaxf(fmaxf(rr[0], rr[kN]), fmaxf(rr[2 * kN], rr[3 * kN]));
+                    // Lazy re-anchor: only when the tile max exceeds m by > 8 (log2).
+                    if (tmax > m[r] + kLazy) {
+                        alpha[r] = fast_exp2(m[r] - tmax);
+                        m[r] = tmax;
+                        any_re = true;
+                    }
+                }
+            }
+            // p = 2^(x - m) on the fp16x2 special-function path; per-thread
+            // partial row sums stay fp32.
+            uint32_t pb[NR / 2];
+#pragma unroll
+            for (int r = 0; r < NR; r += 2) {
+                const float a0 = x[r] - (m[r] == -INFINITY ? 0.f : m[r]);
+                const float a1 = x[r + 1] - (m[r + 1] == -INFINITY ? 0.f : m[r + 1]);
+                uint32_t h, ex;
+                asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(a1), "f"(a0));
+                asm("ex2.approx.f16x2 %0, %1;" : "=r"(ex) : "r"(h));
+                float p0, p1;
+                asm("{\n\t.reg .f16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\tcvt.f32.f16 %0, lo;\n\t"
+                    "cvt.f32.f16 %1, hi;\n\t}"
+                    : "=f"(p0), "=f"(p1)
+                    : "r"(ex));
+                l[r] = l[r] * alpha[r] + p0;
+                l[r + 1] = l[r + 1] * alpha[r + 1] + p1;
+                pb[r / 2] = pack_bf16x2(p0, p1);
+            }
+            // P^T buffer (j & 1) and mask (j & 1) were read by the P.V of tile
+            // j - 2; rescaling O needs the P.V of tile j - 1.
+            bool go = true;
+            if (j >= 2)
+                go = __all_sync(0xffffffffu, dwait(o_done0 + 8 * (j & 1), ((j - 2) >> 1) & 1,
+                                                   abort_flag, p.err));
+            if (go && any_re && j > 0) {
+                go = __all_sync(0xffffffffu, dwait(o_done0 + 8 * ((j - 1) & 1), ((j - 1) >> 1) & 1,
+                                                   abort_flag, p.err));
+                if (go) {
+                    tc::fence_after_sync();
+                    uint32_t o[kN];
+                    ld16(tl + C::kTmemO, o);
+                    tc::wait_ld();
+#pragma unroll
+                    for (int r = 0; r < NR; ++r) o[r] = __float_as_uint(__uint_as_float(o[r]) * alpha[r]);
+                    st16(tl + C::kTmemO, o);
+                    tc::wait_st();
+                }
+            }
+            if (go) {
+                // P^T row r, key t: K-major [16 rows][128 keys] in two 64-key
+                // 128-byte-swizzled panels.
+                uint8_t* pbase = smem + C::kOffP + (j & 1) * C::kPBuf + (t >> 6) * C::kPPanel;
+                const int kin = t & 63;
+#pragma unroll
+                for (int r = 0; r < NR; ++r) {
+                    if (r >= nrows) continue;  // padding columns of O^T are never read
+                    const uint16_t v = (r & 1) ? (uint16_t)(pb[r / 2] >> 16) : (uint16_t)(pb[r / 2] & 0xffffu);
+                    *reinterpret_cast<uint16_t*>(pbase + r * 128 + (((kin >> 3) ^ (r & 7)) << 4) +
+                                                 (kin & 7) * 2) = v;
+                }
+                if (lane == 0) kmask[(j & 1) * 4 + warp] = vmask;
+                fence_proxy_async_smem();
+                tc::fence_before_sync();
+                mbar_arrive(p_full0 + 8 * (j & 1));
+            }
+        }
+        // ------------------------------ epilogue ---------------------------------
+        if (ok) {
+            const bool done = __all_sync(0xffffffffu,
+                                         dwait(o_done0 + 8 * ((n_tiles - 1) & 1),
+                                               ((n_tiles - 1) >> 1) & 1, abort_flag, p.err));
+#pragma unroll
+            for (int r = 0; r < NR; ++r) {
+                if (r < nrows) {
+                    float w = l[r];
+                    w += __shfl_xor_sync(0xffffffffu, w, 1);
+                    w += __shfl_xor_sync(0xffffffffu, w, 2);
+                    w += __shfl_xor_sync(0xffffffffu, w, 4);
+                    w += __shfl_xor_sync(0xffffffffu, w, 8);
+                    w += __shfl_xor_sync(0xffffffffu, w, 16);
+                    if (lane == 0) lsum[warp * kN + r] = w;
+                }
+            }
+            if (dbar_and(1, 128, done)) {
+                tc::fence_after_sync();
+                uint32_t o[kN];
+                ld16(tl + C::kTmemO, o);
+                tc::wait_ld();
+#pragma unroll
+                for (int r = 0; r < NR; ++r) {
+                    if (r >= nrows) continue;
+                    const float L0 = lsum[r] + lsum[kN + r] + lsum[2 * kN + r] + lsum[3 * kN + r];
+                    const int64_t row = token * p.hq + hkv * g + r;
+                    const float ov = __uint_as_float(o[r]);
+                    if (split) {
+                        part_store(p, (row * p.splits + seg) * kD + t, ov);
+                        if (t == 0) {
+                            p.part_ml[(row * p.splits + seg) * 2 + 0] = m[r];
+                            p.part_ml[(row * p.splits + seg) * 2 + 1] = L0;
+                        }
+                    } else {
+                        float num = 1.f, L = L0;
+                        bool zero = false;
+                        if (p.flags & UA_FLAG_SINKS) {
+                            const float s2 = __ldg(p.sinks + hkv * g + r) * kLog2e;
+                            if (s2 == INFINITY) {
+                                zero = true;
+                            } else if (s2 > m[r]) {
+                                const float a = (m[r] == -INFINITY) ? 0.f : fast_exp2(m[r] - s2);
+                                num = a;
+                                L = L * a + 1.0f;
+                            } else if (s2 != -INFINITY) {
+                                L += fast_exp2(s2 - m[r]);
+                            }
+                        }
+                        const float inv = (!zero && L > 0.f) ? num * __frcp_rn(L) : 0.f;
+                        p.out[row * kD + t] = __float2bfloat16_rn(ov * inv);
+                    }
+                }
+            }
+        }
+    }
+
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == kWarpMma) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, C::kTmemCols);
+    }
+}
+
+template <int NS>
+cudaError_t launch_topk_t(const CUtensorMap& tq, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                          const FwdParams& p, const TopkPlan& plan, cudaStream_t stream) {
+    using C = TCfg<NS>;
+    const bool plain = (p.flags & (UA_FLAG_SOFTCAP | UA_FLAG_ALIBI | UA_FLAG_QQ_BIAS)) == 0;
+    auto kern = p.g <= 4 ? (plain ? topk_kernel<NS, 4, true> : topk_kernel<NS, 4, false>)
+              : p.g <= 8 ? (plain ? topk_kernel<NS, 8, true> : topk_kernel<NS, 8, false>)
+                         : (plain ? topk_kernel<NS, 16, true> : topk_kernel<NS, 16, false>);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    if (e != cudaSuccess) return e;
+    dim3 grid((unsigned)p.total_q, (unsigned)p.hk, (unsigned)plan.splits);
+    kern<<<grid, kThreads, C::kSmem, stream>>>(tq, tm_k, tm_v, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool topk_shape_ok(const FwdParams& p) {
+    return p.d == kD && p.g >= 1 && p.g <= kN && (kN % p.g) == 0 && p.topk_stride >= 1 &&
+           p.total_q <= 0x7fffffffLL;
+}
+
+bool encode_gather_map(CUtensorMap* m, const void* cache, int64_t num_blocks, int b, int hk, int d) {
+    // [num_blocks * b * H_k rows, d columns] (bf16), box = 64 columns x 1 row.
+    const int64_t rows = num_blocks * b * hk;
+    if (rows > 0x7fffffffLL) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {2ull * d};
+    cuuint32_t box[2] = {64, 1};
+    return encode_bf16_sw128(m, cache, 2, dims, strides, box);
+}
+
+void plan_topk(const FwdParams& p, int num_sms, size_t workspace_bytes, TopkPlan* plan) {
+    *plan = TopkPlan();
+    // Segments of whole 128-entry tiles, at least UA_TOPK_MIN_TILES each,
+    // aiming at about four waves of the two CTAs an SM holds.
+    const int64_t base = (int64_t)p.hk * p.total_q;
+    const int64_t want = (8LL * num_sms + base - 1) / base;
+    const int64_t by_len = std::max<int64_t>(1, p.topk_stride / (UA_TOPK_MIN_TILES * kBN));
+    int splits = (int)std::min<int64_t>(std::min<int64_t>(want, by_len), 64);
+    const size_t per_split = (size_t)p.total_q * p.hq * (p.d + 2) * sizeof(float);
+    splits = (int)std::min<size_t>((size_t)splits, per_split ? workspace_bytes / per_split : 1);
+    if (splits < 1) splits = 1;
+    if (splits > 1) {
+        const int per = (p.topk_stride + splits - 1) / splits;
+        plan->chunk = (per + kBN - 1) / kBN * kBN;
+        splits = (p.topk_stride + plan->chunk - 1) / plan->chunk;
+    }
+    plan->splits = splits;
+    plan->launches = splits > 1 ? 2 : 1;
+}
+
+cudaError_t launch_topk(const TopkPlan& plan, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                        const FwdParams& p, cudaStream_t stream) {
+    // Q map: [total_q, H_q, d]; box = 64 dims x g heads x 16/g positions (the
+    // token's g rows first; the rest are padding the MMAs compute and nobody reads).
+    CUtensorMap tq;
+    cuuint64_t dims[3] = {(cuuint64_t)p.d, (cuuint64_t)p.hq, (cuuint64_t)p.total_q};
+    cuuint64_t strides[2] = {2ull * p.d, 2ull * p.d * p.hq};
+    cuuint32_t box[3] = {64, (cuuint32_t)p.g, (cuuint32_t)(kN / p.g)};
+    if (!encode_bf16_sw128(&tq, p.q, 3, dims, strides, box)) return cudaErrorInvalidValue;
+    return launch_topk_t<UA_TOPK_NS>(tq, tm_k, tm_v, p, plan, stream);
+}
+
+}  // namespace ua
