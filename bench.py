@@ -37,7 +37,7 @@ METRIC = "prefill TFLOPS and decode KV-read GB/s on 1×GB300, as % of roofline"
 HEADLINE = "decode"
 SECONDARY = ["chunked", "long_prefill", "wide_mha_alibi"]
 # HBM-bound secondary workloads, reported in GB/s of algorithmic bytes.
-SECONDARY_HBM = ["decode_fp8"]
+SECONDARY_HBM = ["decode_fp8", "decode_topk"]
 L2_FLUSH_BYTES = 256 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
@@ -46,7 +46,9 @@ KERNEL_SOURCES = {
     "prefill_kernel": ["ua_prefill.cu", "ua_prefill_common.cuh", "ua_ptx.cuh", "ua_common.cuh", "ua_tc.cuh"],
     "prefill_pair_kernel": ["ua_prefill_pair.cu", "ua_prefill_common.cuh", "ua_ptx.cuh", "ua_common.cuh",
                             "ua_tc.cuh"],
-    "decode_tc_kernel": ["ua_decode_tc.cu", "ua_ptx.cuh", "ua_common.cuh", "ua_tc.cuh"],
+    "decode_tc_kernel": ["ua_decode_tc.cu", "ua_decode_common.cuh", "ua_ptx.cuh", "ua_common.cuh",
+                         "ua_tc.cuh"],
+    "topk_kernel": ["ua_topk.cu", "ua_decode_common.cuh", "ua_ptx.cuh", "ua_common.cuh", "ua_tc.cuh"],
 }
 
 
@@ -180,6 +182,8 @@ def dominant_kernel(path):
     library reports (the combine kernel is ~2% of a split call)."""
     if path.startswith("decode_tc"):
         return "decode_tc_kernel"
+    if path.startswith("topk_tc"):
+        return "topk_kernel"
     if path.startswith("tensor_core_pair"):
         return "prefill_pair_kernel"
     if path.startswith("tensor_core"):
@@ -192,6 +196,9 @@ def workload_units(w):
     kv = w.kv_bytes_read()
     qo = 2 * w.total_q * w.hq * w.d * 2
     meta = sum((k + w.b - 1) // w.b for k in w.seqlens_k) * 4 + (2 * w.num_seqs + 1) * 4
+    if w.topk_len is not None:
+        # the lists and their lengths instead of whole block-table rows
+        meta = int(w.topk_len.to("cpu").sum()) * 4 + w.total_q * 4 + (2 * w.num_seqs + 1) * 4
     flops = 4.0 * w.d * w.hq * w.visible_pairs()
     return kv + qo + meta, flops
 
@@ -362,15 +369,17 @@ def run_ours(args):
         for name in SECONDARY_HBM:
             ws = W.make(name, device=dev)
             b_s, f_s = workload_units(ws)
-            r = time_ours(ws, max(3, min(args.steps, 20)), max(3, args.warmup), flush=False,
-                          torch=torch, ua=ua)
+            # decode_topk touches 0.27 GB per step, only twice L2: flush between steps
+            r = time_ours(ws, max(3, min(args.steps, 20)), max(3, args.warmup),
+                          flush=ws.topk_len is not None, torch=torch, ua=ua)
             ms = statistics.mean(r["step_ms"])
             km = statistics.mean(r["kernel_ms"])
             per_config[name] = {
                 "ms_per_step": round(ms, 4), "gbs": round(b_s / (ms * 1e-3) / 1e9, 1),
                 "kernel_gbs": round(b_s / (km * 1e-3) / 1e9, 1),
                 "frac_of_hbm_peak": round(b_s / (km * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
-                "kv_tokens_per_s": round(sum(ws.seqlens_k) / (ms * 1e-3), 1),
+                "kv_tokens_per_s": round((sum(ws.seqlens_k) if ws.topk_len is None else
+                                          int(ws.topk_len.to("cpu").sum())) / (ms * 1e-3), 1),
                 "path": r["path"], "launches_per_step": r["launches"] // max(1, len(r["step_ms"])),
                 "bytes": b_s, "device_error": r["device_error"]}
             del ws
@@ -501,7 +510,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default=None,
                     choices=["tiny", "decode", "chunked", "long_prefill", "long_prefill_shuffled",
-                             "wide_mha_alibi", "decode_fp8"],
+                             "wide_mha_alibi", "decode_fp8", "decode_topk"],
                     help="time only this workload and print its own short JSON line "
                          "(for profiling); the default is the full headline run")
     ap.add_argument("--path", default="auto", choices=["auto", "split", "tensor", "decode"],

@@ -281,6 +281,8 @@ ua_status prepare_call(ua_problem* p, const void* q, const void* k_cache, const 
     ua::FwdParams& fp = *fpp;
     std::memset(&fp, 0, sizeof fp);
     fp.q = static_cast<const __nv_bfloat16*>(q);
+    fp.k_cache = k_cache;
+    fp.v_cache = v_cache;
     fp.block_table = block_table;
     fp.cu_seqlens_q = cu_seqlens_q;
     fp.seqused_k = seqused_k;

@@ -13,6 +13,8 @@ namespace ua {
 
 struct FwdParams {
     const __nv_bfloat16* q;        // [total_q, hq, d]
+    const void* k_cache;           // [num_blocks, b, hk, d] (paths that read rows directly)
+    const void* v_cache;
     const int32_t* block_table;    // [num_seqs, bt_stride]
     const int32_t* cu_seqlens_q;   // [num_seqs + 1]
     const int32_t* seqused_k;      // [num_seqs]

@@ -43,8 +43,18 @@
 #define UA_TOPK_NS 1
 #endif
 #ifndef UA_TOPK_MIN_TILES
-#define UA_TOPK_MIN_TILES 4
+#define UA_TOPK_MIN_TILES 8
 #endif
+// How each operand's rows are fetched: 1 = 16-byte cp.async from a loader
+// warp (coalesced: one warp instruction moves two 256-byte rows), 0 = TMA
+// tile::gather4 from the producer warp.
+#ifndef UA_TOPK_K_LSU
+#define UA_TOPK_K_LSU 0
+#endif
+#ifndef UA_TOPK_V_LSU
+#define UA_TOPK_V_LSU 1
+#endif
+#define UA_TOPK_LSU (UA_TOPK_K_LSU || UA_TOPK_V_LSU)
 
 namespace ua {
 namespace {
@@ -52,8 +62,10 @@ namespace {
 constexpr int kN = 16;          // rows per tile (MMA N): the g heads of one token, padded
 constexpr int kBN = 128;        // list entries per tile (MMA M of S^T)
 constexpr int kD = 128;         // head size
-constexpr int kThreads = 224;   // 4 softmax warps, gather warp, QK^T issuer, P.V issuer
+// 4 softmax warps, K loader (also Q), QK^T issuer, P.V issuer, V loader (LSU)
+constexpr int kThreads = UA_TOPK_LSU ? 256 : 224;
 constexpr int kWarpTma = 4;
+constexpr int kWarpLdV = 7;
 constexpr int kWarpMma = 5;     // QK^T issuer (also allocates tensor memory)
 constexpr int kWarpPv = 6;      // P.V issuer
 constexpr float kLazy = 8.0f;
@@ -103,7 +115,7 @@ __device__ __forceinline__ int32_t cache_row(const FwdParams& p, const int32_t* 
 // NR: rows the softmax threads track (4, 8 or 16 >= g); the MMAs always run
 // N = 16 and ignore the padding columns.
 template <int NS, int NR, bool PLAIN>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)   // two CTAs per SM
 topk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
             const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
     using C = TCfg<NS>;
@@ -212,15 +224,83 @@ topk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     const uint32_t sV = smem_u32(smem + C::kOffV);
     const uint32_t sP = smem_u32(smem + C::kOffP);
 
-    if (warp == kWarpTma) {
+    if ((UA_TOPK_K_LSU && warp == kWarpTma) || (UA_TOPK_V_LSU && warp == kWarpLdV)) {
+        // ------------------------------ row loaders ------------------------------
+        // Warp 4 copies the K tiles (and loads Q), warp 7 the V tiles.  Lane l
+        // maps list entries 4l .. 4l+3 of a tile to cache rows (one tile ahead);
+        // warp instruction n then moves rows n and n + 64: lanes 0-15 copy the
+        // sixteen 16-byte chunks of row n, lanes 16-31 those of row n + 64, into
+        // the 128-byte-swizzled panels the MMA reads.  Rows of entries that are
+        // not keys of the sequence are skipped (K: their scores are masked) or
+        // zeroed (V: their weight is 0, and 0 times stale data could be NaN).
+        const bool is_k = warp == kWarpTma;
+        if (is_k && lane == 0) {
+            tma_prefetch_desc(&tm_q);
+            mbar_arrive_expect_tx(q_full, C::kQBytes);
+#pragma unroll
+            for (int pn = 0; pn < C::kPanels; ++pn)
+                tma_load_3d(sQ + pn * C::kQPanel, &tm_q, pn * 64, hkv * g, (int)token, q_full);
+        }
+        const char* cache = static_cast<const char*>(is_k ? p.k_cache : p.v_cache);
+        const uint32_t ring = is_k ? sK : sV;
+        const uint32_t full0 = is_k ? k_full0 : v_full0;
+        const uint32_t empty0 = is_k ? k_empty0 : v_empty0;
+        bool bad_block = false;
+        auto tile_rows = [&](int j, int32_t (&rw)[4]) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int e = e_beg + j * kBN + 4 * lane + k;
+                rw[k] = e < e_end ? cache_row(p, bt, __ldg(lst + e), sk, hkv, bad_block) : -1;
+            }
+        };
+        const int half = lane >> 4;           // 0: row n, 1: row n + 64
+        const int c = lane & 15;              // 16-byte chunk of the 256-byte row
+        const uint32_t chunk_off = (uint32_t)(c >> 3) * C::kKvPanel;
+        const int src_base = half * 16;       // lanes holding rows 64 .. 127
+        int32_t nxt[4];
+        tile_rows(0, nxt);
+        for (int j = 0; j < n_tiles; ++j) {
+            const int stg = j % NS;
+            int32_t cur[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) cur[k] = nxt[k];
+            if (j + 1 < n_tiles) tile_rows(j + 1, nxt);
+            if (j >= NS && !__all_sync(0xffffffffu, dwait(empty0 + 8 * stg, ((j / NS) + 1) & 1,
+                                                          abort_flag, p.err)))
+                break;
+            const uint32_t dst0 = ring + stg * C::kKvBytes + chunk_off;
+#pragma unroll 4
+            for (int n4 = 0; n4 < 64; n4 += 4) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int n = n4 + k;             // rows n (owned by lane n/4) and n + 64
+                    const int32_t row = __shfl_sync(0xffffffffu, cur[k], src_base + (n >> 2));
+                    const int r = n + half * 64;
+                    const uint32_t dst = dst0 + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+                    if (row >= 0)
+                        cp_async16(dst, cache + (int64_t)row * (kD * 2) + c * 16);
+                    else if (!is_k)
+                        st_shared_zero16(dst);
+                }
+            }
+            cp_async_wait_all();
+            fence_proxy_async_smem();   // the MMAs read these rows through the async proxy
+            __syncwarp();
+            if (lane == 0) mbar_arrive(full0 + 8 * stg);
+        }
+        if (__any_sync(0xffffffffu, bad_block) && lane == 0) atomicOr(p.err, (int)UA_DEVERR_BLOCK_ID);
+        __syncwarp();
+    } else if (warp == (UA_TOPK_K_LSU ? kWarpLdV : kWarpTma)) {
         // ------------------------------ gather producer ------------------------------
         // Lane l owns list entries 4l .. 4l+3 of each tile: it maps them to cache
         // rows (one tile ahead, so the list and block-table loads overlap the
         // current tile's waits) and issues one four-row gather per panel.
         if (lane == 0) {
-            tma_prefetch_desc(&tm_q);
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
+        }
+        if (!UA_TOPK_K_LSU && lane == 0) {
+            tma_prefetch_desc(&tm_q);
             mbar_arrive_expect_tx(q_full, C::kQBytes);
 #pragma unroll
             for (int pn = 0; pn < C::kPanels; ++pn)
@@ -244,32 +324,36 @@ topk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
 #pragma unroll
             for (int k = 0; k < 4; ++k) cur[k] = nxt[k];
             if (j + 1 < n_tiles) tile_rows(j + 1, nxt);
-            if (j >= NS && !__all_sync(0xffffffffu, dwait(k_empty0 + 8 * stg, ((j / NS) + 1) & 1,
-                                                          abort_flag, p.err)))
-                break;
-            if (lane == 0) mbar_arrive_expect_tx(k_full0 + 8 * stg, C::kKvBytes);
-            __syncwarp();
+            if (!UA_TOPK_K_LSU) {
+                if (j >= NS && !__all_sync(0xffffffffu, dwait(k_empty0 + 8 * stg, ((j / NS) + 1) & 1,
+                                                              abort_flag, p.err)))
+                    break;
+                if (lane == 0) mbar_arrive_expect_tx(k_full0 + 8 * stg, C::kKvBytes);
+                __syncwarp();
 #pragma unroll
-            for (int pn = 0; pn < C::kPanels; ++pn)
-                tma_gather4(sK + stg * C::kKvBytes + pn * C::kKvPanel + lane * 4 * 128, &tm_k, pn * 64,
-                            cur[0], cur[1], cur[2], cur[3], k_full0 + 8 * stg);
-            if (j >= NS && !__all_sync(0xffffffffu, dwait(v_empty0 + 8 * stg, ((j / NS) + 1) & 1,
-                                                          abort_flag, p.err)))
-                break;
-            if (lane == 0) mbar_arrive_expect_tx(v_full0 + 8 * stg, C::kKvBytes);
-            __syncwarp();
+                for (int pn = 0; pn < C::kPanels; ++pn)
+                    tma_gather4(sK + stg * C::kKvBytes + pn * C::kKvPanel + lane * 4 * 128, &tm_k,
+                                pn * 64, cur[0], cur[1], cur[2], cur[3], k_full0 + 8 * stg);
+            }
+            if (!UA_TOPK_V_LSU) {
+                if (j >= NS && !__all_sync(0xffffffffu, dwait(v_empty0 + 8 * stg, ((j / NS) + 1) & 1,
+                                                              abort_flag, p.err)))
+                    break;
+                if (lane == 0) mbar_arrive_expect_tx(v_full0 + 8 * stg, C::kKvBytes);
+                __syncwarp();
 #pragma unroll
-            for (int pn = 0; pn < C::kPanels; ++pn)
-                tma_gather4(sV + stg * C::kKvBytes + pn * C::kKvPanel + lane * 4 * 128, &tm_v, pn * 64,
-                            cur[0], cur[1], cur[2], cur[3], v_full0 + 8 * stg);
+                for (int pn = 0; pn < C::kPanels; ++pn)
+                    tma_gather4(sV + stg * C::kKvBytes + pn * C::kKvPanel + lane * 4 * 128, &tm_v,
+                                pn * 64, cur[0], cur[1], cur[2], cur[3], v_full0 + 8 * stg);
+            }
             issued = j + 1;
         }
         if (__any_sync(0xffffffffu, bad_block) && lane == 0) atomicOr(p.err, (int)UA_DEVERR_BLOCK_ID);
         if (*abort_flag && lane == 0) {
             // Let every copy this warp issued land before the CTA ends.
             for (int j = max(0, issued - NS); j < issued; ++j) {
-                mbar_wait_bounded(k_full0 + 8 * (j % NS), (j / NS) & 1);
-                mbar_wait_bounded(v_full0 + 8 * (j % NS), (j / NS) & 1);
+                if (!UA_TOPK_K_LSU) mbar_wait_bounded(k_full0 + 8 * (j % NS), (j / NS) & 1);
+                if (!UA_TOPK_V_LSU) mbar_wait_bounded(v_full0 + 8 * (j % NS), (j / NS) & 1);
             }
         }
         __syncwarp();
@@ -313,7 +397,7 @@ topk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 // (their weight is 0, but 0 times a NaN in the gathered row is NaN).
                 const uint32_t* mk = kmask + (j & 1) * 4;
                 const uint32_t full = mk[0] & mk[1] & mk[2] & mk[3];
-                if (full != 0xffffffffu) {
+                if (!UA_TOPK_V_LSU && full != 0xffffffffu) {
                     uint8_t* vst = smem + C::kOffV + stg * C::kKvBytes;
 #pragma unroll 1
                     for (int q = 0; q < 4; ++q) {

@@ -123,7 +123,10 @@ class Workload:
     # -- counts used for reporting (no attention arithmetic) ------------------
     def visible_pairs(self) -> int:
         """Number of (query row, key) pairs the masks keep, summed over seqs
-        (per query head)."""
+        (per query head); with top-k lists, the listed entries that are keys
+        of their row."""
+        if self.topk_idx is not None:
+            return self._listed_keys()
         total = 0
         for sq, sk in zip(self.seqlens_q, self.seqlens_k):
             ctx = sk - sq
@@ -131,6 +134,21 @@ class Workload:
                 hi = i + ctx if self.causal else sk - 1
                 lo = max(0, i + ctx - self.window + 1) if self.window > 0 else 0
                 total += max(0, hi - lo + 1)
+        return total
+
+    def _listed_keys(self) -> int:
+        idx = self.topk_idx.cpu().to(torch.int64)
+        n = self.topk_len.cpu().to(torch.int64)
+        total = 0
+        t = 0
+        for sq, sk in zip(self.seqlens_q, self.seqlens_k):
+            ctx = sk - sq
+            for i in range(sq):
+                row = idx[t, :int(n[t])]
+                hi = i + ctx if self.causal else sk - 1
+                lo = i + ctx - self.window + 1 if self.window > 0 else 0
+                total += int(((row >= max(lo, 0)) & (row <= min(hi, sk - 1))).sum())
+                t += 1
         return total
 
     def kv_bytes_read(self) -> int:
