@@ -39,8 +39,12 @@
 #include "ua_tmap.h"
 #include "ua_topk.h"
 
-#ifndef UA_TOPK_NS
-#define UA_TOPK_NS 1
+// K and V ring depths (two CTAs per SM hold NSK + NSV <= 3 stages).
+#ifndef UA_TOPK_NSK
+#define UA_TOPK_NSK 1
+#endif
+#ifndef UA_TOPK_NSV
+#define UA_TOPK_NSV 1
 #endif
 #ifndef UA_TOPK_MIN_TILES
 #define UA_TOPK_MIN_TILES 8
@@ -70,7 +74,7 @@ constexpr int kWarpMma = 5;     // QK^T issuer (also allocates tensor memory)
 constexpr int kWarpPv = 6;      // P.V issuer
 constexpr float kLazy = 8.0f;
 
-template <int NS>
+template <int NSK, int NSV>
 struct TCfg {
     static constexpr int kPanels = kD / 64;
     static constexpr int kQPanel = kN * 128;              // 16 rows x 64 dims
@@ -81,12 +85,12 @@ struct TCfg {
     static constexpr int kPBuf = (kBN / 64) * kPPanel;    // one P^T tile
     static constexpr int kOffQ = 0;
     static constexpr int kOffK = 4096;
-    static constexpr int kOffV = kOffK + NS * kKvBytes;
-    static constexpr int kOffP = kOffV + NS * kKvBytes;   // two P^T buffers
+    static constexpr int kOffV = kOffK + NSK * kKvBytes;
+    static constexpr int kOffP = kOffV + NSV * kKvBytes;  // two P^T buffers
     static constexpr int kOffBar = kOffP + 2 * kPBuf;
-    // q_full, k_full[NS], v_full[NS], k_empty[NS], v_empty[NS], s_full[2],
+    // q_full, k_full[NSK], v_full[NSV], k_empty[NSK], v_empty[NSV], s_full[2],
     // p_full[2], o_done[2], drain[2]
-    static constexpr int kNumBars = 1 + 4 * NS + 8;
+    static constexpr int kNumBars = 1 + 2 * NSK + 2 * NSV + 8;
     static constexpr int kOffRed = kOffBar + kNumBars * 8;    // maxima [2][4][16] fp32
     static constexpr int kOffSum = kOffRed + 2 * 4 * kN * 4;  // row sums [4][16] fp32
     static constexpr int kOffMask = kOffSum + 4 * kN * 4;     // key masks [2][4] words
@@ -114,11 +118,11 @@ __device__ __forceinline__ int32_t cache_row(const FwdParams& p, const int32_t* 
 
 // NR: rows the softmax threads track (4, 8 or 16 >= g); the MMAs always run
 // N = 16 and ignore the padding columns.
-template <int NS, int NR, bool PLAIN>
+template <int NSK, int NSV, int NR, bool PLAIN>
 __global__ void __launch_bounds__(kThreads, 2)   // two CTAs per SM
 topk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
             const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
-    using C = TCfg<NS>;
+    using C = TCfg<NSK, NSV>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -180,10 +184,10 @@ topk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     uint64_t* bm = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
     const uint32_t q_full = smem_u32(&bm[0]);
     const uint32_t k_full0 = smem_u32(&bm[1]);
-    const uint32_t v_full0 = smem_u32(&bm[1 + NS]);
-    const uint32_t k_empty0 = smem_u32(&bm[1 + 2 * NS]);
-    const uint32_t v_empty0 = smem_u32(&bm[1 + 3 * NS]);
-    const uint32_t s_full0 = smem_u32(&bm[1 + 4 * NS]);
+    const uint32_t v_full0 = smem_u32(&bm[1 + NSK]);
+    const uint32_t k_empty0 = smem_u32(&bm[1 + NSK + NSV]);
+    const uint32_t v_empty0 = smem_u32(&bm[1 + 2 * NSK + NSV]);
+    const uint32_t s_full0 = smem_u32(&bm[1 + 2 * NSK + 2 * NSV]);
     const uint32_t p_full0 = s_full0 + 16;
     const uint32_t o_done0 = s_full0 + 32;
     const uint32_t drain = s_full0 + 48;
@@ -195,10 +199,12 @@ topk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
-        for (int k = 0; k < NS; ++k) {
+        for (int k = 0; k < NSK; ++k) {
             mbar_init(k_full0 + 8 * k, 1);
-            mbar_init(v_full0 + 8 * k, 1);
             mbar_init(k_empty0 + 8 * k, 1);
+        }
+        for (int k = 0; k < NSV; ++k) {
+            mbar_init(v_full0 + 8 * k, 1);
             mbar_init(v_empty0 + 8 * k, 1);
         }
         for (int k = 0; k < 2; ++k) {
@@ -259,14 +265,15 @@ topk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         const int src_base = half * 16;       // lanes holding rows 64 .. 127
         int32_t nxt[4];
         tile_rows(0, nxt);
+        const int nst = is_k ? NSK : NSV;
         for (int j = 0; j < n_tiles; ++j) {
-            const int stg = j % NS;
+            const int stg = j % nst;
             int32_t cur[4];
 #pragma unroll
             for (int k = 0; k < 4; ++k) cur[k] = nxt[k];
             if (j + 1 < n_tiles) tile_rows(j + 1, nxt);
-            if (j >= NS && !__all_sync(0xffffffffu, dwait(empty0 + 8 * stg, ((j / NS) + 1) & 1,
-                                                          abort_flag, p.err)))
+            if (j >= nst && !__all_sync(0xffffffffu, dwait(empty0 + 8 * stg, ((j / nst) + 1) & 1,
+                                                           abort_flag, p.err)))
                 break;
             const uint32_t dst0 = ring + stg * C::kKvBytes + chunk_off;
 #pragma unroll 4
@@ -319,42 +326,42 @@ topk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         tile_rows(0, nxt);
         int issued = 0;
         for (int j = 0; j < n_tiles; ++j) {
-            const int stg = j % NS;
+            const int stk = j % NSK, stv = j % NSV;
             int32_t cur[4];
 #pragma unroll
             for (int k = 0; k < 4; ++k) cur[k] = nxt[k];
             if (j + 1 < n_tiles) tile_rows(j + 1, nxt);
             if (!UA_TOPK_K_LSU) {
-                if (j >= NS && !__all_sync(0xffffffffu, dwait(k_empty0 + 8 * stg, ((j / NS) + 1) & 1,
-                                                              abort_flag, p.err)))
+                if (j >= NSK && !__all_sync(0xffffffffu, dwait(k_empty0 + 8 * stk, ((j / NSK) + 1) & 1,
+                                                               abort_flag, p.err)))
                     break;
-                if (lane == 0) mbar_arrive_expect_tx(k_full0 + 8 * stg, C::kKvBytes);
+                if (lane == 0) mbar_arrive_expect_tx(k_full0 + 8 * stk, C::kKvBytes);
                 __syncwarp();
 #pragma unroll
                 for (int pn = 0; pn < C::kPanels; ++pn)
-                    tma_gather4(sK + stg * C::kKvBytes + pn * C::kKvPanel + lane * 4 * 128, &tm_k,
-                                pn * 64, cur[0], cur[1], cur[2], cur[3], k_full0 + 8 * stg);
+                    tma_gather4(sK + stk * C::kKvBytes + pn * C::kKvPanel + lane * 4 * 128, &tm_k,
+                                pn * 64, cur[0], cur[1], cur[2], cur[3], k_full0 + 8 * stk);
             }
             if (!UA_TOPK_V_LSU) {
-                if (j >= NS && !__all_sync(0xffffffffu, dwait(v_empty0 + 8 * stg, ((j / NS) + 1) & 1,
-                                                              abort_flag, p.err)))
+                if (j >= NSV && !__all_sync(0xffffffffu, dwait(v_empty0 + 8 * stv, ((j / NSV) + 1) & 1,
+                                                               abort_flag, p.err)))
                     break;
-                if (lane == 0) mbar_arrive_expect_tx(v_full0 + 8 * stg, C::kKvBytes);
+                if (lane == 0) mbar_arrive_expect_tx(v_full0 + 8 * stv, C::kKvBytes);
                 __syncwarp();
 #pragma unroll
                 for (int pn = 0; pn < C::kPanels; ++pn)
-                    tma_gather4(sV + stg * C::kKvBytes + pn * C::kKvPanel + lane * 4 * 128, &tm_v,
-                                pn * 64, cur[0], cur[1], cur[2], cur[3], v_full0 + 8 * stg);
+                    tma_gather4(sV + stv * C::kKvBytes + pn * C::kKvPanel + lane * 4 * 128, &tm_v,
+                                pn * 64, cur[0], cur[1], cur[2], cur[3], v_full0 + 8 * stv);
             }
             issued = j + 1;
         }
         if (__any_sync(0xffffffffu, bad_block) && lane == 0) atomicOr(p.err, (int)UA_DEVERR_BLOCK_ID);
         if (*abort_flag && lane == 0) {
             // Let every copy this warp issued land before the CTA ends.
-            for (int j = max(0, issued - NS); j < issued; ++j) {
-                if (!UA_TOPK_K_LSU) mbar_wait_bounded(k_full0 + 8 * (j % NS), (j / NS) & 1);
-                if (!UA_TOPK_V_LSU) mbar_wait_bounded(v_full0 + 8 * (j % NS), (j / NS) & 1);
-            }
+            for (int j = max(0, issued - NSK); j < issued && !UA_TOPK_K_LSU; ++j)
+                mbar_wait_bounded(k_full0 + 8 * (j % NSK), (j / NSK) & 1);
+            for (int j = max(0, issued - NSV); j < issued && !UA_TOPK_V_LSU; ++j)
+                mbar_wait_bounded(v_full0 + 8 * (j % NSV), (j / NSV) & 1);
         }
         __syncwarp();
     } else if (warp == kWarpMma || warp == kWarpPv) {
@@ -369,8 +376,8 @@ topk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             for (int j = 0; ok && j < n_tiles; ++j) {
                 // S^T buffer (j & 1) is free once P of tile j - 2 is published.
                 if (j >= 2 && !wwait(p_full0 + 8 * (j & 1), ((j - 2) >> 1) & 1)) break;
-                const int stg = j % NS;
-                if (!wwait(k_full0 + 8 * stg, (j / NS) & 1)) break;
+                const int stg = j % NSK;
+                if (!wwait(k_full0 + 8 * stg, (j / NSK) & 1)) break;
                 tc::fence_after_sync();
                 if (lane == 0) {
                     const uint32_t kst = sK + stg * C::kKvBytes;
@@ -389,9 +396,9 @@ topk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             }
         } else {
             for (int j = 0; j < n_tiles; ++j) {
-                const int stg = j % NS;
+                const int stg = j % NSV;
                 if (!wwait(p_full0 + 8 * (j & 1), (j >> 1) & 1)) break;
-                if (!wwait(v_full0 + 8 * stg, (j / NS) & 1)) break;
+                if (!wwait(v_full0 + 8 * stg, (j / NSV) & 1)) break;
                 tc::fence_after_sync();
                 // V rows of entries that are not keys of the row become zeros
                 // (their weight is 0, but 0 times a NaN in the gathered row is NaN).
@@ -645,14 +652,14 @@ topk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
     }
 }
 
-template <int NS>
+template <int NSK, int NSV>
 cudaError_t launch_topk_t(const CUtensorMap& tq, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                           const FwdParams& p, const TopkPlan& plan, cudaStream_t stream) {
-    using C = TCfg<NS>;
+    using C = TCfg<NSK, NSV>;
     const bool plain = (p.flags & (UA_FLAG_SOFTCAP | UA_FLAG_ALIBI | UA_FLAG_QQ_BIAS)) == 0;
-    auto kern = p.g <= 4 ? (plain ? topk_kernel<NS, 4, true> : topk_kernel<NS, 4, false>)
-              : p.g <= 8 ? (plain ? topk_kernel<NS, 8, true> : topk_kernel<NS, 8, false>)
-                         : (plain ? topk_kernel<NS, 16, true> : topk_kernel<NS, 16, false>);
+    auto kern = p.g <= 4 ? (plain ? topk_kernel<NSK, NSV, 4, true> : topk_kernel<NSK, NSV, 4, false>)
+              : p.g <= 8 ? (plain ? topk_kernel<NSK, NSV, 8, true> : topk_kernel<NSK, NSV, 8, false>)
+                         : (plain ? topk_kernel<NSK, NSV, 16, true> : topk_kernel<NSK, NSV, 16, false>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)p.total_q, (unsigned)p.hk, (unsigned)plan.splits);
@@ -706,7 +713,7 @@ cudaError_t launch_topk(const TopkPlan& plan, const CUtensorMap& tm_k, const CUt
     cuuint64_t strides[2] = {2ull * p.d, 2ull * p.d * p.hq};
     cuuint32_t box[3] = {64, (cuuint32_t)p.g, (cuuint32_t)(kN / p.g)};
     if (!encode_bf16_sw128(&tq, p.q, 3, dims, strides, box)) return cudaErrorInvalidValue;
-    return launch_topk_t<UA_TOPK_NS>(tq, tm_k, tm_v, p, plan, stream);
+    return launch_topk_t<UA_TOPK_NSK, UA_TOPK_NSV>(tq, tm_k, tm_v, p, plan, stream);
 }
 
 }  // namespace ua
