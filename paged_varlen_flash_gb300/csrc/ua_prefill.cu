@@ -84,7 +84,9 @@ struct PCfg {
 // engine moves half the bytes per flop; a stage is reloaded only after both
 // CTAs' MMAs released it.  Both CTAs walk the union of their key ranges (a
 // row still masks keys outside its own range).
-template <int D, int BN, int NK, int NV, int SPLIT, bool PLAIN, int CL>
+// QQ: the query-query bias pass is compiled in (a separate instantiation, so
+// that the score loop of the other non-plain calls keeps its registers).
+template <int D, int BN, int NK, int NV, int SPLIT, bool PLAIN, int CL, bool QQ>
 __global__ void __launch_bounds__(Roles<SPLIT>::kThreads, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
@@ -409,7 +411,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         const float slope = alibi ? __ldg(p.alibi + head) : 0.f;
         const float inv_cap = softcap ? 1.0f / p.softcap : 0.f;
         // The row's line of the query-query bias (none for padding rows).
-        const float* qrow = ((p.flags & UA_FLAG_QQ_BIAS) && row_valid)
+        const float* qrow = (QQ && row_valid)
                                 ? p.qq_bias + (int64_t)i * p.qq_stride
                                 : nullptr;
         const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16);
@@ -442,9 +444,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     // ALiBi: one int -> float conversion per tile; the per-key
                     // offsets are compile-time constants.
                     const float abias = slope * (float)(key0 - ctx);
-                    // Query-query bias on the query-section keys up to the
-                    // row's last visible key (so j - ctx < S_q).
-                    const bool qtile = qrow != nullptr && key0 + CPT > ctx && key0 <= hi;
 #pragma unroll
                     for (int c = 0; c < CPT / 32; ++c)
 #pragma unroll
@@ -452,12 +451,23 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                             float t = __uint_as_float(sr[c][e]) * p.scale;
                             if (softcap) t = p.softcap * tanh_via_exp2(t * inv_cap);
                             if (alibi) t += abias + slope * (float)(c * 32 + e);
-                            if (qtile) {
-                                const int kc = key0 - ctx + c * 32 + e;
-                                if (kc >= 0 && kc <= hi - ctx) t += __ldg(qrow + kc);
-                            }
                             sr[c][e] = __float_as_uint(t * kLog2e);
                         }
+                    // Query-query bias, in its own pass so that the loop above
+                    // stays as lean without it: the query-section keys up to
+                    // the row's last visible key (so j - ctx < S_q), in log2
+                    // units like the scores it joins.
+                    if (QQ && qrow != nullptr && key0 + CPT > ctx && key0 <= hi) {
+#pragma unroll
+                        for (int c = 0; c < CPT / 32; ++c)
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) {
+                                const int kc = key0 - ctx + c * 32 + e;
+                                if (kc >= 0 && kc <= hi - ctx)
+                                    sr[c][e] = __float_as_uint(__uint_as_float(sr[c][e]) +
+                                                               __ldg(qrow + kc) * kLog2e);
+                            }
+                    }
                 }
                 if (!mask_free) {
 #pragma unroll
@@ -648,12 +658,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     }
 }
 
-template <int D, int BN, int NK, int NV, int SPLIT, bool PLAIN, int CL>
+template <int D, int BN, int NK, int NV, int SPLIT, bool PLAIN, int CL, bool QQ = false>
 cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                      const FwdParams& p, int tiles, cudaStream_t stream) {
     using C = PCfg<D, BN, NK, NV, SPLIT>;
     constexpr int kThreads = Roles<SPLIT>::kThreads;
-    auto kern = prefill_kernel<D, BN, NK, NV, SPLIT, PLAIN, CL>;
+    auto kern = prefill_kernel<D, BN, NK, NV, SPLIT, PLAIN, CL, QQ>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
     // With clusters of two, grid x holds (pair, segment, rank); an odd tile
@@ -725,8 +735,10 @@ cudaError_t launch_prefill(const PrefillPlan& plan, const CUtensorMap& tm_k, con
     if (plan.num_tiles <= 0) return cudaSuccess;
     if (prefill_pair_supported(p.d))
         return launch_prefill_pair(tq, tm_k, tm_v, p, (plan.num_tiles + 1) / 2, stream);
-    const bool plain = (p.flags & (UA_FLAG_SOFTCAP | UA_FLAG_ALIBI | UA_FLAG_QQ_BIAS)) == 0;
+    const bool qq = (p.flags & UA_FLAG_QQ_BIAS) != 0;
+    const bool plain = !qq && (p.flags & (UA_FLAG_SOFTCAP | UA_FLAG_ALIBI)) == 0;
     if (p.d != 256) return cudaErrorInvalidValue;
+    if (qq) return launch_t<256, 64, 2, 2, 2, false, UA_PF256_CL, true>(tq, tm_k, tm_v, p, plan.num_tiles, stream);
     return plain ? launch_t<256, 64, 2, 2, 2, true, UA_PF256_CL>(tq, tm_k, tm_v, p, plan.num_tiles, stream)
                  : launch_t<256, 64, 2, 2, 2, false, UA_PF256_CL>(tq, tm_k, tm_v, p, plan.num_tiles, stream);
 }

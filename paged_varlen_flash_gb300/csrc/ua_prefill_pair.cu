@@ -89,7 +89,9 @@ struct PR {
     static constexpr uint32_t kRegsOther = 56;
 };
 
-template <int D, int NK, int NV, bool PLAIN>
+// QQ: the query-query bias pass is compiled in (a separate instantiation, so
+// that the score loop of the other non-plain calls keeps its registers).
+template <int D, int NK, int NV, bool PLAIN, bool QQ>
 __global__ void __launch_bounds__(PR::kThreads, 1)
 prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
@@ -393,7 +395,7 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         const int hi = causal ? min(pos + ctx, sk - 1) : sk - 1;
         const int lo = window ? max(0, pos + ctx - p.window + 1) : 0;
         // The row's line of the query-query bias (none for padding rows).
-        const float* qrow = ((p.flags & UA_FLAG_QQ_BIAS) && valid)
+        const float* qrow = (QQ && valid)
                                 ? p.qq_bias + (int64_t)pos * p.qq_stride
                                 : nullptr;
         // Keys every row of the tile sees: [kfree_lo, kfree_hi].
@@ -440,9 +442,6 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                     // ALiBi: one int -> float conversion per tile; the per-key
                     // offsets are compile-time constants.
                     const float abias = slope * (float)(key0 - ctx);
-                    // Query-query bias on the query-section keys up to the
-                    // row's last visible key (so j - ctx < S_q).
-                    const bool qtile = qrow != nullptr && key0 + kBN > ctx && key0 <= hi;
 #pragma unroll
                     for (int c = 0; c < kBN / 32; ++c)
 #pragma unroll
@@ -450,12 +449,23 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                             float t = __uint_as_float(sr[c][e]) * p.scale;
                             if (softcap) t = p.softcap * tanh_via_exp2(t * inv_cap);
                             if (alibi) t += abias + slope * (float)(c * 32 + e);
-                            if (qtile) {
-                                const int kc = key0 - ctx + c * 32 + e;
-                                if (kc >= 0 && kc <= hi - ctx) t += __ldg(qrow + kc);
-                            }
                             sr[c][e] = __float_as_uint(t * kLog2e);
                         }
+                    // Query-query bias, in its own pass so that the loop above
+                    // stays as lean without it: the query-section keys up to
+                    // the row's last visible key (so j - ctx < S_q), in log2
+                    // units like the scores it joins.
+                    if (QQ && qrow != nullptr && key0 + kBN > ctx && key0 <= hi) {
+#pragma unroll
+                        for (int c = 0; c < kBN / 32; ++c)
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) {
+                                const int kc = key0 - ctx + c * 32 + e;
+                                if (kc >= 0 && kc <= hi - ctx)
+                                    sr[c][e] = __float_as_uint(__uint_as_float(sr[c][e]) +
+                                                               __ldg(qrow + kc) * kLog2e);
+                            }
+                    }
                 }
                 if (!mask_free) {
 #pragma unroll
@@ -611,12 +621,12 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     }
 }
 
-template <int D, int NK, int NV, bool PLAIN>
+template <int D, int NK, int NV, bool PLAIN, bool QQ = false>
 cudaError_t launch_pair_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           const FwdParams& p, int pairs, cudaStream_t stream) {
     using C = PairCfg<D, NK, NV>;
     constexpr int kThreads = PR::kThreads;
-    auto kern = prefill_pair_kernel<D, NK, NV, PLAIN>;
+    auto kern = prefill_pair_kernel<D, NK, NV, PLAIN, QQ>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)(pairs * p.splits), (unsigned)p.hk, (unsigned)p.num_seqs);
@@ -630,12 +640,15 @@ bool prefill_pair_supported(int d) { return d == 64 || d == 128; }
 
 cudaError_t launch_prefill_pair(const CUtensorMap& tq, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                                 const FwdParams& p, int pairs, cudaStream_t stream) {
-    const bool plain = (p.flags & (UA_FLAG_SOFTCAP | UA_FLAG_ALIBI | UA_FLAG_QQ_BIAS)) == 0;
+    const bool qq = (p.flags & UA_FLAG_QQ_BIAS) != 0;
+    const bool plain = !qq && (p.flags & (UA_FLAG_SOFTCAP | UA_FLAG_ALIBI)) == 0;
     switch (p.d) {
         case 64:
+            if (qq) return launch_pair_t<64, 4, 4, false, true>(tq, tm_k, tm_v, p, pairs, stream);
             return plain ? launch_pair_t<64, 4, 4, true>(tq, tm_k, tm_v, p, pairs, stream)
                          : launch_pair_t<64, 4, 4, false>(tq, tm_k, tm_v, p, pairs, stream);
         case 128:
+            if (qq) return launch_pair_t<128, 2, 2, false, true>(tq, tm_k, tm_v, p, pairs, stream);
             return plain ? launch_pair_t<128, 2, 2, true>(tq, tm_k, tm_v, p, pairs, stream)
                          : launch_pair_t<128, 2, 2, false>(tq, tm_k, tm_v, p, pairs, stream);
         default: return cudaErrorInvalidValue;
