@@ -271,7 +271,6 @@ topk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             int32_t cur[4];
 #pragma unroll
             for (int k = 0; k < 4; ++k) cur[k] = nxt[k];
-            if (j + 1 < n_tiles) tile_rows(j + 1, nxt);
             if (j >= nst && !__all_sync(0xffffffffu, dwait(empty0 + 8 * stg, ((j / nst) + 1) & 1,
                                                            abort_flag, p.err)))
                 break;
@@ -290,6 +289,9 @@ topk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                         st_shared_zero16(dst);
                 }
             }
+            // The next tile's rows (a list load, then a dependent block-table
+            // load) are looked up while this tile's copies are in flight.
+            if (j + 1 < n_tiles) tile_rows(j + 1, nxt);
             cp_async_wait_all();
             fence_proxy_async_smem();   // the MMAs read these rows through the async proxy
             __syncwarp();
@@ -330,7 +332,6 @@ topk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             int32_t cur[4];
 #pragma unroll
             for (int k = 0; k < 4; ++k) cur[k] = nxt[k];
-            if (j + 1 < n_tiles) tile_rows(j + 1, nxt);
             if (!UA_TOPK_K_LSU) {
                 if (j >= NSK && !__all_sync(0xffffffffu, dwait(k_empty0 + 8 * stk, ((j / NSK) + 1) & 1,
                                                                abort_flag, p.err)))
@@ -354,6 +355,9 @@ topk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                                 pn * 64, cur[0], cur[1], cur[2], cur[3], v_full0 + 8 * stv);
             }
             issued = j + 1;
+            // The next tile's rows are looked up after this tile's gathers
+            // are on their way (in-order issue would otherwise hold them).
+            if (j + 1 < n_tiles) tile_rows(j + 1, nxt);
         }
         if (__any_sync(0xffffffffu, bad_block) && lane == 0) atomicOr(p.err, (int)UA_DEVERR_BLOCK_ID);
         if (*abort_flag && lane == 0) {
@@ -464,17 +468,25 @@ topk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
             rslope[r] = (!PLAIN && alibi && r < nrows) ? __ldg(p.alibi + hkv * g + r) : 0.f;
         }
         bool ok = true;
-        for (int j = 0; j < n_tiles; ++j) {
-            // The entry's listed position and whether it is a key of the row;
-            // loaded before the wait so the two dependent loads overlap it.
+        // The entry's listed position and whether it is a key of the row, one
+        // tile ahead: looked up after P of the previous tile is published, so
+        // the two dependent loads overlap the wait for the next S.
+        auto lookup = [&](int j, int& jp, bool& valid) {
             const int e = e_beg + j * kBN + t;
-            int jp = -1;
-            bool valid = false;
+            jp = -1;
+            valid = false;
             if (e < e_end) {
                 jp = __ldg(lst + e);
                 bool bad = false;
                 valid = cache_row(p, bt, jp, sk, hkv, bad) >= 0 && jp <= khi && jp >= klo;
             }
+        };
+        int jp_next;
+        bool valid_next;
+        lookup(0, jp_next, valid_next);
+        for (int j = 0; j < n_tiles; ++j) {
+            const int jp = jp_next;
+            const bool valid = valid_next;
             const bool got = __all_sync(0xffffffffu, dwait(s_full0 + 8 * (j & 1), (j >> 1) & 1,
                                                            abort_flag, p.err));
             float x[NR];
@@ -586,6 +598,7 @@ topk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                 tc::fence_before_sync();
                 mbar_arrive(p_full0 + 8 * (j & 1));
             }
+            if (j + 1 < n_tiles) lookup(j + 1, jp_next, valid_next);
         }
         // ------------------------------ epilogue ---------------------------------
         if (ok) {
