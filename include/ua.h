@@ -194,7 +194,7 @@ ua_status ua_forward(ua_problem *p, const void *q, const void *k_cache, const vo
  *   topk_len     int32 [total_q] device, list lengths in [0, topk_stride];
  *                a length outside it sets UA_DEVERR_BOUNDS and writes the
  *                token's rows as 0
- *   topk_stride  > 0, entries per list row
+ *   topk_stride  > 0, entries per list row (at most 2^30)
  * A listed key in a block whose id is out of range is dropped and sets
  * UA_DEVERR_BLOCK_ID.  Needs d = 128, 16 % g == 0, a bf16 cache, path AUTO
  * or DECODE_TC and num_blocks * b * H_k < 2^31 (else UA_ERR_UNSUPPORTED).

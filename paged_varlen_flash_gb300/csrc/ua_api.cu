@@ -492,6 +492,7 @@ ua_status ua_forward_topk(ua_problem* p, const void* q, const void* k_cache, con
                                 alibi_slopes, out, &fp, &skip);
     if (rs != UA_OK) return rs;
     if (topk_stride < 1) return UA_ERR_INVALID_ARG;
+    if (topk_stride > (1 << 30)) return UA_ERR_UNSUPPORTED;   // entry indices stay in int32
     if (skip) return UA_OK;
     if (!topk_idx || !topk_len) return UA_ERR_INVALID_ARG;
     const ua_problem_desc& d = p->desc;

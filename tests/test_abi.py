@@ -107,3 +107,9 @@ def test_noalloc_rejects_the_qq_bias_flag_before_any_device_work(lib):
                                ua.UA_FLAG_CAUSAL | ua.UA_FLAG_QQ_BIAS, None, None, None,
                                stream=0)
     assert st == 2
+
+
+def test_topk_entry_checks_its_handle_on_the_host(lib):
+    # No problem handle: rejected before any pointer is looked at.
+    assert ua.ua_forward_topk(None, None, None, None, None, None, None, 1, 1, 1, 1, None, None,
+                              16, ua.UA_FLAG_CAUSAL, None, None, None, stream=0) == 1

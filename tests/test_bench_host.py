@@ -88,3 +88,14 @@ def test_dominant_kernel_follows_the_reported_path():
     assert bench.dominant_kernel("tensor_core") == "prefill_kernel"
     assert bench.dominant_kernel("tensor_core_pair+combine") == "prefill_pair_kernel"
     assert bench.dominant_kernel("split_kv+combine") == "split_kernel"
+
+
+def test_workload_units_of_a_topk_workload_count_listed_keys():
+    w = W.make("decode_topk", values=False)
+    nbytes, flops = bench.workload_units(w)
+    listed = 256 * 2048
+    kv = listed * w.hk * w.d * 2 * 2
+    qo = 2 * w.total_q * w.hq * w.d * 2
+    meta = listed * 4 + w.total_q * 4 + (2 * w.num_seqs + 1) * 4
+    assert nbytes == kv + qo + meta
+    assert flops == 4.0 * w.d * w.hq * listed
