@@ -10,16 +10,19 @@
 //     S^T [128 listed keys x 16 rows] = K_gathered [128 x d] * Q^T [d x 16]
 //     O^T [d x 16 rows]              += V_gathered^T [d x 128] * P^T [128 x 16]
 //
-// The K and V tiles are gathered row by row with TMA tile::gather4 loads from
-// a 2-D view of each cache ([num_blocks * b * H_k rows, d columns], box = one
-// 128-byte panel of one row): a lane of the producer warp looks up four list
-// entries, maps each through the block table to its cache row and issues one
-// gather per 64-dim panel, so the 128 rows of a tile land in the same
-// swizzled layout a paged TMA box would give.  Entries that are not keys of
-// the row (padding, out of range, hidden by the causal mask or the window,
-// or in a bad block) gather row 0 instead, their scores are masked, and the
-// P.V issuer zeroes their V rows before the MMA (a masked weight of 0 times
-// whatever row 0 holds must stay 0).
+// The K and V tiles are gathered row by row into the same 128-byte-swizzled
+// panels a paged TMA box would give.  Each cache is viewed as a 2-D tensor
+// [num_blocks * b * H_k rows, d columns]; a lane maps four list entries
+// through the block table to their cache rows.  By default K comes through
+// TMA tile::gather4 (box = one 64-dim panel of one row, four rows per
+// instruction) and V through 16-byte cp.async from a second loader warp (one
+// warp instruction moves two 256-byte rows): the row requests an SM keeps in
+// flight bound this kernel, and the two paths draw on separate capacity.
+// Entries that are not keys of the row (padding, out of range, hidden by the
+// causal mask or the window, or in a bad block) have their scores masked;
+// their V rows are written as zeros (cp.async loader) or zeroed by the P.V
+// issuer before the MMA (gather4 loader, which fetches row 0 for them), since
+// a weight of 0 times stale data could still be NaN.
 //
 // The softmax is the decode kernel's: base 2, lazy re-anchor, fp32 (m, l),
 // P in bf16, O^T rescaled in tensor memory; the score chain (scale, softcap,
