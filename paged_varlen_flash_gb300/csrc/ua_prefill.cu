@@ -39,14 +39,6 @@
 #include "ua_tc.cuh"
 #include "ua_tmap.h"
 
-// Cluster size of the d = 256 kernel: 2 shares each K/V tile between two
-// CTAs on adjacent query tiles through TMA multicast.  Measured on the wide
-// MHA prefill it is slower than one CTA per tile (the coupled CTAs wait on
-// each other's releases), so 1 is the default.
-#ifndef UA_PF256_CL
-#define UA_PF256_CL 1
-#endif
-
 namespace ua {
 namespace {
 
@@ -78,15 +70,9 @@ struct PCfg {
     static_assert(kSmem <= 232448, "shared memory budget");
 };
 
-// CL = 2: the CTA is one of a cluster of two working on adjacent query tiles
-// of the same (sequence, KV head, segment).  Each CTA fetches half of every
-// K/V tile's head-dim panels and multicasts them to both, so each SM's copy
-// engine moves half the bytes per flop; a stage is reloaded only after both
-// CTAs' MMAs released it.  Both CTAs walk the union of their key ranges (a
-// row still masks keys outside its own range).
 // QQ: the query-query bias pass is compiled in (a separate instantiation, so
 // that the score loop of the other non-plain calls keeps its registers).
-template <int D, int BN, int NK, int NV, int SPLIT, bool PLAIN, int CL, bool QQ>
+template <int D, int BN, int NK, int NV, int SPLIT, bool PLAIN, bool QQ>
 __global__ void __launch_bounds__(Roles<SPLIT>::kThreads, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
@@ -105,39 +91,25 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     const int s = blockIdx.z;
     const int hkv = blockIdx.y;
     const bool split = p.splits > 1;             // write (m, l, o) partials per KV segment
-    static_assert(CL == 1 || CL == 2, "cluster size");
-    uint32_t rank = 0;
-    int seg, qt;
-    if constexpr (CL == 2) {
-        rank = cluster_ctarank();
-        const int cx = (int)(blockIdx.x >> 1);   // cluster index along x
-        const int npairs = (int)(gridDim.x >> 1) / p.splits;
-        seg = cx % p.splits;
-        qt = 2 * (npairs - 1 - cx / p.splits) + (int)rank;   // heaviest pairs first
-    } else {
-        seg = blockIdx.x % p.splits;
-        qt = (int)(gridDim.x / p.splits) - 1 - (int)(blockIdx.x / p.splits);  // heaviest first
-    }
+    const int seg = blockIdx.x % p.splits;
+    const int qt = (int)(gridDim.x / p.splits) - 1 - (int)(blockIdx.x / p.splits);  // heaviest first
     const int g = p.g;
     const int ppt = kRows / g;                  // positions per tile
     const int p0 = qt * ppt;
-    const int pc0 = (qt - (int)rank) * ppt;     // first position of the cluster's tiles
 
     int sq, sk;
     int64_t q0;
     const uint32_t st = seq_status(p, s, sq, sk, q0);
     if (st && qt == 0 && hkv == 0 && seg == 0 && threadIdx.x == 0) atomicOr(p.err, (int)st);
-    // Every early exit below is taken by both CTAs of a cluster or by neither.
     if (st & UA_DEVERR_CU_SEQLENS) return;
-    if (pc0 >= sq) return;
+    if (p0 >= sq) return;
     if (seg >= (split ? seq_segments(p, st, sk) : 1)) return;
-    const int p_last = min(p0 + ppt, sq) - 1;   // < p0: this tile lies past the sequence (CL = 2)
-    const int pc_last = min(pc0 + CL * ppt, sq) - 1;
+    const int p_last = min(p0 + ppt, sq) - 1;
     const int ctx = sk - sq;
     const bool causal = (p.flags & UA_FLAG_CAUSAL) != 0;
     const bool window = (p.flags & UA_FLAG_WINDOW) != 0;
-    int k_end = causal ? min(sk, pc_last + ctx + 1) : sk;
-    int k_beg = window ? max(0, pc0 + ctx - p.window + 1) : 0;
+    int k_end = causal ? min(sk, p_last + ctx + 1) : sk;
+    int k_beg = window ? max(0, p0 + ctx - p.window + 1) : 0;
     if (split) {  // this CTA's KV segment; segments are whole BN tiles
         k_beg = max(k_beg, seg * p.chunk);
         k_end = min(k_end, seg * p.chunk + p.chunk);
@@ -193,11 +165,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         mbar_init(B.q_full, 1);
         for (int i = 0; i < NK; ++i) {
             mbar_init(B.k_full0 + 8 * i, 1);
-            mbar_init(B.k_empty0 + 8 * i, CL);   // one release per CTA of the cluster
+            mbar_init(B.k_empty0 + 8 * i, 1);
         }
         for (int i = 0; i < NV; ++i) {
             mbar_init(B.v_full0 + 8 * i, 1);
-            mbar_init(B.v_empty0 + 8 * i, CL);
+            mbar_init(B.v_empty0 + 8 * i, 1);
         }
         mbar_init(B.s_full0, 1);
         mbar_init(B.s_full0 + 8, 1);
@@ -215,9 +187,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         tc::tmem_relinquish();
     }
     tc::fence_before_sync();
-    // With a cluster: no copy lands in, and no release arrives at, the peer
-    // before its barriers exist.
-    if constexpr (CL == 2) cluster_sync(); else __syncthreads();
+    __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
 
@@ -258,7 +228,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             const uint32_t bytes = (uint32_t)nb * b * 128 * C::kPanels;
             const int32_t id = id_next;
             if (j + 1 < n_tiles) id_next = tile_id(j + 1);
-            if (rank == 0 && lane < nb && (id < 0 || (int64_t)id >= p.num_blocks))
+            if (lane < nb && (id < 0 || (int64_t)id >= p.num_blocks))
                 atomicOr(p.err, (int)UA_DEVERR_BLOCK_ID);
             if (j >= NK && !__all_sync(0xffffffffu, wait_or_abort(B.k_empty0 + 8 * stk, ((j / NK) + 1) & 1,
                                                                    abort_flag, p.err)))
@@ -267,14 +237,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             __syncwarp();
             if (lane < nb) {
 #pragma unroll
-                for (int q = 0; q < C::kPanels / CL; ++q) {
-                    const int pn = (int)rank * (C::kPanels / CL) + q;
-                    const uint32_t dst = sK + stk * C::kKvBytes + pn * C::kKvPanel + lane * b * 128;
-                    if constexpr (CL == 2)
-                        tma_load_4d_mc(dst, &tm_k, pn * 64, hkv, 0, id, B.k_full0 + 8 * stk, 0x3);
-                    else
-                        tma_load_4d(dst, &tm_k, pn * 64, hkv, 0, id, B.k_full0 + 8 * stk);
-                }
+                for (int pn = 0; pn < C::kPanels; ++pn)
+                    tma_load_4d(sK + stk * C::kKvBytes + pn * C::kKvPanel + lane * b * 128, &tm_k,
+                                pn * 64, hkv, 0, id, B.k_full0 + 8 * stk);
             }
             if (j >= NV && !__all_sync(0xffffffffu, wait_or_abort(B.v_empty0 + 8 * stv, ((j / NV) + 1) & 1,
                                                                    abort_flag, p.err)))
@@ -283,14 +248,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             __syncwarp();
             if (lane < nb) {
 #pragma unroll
-                for (int q = 0; q < C::kPanels / CL; ++q) {
-                    const int pn = (int)rank * (C::kPanels / CL) + q;
-                    const uint32_t dst = sV + stv * C::kKvBytes + pn * C::kKvPanel + lane * b * 128;
-                    if constexpr (CL == 2)
-                        tma_load_4d_mc(dst, &tm_v, pn * 64, hkv, 0, id, B.v_full0 + 8 * stv, 0x3);
-                    else
-                        tma_load_4d(dst, &tm_v, pn * 64, hkv, 0, id, B.v_full0 + 8 * stv);
-                }
+                for (int pn = 0; pn < C::kPanels; ++pn)
+                    tma_load_4d(sV + stv * C::kKvBytes + pn * C::kKvPanel + lane * b * 128, &tm_v,
+                                pn * 64, hkv, 0, id, B.v_full0 + 8 * stv);
             }
             issued = j + 1;
         }
@@ -332,13 +292,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                         tc::mma_bf16(dS, a, bdesc, idesc_qk, k > 0 ? 1u : 0u);
                     }
                     tc::commit(B.s_full0 + 8 * (j & 1));
-                    if constexpr (CL == 2) {
-                        // Release the stage in both CTAs (only if it is reloaded:
-                        // no arrival may be in flight to a CTA that has finished).
-                        if (j + NK < n_tiles) tc::commit_mc(B.k_empty0 + 8 * stg, 0x3);
-                    } else {
-                        tc::commit(B.k_empty0 + 8 * stg);
-                    }
+                    tc::commit(B.k_empty0 + 8 * stg);
                 }
                 __syncwarp();
             }
@@ -374,11 +328,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                         tc::mma_bf16_ts(dO, aP + k * 8, bdesc, idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
                     }
                     tc::commit(B.o_done + 8 * (j % 3));
-                    if constexpr (CL == 2) {
-                        if (j + NV < n_tiles) tc::commit_mc(B.v_empty0 + 8 * stg, 0x3);
-                    } else {
-                        tc::commit(B.v_empty0 + 8 * stg);
-                    }
+                    tc::commit(B.v_empty0 + 8 * stg);
                 }
                 __syncwarp();
             }
@@ -649,40 +599,24 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     }
 
     tc::fence_before_sync();
-    // With a cluster: neither CTA leaves while the other may still write into
-    // its shared memory.
-    if constexpr (CL == 2) cluster_sync(); else __syncthreads();
+    __syncthreads();
     if (warp == kWarpMma) {
         tc::fence_after_sync();
         tc::tmem_dealloc(tmem, kTmemCols);
     }
 }
 
-template <int D, int BN, int NK, int NV, int SPLIT, bool PLAIN, int CL, bool QQ = false>
+template <int D, int BN, int NK, int NV, int SPLIT, bool PLAIN, bool QQ = false>
 cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                      const FwdParams& p, int tiles, cudaStream_t stream) {
     using C = PCfg<D, BN, NK, NV, SPLIT>;
     constexpr int kThreads = Roles<SPLIT>::kThreads;
-    auto kern = prefill_kernel<D, BN, NK, NV, SPLIT, PLAIN, CL, QQ>;
+    auto kern = prefill_kernel<D, BN, NK, NV, SPLIT, PLAIN, QQ>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
-    // With clusters of two, grid x holds (pair, segment, rank); an odd tile
-    // count leaves the last pair's second tile empty (it still fetches its
-    // half of each K/V tile).
-    const int units = CL == 2 ? (tiles + 1) / 2 * 2 : tiles;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(units * p.splits), (unsigned)p.hk, (unsigned)p.num_seqs);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = C::kSmem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = CL;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, p);
+    dim3 grid((unsigned)(tiles * p.splits), (unsigned)p.hk, (unsigned)p.num_seqs);
+    kern<<<grid, kThreads, C::kSmem, stream>>>(tq, tk, tv, p);
+    return cudaGetLastError();
 }
 
 }  // namespace
@@ -738,9 +672,9 @@ cudaError_t launch_prefill(const PrefillPlan& plan, const CUtensorMap& tm_k, con
     const bool qq = (p.flags & UA_FLAG_QQ_BIAS) != 0;
     const bool plain = !qq && (p.flags & (UA_FLAG_SOFTCAP | UA_FLAG_ALIBI)) == 0;
     if (p.d != 256) return cudaErrorInvalidValue;
-    if (qq) return launch_t<256, 64, 2, 2, 2, false, UA_PF256_CL, true>(tq, tm_k, tm_v, p, plan.num_tiles, stream);
-    return plain ? launch_t<256, 64, 2, 2, 2, true, UA_PF256_CL>(tq, tm_k, tm_v, p, plan.num_tiles, stream)
-                 : launch_t<256, 64, 2, 2, 2, false, UA_PF256_CL>(tq, tm_k, tm_v, p, plan.num_tiles, stream);
+    if (qq) return launch_t<256, 64, 2, 2, 2, false, true>(tq, tm_k, tm_v, p, plan.num_tiles, stream);
+    return plain ? launch_t<256, 64, 2, 2, 2, true>(tq, tm_k, tm_v, p, plan.num_tiles, stream)
+                 : launch_t<256, 64, 2, 2, 2, false>(tq, tm_k, tm_v, p, plan.num_tiles, stream);
 }
 
 }  // namespace ua

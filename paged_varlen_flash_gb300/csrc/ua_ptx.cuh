@@ -95,31 +95,6 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* tmap, int3
         : "memory");
 }
 
-// 4-D tiled load multicast to the CTAs of this cluster in `cta_mask`: the box
-// lands at the same shared-memory offset in each, and each one's mbarrier at
-// offset `bar` receives the bytes that landed there.
-__device__ __forceinline__ void tma_load_4d_mc(uint32_t dst, const void* tmap, int32_t c0, int32_t c1,
-                                               int32_t c2, int32_t c3, uint32_t bar, uint16_t cta_mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        ".multicast::cluster [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar),
-        "h"(cta_mask)
-        : "memory");
-}
-
-// ---- thread-block clusters ----------------------------------------------------
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-// Every thread of every CTA in the cluster arrives, then waits for all.
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int32_t c0, int32_t c1,
                                             int32_t c2, uint32_t bar) {
     asm volatile(

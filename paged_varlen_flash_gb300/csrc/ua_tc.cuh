@@ -75,16 +75,6 @@ __device__ __forceinline__ void commit(uint32_t bar) {
         : "memory");
 }
 
-// Same, arriving on the mbarrier at offset `bar` of every CTA of the cluster
-// in `cta_mask`.
-__device__ __forceinline__ void commit_mc(uint32_t bar, uint16_t cta_mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-        " [%0], %1;" ::"r"(bar),
-        "h"(cta_mask)
-        : "memory");
-}
-
 // ---- tensor memory <-> registers (32 lanes x 32 consecutive columns) --------
 __device__ __forceinline__ void ld32(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile(
