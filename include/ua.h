@@ -96,11 +96,12 @@ enum { UA_DTYPE_BF16 = 0, UA_DTYPE_FP8_E4M3 = 1 };
  * the device versus split-KV segments plus a reduction).
  *   SPLIT_KV     CUDA-core split-KV kernel + combine, any shape.
  *   TENSOR_CORE  tcgen05 kernel over tiles of 128 packed (position, head)
- *                rows, KV-split + combine when the tile grid is small;
- *                needs 128 % g == 0.
+ *                rows (floor(128 / g) positions of the g heads of one KV
+ *                head), KV-split + combine when the tile grid is small;
+ *                needs g <= 128.
  *   DECODE_TC    tcgen05 kernel with the keys on the MMA M dimension for
- *                calls with at most 16 packed rows per KV head; needs d = 128,
- *                16 % g == 0 and g * max_seqlen_q <= 16.
+ *                calls with at most 16 packed rows per KV head; needs d = 128
+ *                and g * max_seqlen_q <= 16.
  *   AUTO         DECODE_TC when it applies, else TENSOR_CORE when it applies
  *                and a KV head has more than 16 packed rows, else SPLIT_KV.
  * A forced path that does not apply returns UA_ERR_UNSUPPORTED. */
@@ -159,7 +160,8 @@ ua_status ua_problem_create(const ua_problem_desc *desc, ua_problem **out);
  * Forward pass, enqueued on `stream` (a cudaStream_t; NULL = legacy default
  * stream), without host synchronisation.
  *
- * num_seqs <= max_num_seqs; total_q = cu_seqlens_q[num_seqs] <= max_total_q;
+ * num_seqs <= max_num_seqs and num_seqs <= 65535 (else UA_ERR_UNSUPPORTED);
+ * total_q = cu_seqlens_q[num_seqs] <= max_total_q;
  * max_seqlen_q / max_seqlen_k are host-side upper bounds on S_q(s) / S_k(s)
  * used to size the launch (the device checks them and reports
  * UA_DEVERR_BOUNDS).  `flags` must be a subset of the problem's flags;
@@ -196,7 +198,7 @@ ua_status ua_forward(ua_problem *p, const void *q, const void *k_cache, const vo
  *                token's rows as 0
  *   topk_stride  > 0, entries per list row (at most 2^30)
  * A listed key in a block whose id is out of range is dropped and sets
- * UA_DEVERR_BLOCK_ID.  Needs d = 128, 16 % g == 0, a bf16 cache, path AUTO
+ * UA_DEVERR_BLOCK_ID.  Needs d = 128, g <= 16, a bf16 cache, path AUTO
  * or DECODE_TC and num_blocks * b * H_k < 2^31 (else UA_ERR_UNSUPPORTED).
  * The lists are split into segments of 128-entry tiles per token (one CTA
  * each, merged by the combine kernel), counted from each token's own length.
@@ -294,10 +296,18 @@ ua_status ua_set_profile_events(ua_problem *p, void *ev_begin, void *ev_end);
  * a word inside the static array, cleared at the start of each call, and are
  * not reported.
  *
- * The first call on a device resolves the array's address (once per device);
- * make that first call before any stream capture.  All calls on a device share
- * the array and leave their partials in it: calls whose kernels may overlap on
- * the GPU race on it and must be ordered by the caller.
+ * The first call in a CUDA context resolves the array's address in that
+ * context (once per context; a caller that switches contexts on one device
+ * gets each context's own address); make that first call before any stream
+ * capture.  All calls on a device share the array and leave their partials in
+ * it: calls whose kernels may overlap on the GPU race on it and must be
+ * ordered by the caller.
+ *
+ * desc->path must be UA_PATH_AUTO or UA_PATH_SPLIT_KV (this entry point runs
+ * the split kernel only; TENSOR_CORE or DECODE_TC return UA_ERR_UNSUPPORTED,
+ * a value past UA_PATH_DECODE_TC UA_ERR_INVALID_ARG); desc->max_num_seqs and
+ * desc->max_total_q are not used.  num_seqs above 65535 returns
+ * UA_ERR_UNSUPPORTED.
  */
 ua_status ua_forward_noalloc(const ua_problem_desc *desc, const void *q, const void *k_cache,
                              const void *v_cache, const int32_t *block_table,

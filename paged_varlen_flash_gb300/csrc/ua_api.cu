@@ -16,6 +16,7 @@
 #include "ua_decode_tc.h"
 #include "ua_prefill.h"
 #include "ua_split.h"
+#include "ua_tmap.h"
 #include "ua_topk.h"
 
 namespace {
@@ -29,44 +30,10 @@ void note_cuda(cudaError_t e, const char* where) {
 constexpr int kMaxSplits = 64;
 constexpr size_t kWorkspaceCap = size_t(128) << 20;  // bytes of split partials
 
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
-                                             cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    });
-    return fn;
-}
-
-// 4-D map over a paged cache [num_blocks, b, H_k, d] (innermost first:
-// d, H_k, b, num_blocks) with a box of 64 head-dim elements (one 128-byte
-// swizzle panel), one KV head and `box_rows` consecutive slots of one block.
-// Addresses are formed by the TMA unit in 64 bits, so caches beyond 2 GiB need
-// no special path (the overflow hazard described in gfx950 section 7.2).
-// Tensor map of a paged cache [num_blocks, b, H_k, d]; a box is one
-// 128-byte swizzle panel (64 bf16 or 128 fp8 elements) x 1 head x box_rows
-// slots x 1 block.
+// Cache map of the problem's caches with boxes of `box_rows` slots.
 bool encode_cache_map(CUtensorMap* m, const void* base, const ua_problem_desc& d, int box_rows) {
-    auto enc = tensor_map_encoder();
-    if (!enc) return false;
-    const bool fp8 = d.kv_dtype == UA_DTYPE_FP8_E4M3;
-    const cuuint64_t es = fp8 ? 1 : 2;
-    cuuint64_t dims[4] = {(cuuint64_t)d.head_size, (cuuint64_t)d.num_kv_heads,
-                          (cuuint64_t)d.block_size, (cuuint64_t)d.num_blocks};
-    cuuint64_t strides[3] = {es * d.head_size, es * d.head_size * d.num_kv_heads,
-                             es * d.head_size * d.num_kv_heads * d.block_size};
-    cuuint32_t box[4] = {(cuuint32_t)(128 / es), 1, (cuuint32_t)box_rows, 1};
-    cuuint32_t estr[4] = {1, 1, 1, 1};
-    CUresult r = enc(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
-                     const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
+    return ua::encode_cache_map(m, base, d.head_size, d.num_kv_heads, d.block_size, d.num_blocks,
+                                d.kv_dtype == UA_DTYPE_FP8_E4M3, box_rows);
 }
 
 int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
@@ -267,6 +234,7 @@ ua_status prepare_call(ua_problem* p, const void* q, const void* k_cache, const 
         *skip = true;
         return UA_OK;
     }
+    if (num_seqs > 65535) return UA_ERR_UNSUPPORTED;   // grids index sequences on gridDim.z
     if (!q || !k_cache || !v_cache || !block_table || !cu_seqlens_q || !seqused_k || !out)
         return UA_ERR_INVALID_ARG;
     auto misaligned = [](const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) != 0; };

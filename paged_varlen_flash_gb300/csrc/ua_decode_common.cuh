@@ -1,7 +1,7 @@
 // ua_decode_common.cuh -- device helpers shared by the transposed decode
 // kernels (keys on the MMA M dimension, 16 packed rows on N): bounded mbarrier
 // waits that honour the CTA abort flag, a vote barrier, 16-column tensor
-// memory loads and stores, a warp max and tanh from exp2.
+// memory loads and stores and a warp max.
 #pragma once
 
 #include <cstdint>
@@ -71,12 +71,6 @@ __device__ __forceinline__ float warp_max_f32(float v) {
     int r;
     asm volatile("redux.sync.max.s32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(key));
     return __int_as_float(r >= 0 ? r : (r ^ 0x7fffffff));
-}
-
-__device__ __forceinline__ float tanh_e2(float x) {
-    // tanh(x) = 1 - 2 / (e^{2x} + 1)
-    const float e = fast_exp2(x * (2.0f * kLog2e));
-    return 1.0f - __fdividef(2.0f, e + 1.0f);
 }
 
 }  // namespace ua

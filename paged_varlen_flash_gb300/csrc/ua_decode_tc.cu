@@ -225,7 +225,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             tma_prefetch_desc(&tm_q);
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
-            mbar_arrive_expect_tx(q_full, C::kQBytes);
+            // g heads x floor(16 / g) positions per panel
+            mbar_arrive_expect_tx(q_full, (uint32_t)(g * (kN / g)) * 128u * C::kPanels);
 #pragma unroll
             for (int pn = 0; pn < C::kPanels; ++pn)
                 tma_load_3d(sQ + pn * C::kQPanel, &tm_q, pn * 64, hkv * g, (int)q0, q_full);
@@ -494,7 +495,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         v = __uint_as_float(sv[r]) * sl2;
                     } else {
                         float tt = __uint_as_float(sv[r]) * tau;
-                        if (softcap) tt = p.softcap * tanh_e2(tt / p.softcap);
+                        if (softcap) tt = p.softcap * tanh_from_exp2(tt / p.softcap);
                         if (alibi) tt += rslope[r] * (float)(key - ctx);
                         // Query section of row r (position r / g); keys past
                         // the row's last visible key read nothing.
@@ -661,8 +662,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 }  // namespace
 
 bool decode_tc_shape_ok(const FwdParams& p) {
-    return p.d == kD && p.g >= 1 && p.g <= kN && (kN % p.g) == 0 &&
-           (int64_t)p.g * p.max_seqlen_q <= kN;
+    return p.d == kD && p.g >= 1 && p.g <= kN && (int64_t)p.g * p.max_seqlen_q <= kN;
 }
 
 void plan_decode_tc(const FwdParams& p, int num_sms, size_t workspace_bytes, DecodePlan* plan) {
@@ -710,7 +710,8 @@ cudaError_t launch_decode_t(const CUtensorMap& tq, const CUtensorMap& tm_k, cons
 
 cudaError_t launch_decode_tc(const DecodePlan& plan, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                              const FwdParams& p, cudaStream_t stream) {
-    // Q map: [total_q, H_q, d]; box = 64 dims x g heads x 16/g positions = 16 rows.
+    // Q map: [total_q, H_q, d]; box = 64 dims x g heads x floor(16/g) positions
+    // (16 rows when g divides 16; the rows past g * S_q are padding).
     CUtensorMap tq;
     cuuint64_t dims[3] = {(cuuint64_t)p.d, (cuuint64_t)p.hq, (cuuint64_t)p.total_q};
     cuuint64_t strides[2] = {2ull * p.d, 2ull * p.d * p.hq};

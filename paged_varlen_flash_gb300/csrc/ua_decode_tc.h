@@ -12,7 +12,7 @@ struct DecodePlan {
     int launches = 0;      // kernels enqueued per call
 };
 
-// True when the call fits the kernel: d = 128, g divides 16 and every KV head
+// True when the call fits the kernel: d = 128, g <= 16 and every KV head
 // has at most 16 packed query rows (g * max_seqlen_q <= 16).
 bool decode_tc_shape_ok(const FwdParams& p);
 

@@ -19,9 +19,12 @@
 // partials' address differs.
 //
 // Rules that follow from a single shared array:
-//  * The first call on a device resolves the array's device address with
-//    cudaGetSymbolAddress (once per device, with that device current).  Make
-//    that first call before any stream capture begins.
+//  * The first call in a CUDA context resolves the array's device address in
+//    that context with cudaGetSymbolAddress (once per context: the address
+//    is cached under the context's process-unique id, so a caller that makes
+//    another context current on the same device gets that context's own
+//    address, never a stale one).  Make that first call before any stream
+//    capture begins.
 //  * Every call on a device uses the same array and leaves its contents
 //    behind; the error word is cleared at the start of each call.  Calls whose
 //    kernels overlap on the GPU (different streams, no ordering between them)
@@ -35,60 +38,71 @@
 
 #include "ua_common.cuh"
 #include "ua_split.h"
+#include "ua_tmap.h"
 
 namespace {
 
 // Scratch capacity: 16 MiB of fp32 partials, plus the error word.
 constexpr size_t kScratchBytes = size_t(16) << 20;
-constexpr int kMaxDevices = 64;
+constexpr int kMaxContexts = 64;
 constexpr int kMaxSplitsNoAlloc = 64;
 
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes + 256];
 
+// Driver entry points, reached through the runtime (no -lcuda link).
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+template <typename F>
+F driver_fn(const char* name) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion(name, &ptr, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+        return nullptr;
+    return reinterpret_cast<F>(ptr);
+}
+
 std::mutex g_setup_mutex;
-void* g_scratch_addr[kMaxDevices] = {};
+struct ScratchEntry {
+    unsigned long long ctx_id;
+    void* addr;
+};
+ScratchEntry g_scratch_addr[kMaxContexts];
+int g_num_scratch = 0;
 
-// Device address of g_scratch on `device` (the current device); resolved once.
-cudaError_t scratch_address(int device, void** out) {
+// Id of the context current on this thread (0 and false if none or unknown).
+bool current_context_id(unsigned long long* id) {
+    static CtxGetCurrentFn get_current = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent");
+    static CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId");
+    if (!get_current || !get_id) return false;
+    CUcontext ctx = nullptr;
+    if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
+    return get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// Device address of g_scratch in the current context (the runtime makes the
+// device's primary context current if no context is); resolved once per
+// context.
+cudaError_t scratch_address(void** out) {
     std::lock_guard<std::mutex> lock(g_setup_mutex);
-    if (!g_scratch_addr[device]) {
-        void* ptr = nullptr;
-        cudaError_t e = cudaGetSymbolAddress(&ptr, g_scratch);
-        if (e != cudaSuccess) return e;
-        g_scratch_addr[device] = ptr;
+    unsigned long long id = 0;
+    bool have_id = current_context_id(&id);
+    if (have_id) {
+        for (int i = 0; i < g_num_scratch; ++i)
+            if (g_scratch_addr[i].ctx_id == id) {
+                *out = g_scratch_addr[i].addr;
+                return cudaSuccess;
+            }
     }
-    *out = g_scratch_addr[device];
+    void* ptr = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&ptr, g_scratch);
+    if (e != cudaSuccess) return e;
+    // The runtime call above binds a context if none was current.
+    if (!have_id) have_id = current_context_id(&id);
+    if (have_id && g_num_scratch < kMaxContexts) g_scratch_addr[g_num_scratch++] = {id, ptr};
+    *out = ptr;
     return cudaSuccess;
-}
-
-PFN_cuTensorMapEncodeTiled_v12000 encoder() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
-                                             cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    });
-    return fn;
-}
-
-// Map over a paged cache [num_blocks, b, H_k, d]: 64-element, 16-slot boxes
-// with the 128-byte swizzle the split kernel reads.
-bool encode_map(CUtensorMap* m, const void* base, const ua_problem_desc& d) {
-    auto enc = encoder();
-    if (!enc) return false;
-    cuuint64_t dims[4] = {(cuuint64_t)d.head_size, (cuuint64_t)d.num_kv_heads,
-                          (cuuint64_t)d.block_size, (cuuint64_t)d.num_blocks};
-    cuuint64_t strides[3] = {2ull * d.head_size, 2ull * d.head_size * d.num_kv_heads,
-                             2ull * d.head_size * d.num_kv_heads * d.block_size};
-    cuuint32_t box[4] = {64, 1, 16, 1};
-    cuuint32_t estr[4] = {1, 1, 1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
-               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 int cdiv(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
@@ -110,6 +124,10 @@ extern "C" ua_status ua_forward_noalloc(const ua_problem_desc* d, const void* q,
         d->num_blocks <= 0 || d->max_blocks_per_seq <= 0 || (d->flags & ~known) ||
         !(d->scale > 0.f) || !std::isfinite(d->scale))
         return UA_ERR_INVALID_ARG;
+    if (d->path > UA_PATH_DECODE_TC) return UA_ERR_INVALID_ARG;
+    // This entry point runs the split kernel only: a description that forces
+    // another kernel family is refused rather than silently served by it.
+    if (d->path != UA_PATH_AUTO && d->path != UA_PATH_SPLIT_KV) return UA_ERR_UNSUPPORTED;
     if (d->flags & UA_FLAG_QQ_BIAS) return UA_ERR_UNSUPPORTED;   // the bias is bound to a ua_problem
     if (d->split_partials != UA_PARTIALS_F32 && d->split_partials != UA_PARTIALS_BF16)
         return UA_ERR_INVALID_ARG;
@@ -131,6 +149,7 @@ extern "C" ua_status ua_forward_noalloc(const ua_problem_desc* d, const void* q,
         (((flags & UA_FLAG_ALIBI) != 0) != (alibi_slopes != nullptr)))
         return UA_ERR_INVALID_ARG;
     if (num_seqs == 0 || total_q == 0) return UA_OK;
+    if (num_seqs > 65535) return UA_ERR_UNSUPPORTED;   // one grid row of CTAs per sequence
     if (!q || !k_cache || !v_cache || !block_table || !cu_seqlens_q || !seqused_k || !out)
         return UA_ERR_INVALID_ARG;
     auto misaligned = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; };
@@ -147,16 +166,20 @@ extern "C" ua_status ua_forward_noalloc(const ua_problem_desc* d, const void* q,
     int device = 0;
     cudaError_t e = cudaGetDevice(&device);
     if (e != cudaSuccess) return UA_ERR_CUDA;
-    if (device < 0 || device >= kMaxDevices) return UA_ERR_UNSUPPORTED;
     int num_sms = 0;
     e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, device);
     if (e != cudaSuccess) return UA_ERR_CUDA;
     void* scratch = nullptr;
-    e = scratch_address(device, &scratch);
+    e = scratch_address(&scratch);
     if (e != cudaSuccess) return UA_ERR_CUDA;
 
     CUtensorMap tk, tv;
-    if (!encode_map(&tk, k_cache, *d) || !encode_map(&tv, v_cache, *d)) return UA_ERR_CUDA;
+    // 16-slot boxes with the 128-byte swizzle the split kernel reads.
+    if (!ua::encode_cache_map(&tk, k_cache, d->head_size, d->num_kv_heads, d->block_size,
+                              d->num_blocks, false, 16) ||
+        !ua::encode_cache_map(&tv, v_cache, d->head_size, d->num_kv_heads, d->block_size,
+                              d->num_blocks, false, 16))
+        return UA_ERR_CUDA;
 
     const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     int32_t* err = device_error ? device_error

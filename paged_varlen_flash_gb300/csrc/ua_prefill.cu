@@ -204,7 +204,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             tma_prefetch_desc(&tm_q);
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
-            mbar_arrive_expect_tx(B.q_full, C::kQBytes);
+            // g heads x ppt positions per panel (rows past g * ppt are padding)
+            mbar_arrive_expect_tx(B.q_full, (uint32_t)(g * ppt) * 128u * C::kPanels);
 #pragma unroll
             for (int pn = 0; pn < C::kPanels; ++pn)
                 tma_load_3d(sQ + pn * C::kQPanel, &tm_q, pn * 64, hkv * g, (int)(q0 + p0), B.q_full);
@@ -399,7 +400,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 #pragma unroll
                         for (int e = 0; e < 32; ++e) {
                             float t = __uint_as_float(sr[c][e]) * p.scale;
-                            if (softcap) t = p.softcap * tanh_via_exp2(t * inv_cap);
+                            if (softcap) t = p.softcap * tanh_from_exp2(t * inv_cap);
                             if (alibi) t += abias + slope * (float)(c * 32 + e);
                             sr[c][e] = __float_as_uint(t * kLog2e);
                         }
@@ -654,13 +655,15 @@ void plan_prefill(const FwdParams& p, int num_sms, size_t workspace_bytes, Prefi
 }
 
 bool prefill_shape_ok(const FwdParams& p) {
-    return prefill_supported(p.d) && p.g >= 1 && p.g <= kRows && (kRows % p.g) == 0;
+    // A tile holds floor(128 / g) positions of all g heads of one KV head;
+    // when g does not divide 128 the last 128 mod g rows are padding.
+    return prefill_supported(p.d) && p.g >= 1 && p.g <= kRows;
 }
 
 cudaError_t launch_prefill(const PrefillPlan& plan, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                            const FwdParams& p, cudaStream_t stream) {
     // Q map: [total_q, H_q, d] innermost first; box = one 64-wide panel x g heads
-    // x 128/g positions, i.e. exactly the tile's 128 packed rows.
+    // x floor(128/g) positions: the tile's packed rows (all 128 when g divides 128).
     CUtensorMap tq;
     cuuint64_t dims[3] = {(cuuint64_t)p.d, (cuuint64_t)p.hq, (cuuint64_t)p.total_q};
     cuuint64_t strides[2] = {2ull * p.d, 2ull * p.d * p.hq};

@@ -17,7 +17,7 @@ struct PrefillPlan {
 bool prefill_supported(int d);
 
 // True when the call's shape fits the tensor-core tile (128 packed rows hold
-// whole GQA groups: g divides 128).
+// floor(128 / g) positions of whole GQA groups: g <= 128).
 bool prefill_shape_ok(const FwdParams& p);
 
 // Fill *plan for the call described by p; split partials may use up to

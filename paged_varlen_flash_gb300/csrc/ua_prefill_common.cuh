@@ -1,7 +1,7 @@
 // ua_prefill_common.cuh -- device helpers shared by the tensor-core prefill
 // kernels: warp roles, bounded mbarrier waits that honour the CTA's abort
 // flag, packed fp32 arithmetic, the base-2 exponential of a pair, a named
-// barrier with an AND vote, and tanh through exp2.
+// barrier with an AND vote.
 #pragma once
 
 #include <cstdint>
@@ -102,12 +102,6 @@ __device__ __forceinline__ bool bar_and_sync(int id, int count, bool pred) {
         : "r"((uint32_t)pred), "r"(id), "r"(count)
         : "memory");
     return r != 0;
-}
-
-__device__ __forceinline__ float tanh_via_exp2(float x) {
-    // tanh(x) = 1 - 2 / (e^{2x} + 1)
-    const float e = fast_exp2(x * (2.0f * kLog2e));
-    return 1.0f - __fdividef(2.0f, e + 1.0f);
 }
 
 }  // namespace pf

@@ -221,7 +221,10 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             tma_prefetch_desc(&tm_q);
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
-            mbar_arrive_expect_tx(q_full, (has_b ? 2u : 1u) * C::kQTile);
+            // One box per panel and tile: g heads x ppt positions = g * ppt
+            // rows (128 when g divides 128; the rows past them are padding
+            // whose outputs are never stored).
+            mbar_arrive_expect_tx(q_full, (has_b ? 2u : 1u) * (uint32_t)(g * ppt) * 128u * C::kPanels);
 #pragma unroll
             for (int pn = 0; pn < C::kPanels; ++pn) {
                 tma_load_3d(sQ + pn * C::kQPanel, &tm_q, pn * 64, hkv * g, (int)(q0 + p0), q_full);
@@ -447,7 +450,7 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
 #pragma unroll
                         for (int e = 0; e < 32; ++e) {
                             float t = __uint_as_float(sr[c][e]) * p.scale;
-                            if (softcap) t = p.softcap * tanh_via_exp2(t * inv_cap);
+                            if (softcap) t = p.softcap * tanh_from_exp2(t * inv_cap);
                             if (alibi) t += abias + slope * (float)(c * 32 + e);
                             sr[c][e] = __float_as_uint(t * kLog2e);
                         }

@@ -62,14 +62,6 @@ __device__ __forceinline__ float dot8(const float* q, uint4 k) {
     return a;
 }
 
-// tanh from its exponential form, tanh(x) = 1 - 2 / (e^{2x} + 1), with the
-// hardware base-2 exponential; relative error a few fp32 ulps away from 0 and
-// absolute error ~1e-7 near 0, far below the bf16 output resolution.
-__device__ __forceinline__ float tanh_exp2(float x) {
-    float e = fast_exp2(x * (2.0f * kLog2e));
-    return 1.0f - __fdividef(2.0f, e + 1.0f);
-}
-
 template <int D, int ROWS, bool SPLIT>
 __global__ void __launch_bounds__(kWarps * 32)
 split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -251,7 +243,7 @@ split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
             float x2;
             if (softcap || alibi || qq) {
                 float t = acc[r] * p.scale;
-                if (softcap) t = p.softcap * tanh_exp2(t / p.softcap);
+                if (softcap) t = p.softcap * tanh_from_exp2(t / p.softcap);
                 if (alibi) t += __ldg(p.alibi + row_h[r]) * (float)(j - ctx);
                 // Query section only; row_hi < S_k keeps j - ctx < S_q, and
                 // padding rows (row_hi = -1) read nothing.

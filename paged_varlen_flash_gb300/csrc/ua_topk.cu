@@ -245,7 +245,7 @@ topk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         const bool is_k = warp == kWarpTma;
         if (is_k && lane == 0) {
             tma_prefetch_desc(&tm_q);
-            mbar_arrive_expect_tx(q_full, C::kQBytes);
+            mbar_arrive_expect_tx(q_full, (uint32_t)g * 128u * C::kPanels);   // the token's g rows
 #pragma unroll
             for (int pn = 0; pn < C::kPanels; ++pn)
                 tma_load_3d(sQ + pn * C::kQPanel, &tm_q, pn * 64, hkv * g, (int)token, q_full);
@@ -313,7 +313,7 @@ topk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
         }
         if (!UA_TOPK_K_LSU && lane == 0) {
             tma_prefetch_desc(&tm_q);
-            mbar_arrive_expect_tx(q_full, C::kQBytes);
+            mbar_arrive_expect_tx(q_full, (uint32_t)g * 128u * C::kPanels);   // the token's g rows
 #pragma unroll
             for (int pn = 0; pn < C::kPanels; ++pn)
                 tma_load_3d(sQ + pn * C::kQPanel, &tm_q, pn * 64, hkv * g, (int)token, q_full);
@@ -505,7 +505,7 @@ topk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CU
                         v = __uint_as_float(sv[r]) * sl2;
                     } else {
                         float tt = __uint_as_float(sv[r]) * p.scale;
-                        if (softcap) tt = p.softcap * tanh_e2(tt / p.softcap);
+                        if (softcap) tt = p.softcap * tanh_from_exp2(tt / p.softcap);
                         if (alibi) tt += rslope[r] * (float)(jp - ctx);
                         if (qrow && valid && jp >= ctx) tt += __ldg(qrow + (jp - ctx));
                         v = tt * kLog2e;
@@ -686,7 +686,7 @@ cudaError_t launch_topk_t(const CUtensorMap& tq, const CUtensorMap& tm_k, const 
 }  // namespace
 
 bool topk_shape_ok(const FwdParams& p) {
-    return p.d == kD && p.g >= 1 && p.g <= kN && (kN % p.g) == 0 && p.topk_stride >= 1 &&
+    return p.d == kD && p.g >= 1 && p.g <= kN && p.topk_stride >= 1 &&
            p.total_q <= 0x7fffffffLL;
 }
 
@@ -724,12 +724,13 @@ void plan_topk(const FwdParams& p, int num_sms, size_t workspace_bytes, TopkPlan
 
 cudaError_t launch_topk(const TopkPlan& plan, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                         const FwdParams& p, cudaStream_t stream) {
-    // Q map: [total_q, H_q, d]; box = 64 dims x g heads x 16/g positions (the
-    // token's g rows first; the rest are padding the MMAs compute and nobody reads).
+    // Q map: [total_q, H_q, d]; box = 64 dims x g heads x 1 position (the
+    // token's g rows; the other rows of the 16-row tile are padding that the
+    // MMAs compute and nobody reads).
     CUtensorMap tq;
     cuuint64_t dims[3] = {(cuuint64_t)p.d, (cuuint64_t)p.hq, (cuuint64_t)p.total_q};
     cuuint64_t strides[2] = {2ull * p.d, 2ull * p.d * p.hq};
-    cuuint32_t box[3] = {64, (cuuint32_t)p.g, (cuuint32_t)(kN / p.g)};
+    cuuint32_t box[3] = {64, (cuuint32_t)p.g, 1};
     if (!encode_bf16_sw128(&tq, p.q, 3, dims, strides, box)) return cudaErrorInvalidValue;
     return launch_topk_t<UA_TOPK_NSK, UA_TOPK_NSV>(tq, tm_k, tm_v, p, plan, stream);
 }

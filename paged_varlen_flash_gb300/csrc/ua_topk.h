@@ -11,7 +11,7 @@ struct TopkPlan {
     int launches = 0;  // kernels enqueued per call
 };
 
-// True when the call fits the kernel: d = 128, g divides 16.
+// True when the call fits the kernel: d = 128, g <= 16.
 bool topk_shape_ok(const FwdParams& p);
 
 // 2-D gather view of a bf16 cache: [num_blocks * b * H_k rows, d columns],

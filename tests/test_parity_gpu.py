@@ -34,17 +34,17 @@ PATHS = [ua.UA_PATH_SPLIT_KV, ua.UA_PATH_TENSOR_CORE, ua.UA_PATH_DECODE_TC]
 
 
 def tc_ok(w):
-    return 128 % (w.hq // w.hk) == 0
+    return (w.hq // w.hk) <= 128
 
 
 def dec_ok(w):
     g = w.hq // w.hk
-    return w.d == 128 and 16 % g == 0 and g * w.max_seqlen_q <= 16
+    return w.d == 128 and g <= 16 and g * w.max_seqlen_q <= 16
 
 
 def run_gpu(w, problem=None, out=None, path=ua.UA_PATH_AUTO):
     if path == ua.UA_PATH_TENSOR_CORE and not tc_ok(w):
-        pytest.skip("g does not divide the 128-row tile")
+        pytest.skip("g > 128")
     if path == ua.UA_PATH_DECODE_TC and not dec_ok(w):
         pytest.skip("not a decode-shaped call for the transposed kernel")
     wd = w.to("cuda")

@@ -5,12 +5,14 @@ a static device array inside the library instead of a problem workspace.
 
 Checked through the C ABI against ua_forward on the same inputs, on two calls
 in a row (the second call finds the first call's partials still in the shared
-array), with the tolerance of the parity tests.  This file is collected last
-so that a failure here cannot hide another test's result."""
+array), and against the fp64 CPU oracle directly, with the tolerance of the
+parity tests.  This file is collected last so that a failure here cannot hide
+another test's result."""
 import numpy as np
 import pytest
 import torch
 
+import oracle
 import paged_varlen_flash_gb300 as ua
 from paged_varlen_flash_gb300 import binding
 from paged_varlen_flash_gb300 import workloads as W
@@ -28,16 +30,16 @@ def _built():
     ua.load_library()
 
 
-def _desc(w):
+def _desc(w, path=0, partials=0):
     flags = ua.flags_of(w.causal, w.softcap, w.alibi_slopes is not None, w.window,
                         w.sinks is not None)
     return binding.ProblemDesc(w.hq, w.hk, w.d, w.b, w.num_blocks, max(1, w.num_seqs),
                                w.max_blocks_per_seq, max(1, w.total_q), 0, flags, w.scale,
-                               w.softcap, w.window), flags
+                               w.softcap, w.window, path, 0, 1.0, 1.0, partials), flags
 
 
-def _noalloc(w, out, err=None):
-    desc, flags = _desc(w)
+def _noalloc(w, out, err=None, path=0, partials=0):
+    desc, flags = _desc(w, path, partials)
     return binding.ua_forward_noalloc(desc, w.q, w.k_cache, w.v_cache, w.block_table,
                                  w.cu_seqlens_q, w.seqused_k, w.num_seqs, w.total_q,
                                  w.max_seqlen_q, w.max_seqlen_k, flags, w.sinks,
@@ -97,4 +99,46 @@ def test_noalloc_rejects_sizes_beyond_its_scratch():
                 poison=False, device="cuda")
     out = torch.empty_like(w.q)
     assert _noalloc(w, out) == 2   # UA_ERR_UNSUPPORTED, nothing launched
+    torch.cuda.synchronize()
+
+
+def _oracle_close(out, w):
+    want = oracle.forward_workload(w.to("cpu"))
+    got = out.float().cpu().numpy()
+    assert np.all(np.isfinite(got))
+    d = np.abs(got - want)
+    assert d.max() <= MAX_ABS and d.mean() <= MEAN_ABS, (d.max(), d.mean())
+
+
+def test_noalloc_matches_oracle_directly():
+    # Decode rows, GQA 4, softcap + window + sinks, NaN in every unused slot.
+    w = W.random_small(31, num_seqs=6, hq=16, hk=4, d=128, b=16, sq=(1, 2), ctx=(0, 1500),
+                       softcap=30.0, window=700, sinks=True).to("cuda")
+    for _ in range(2):
+        out = torch.full_like(w.q, float("nan"))
+        assert _noalloc(w, out) == 0
+        torch.cuda.synchronize()
+        _oracle_close(out, w)
+
+
+def test_noalloc_at_its_largest_accepted_size():
+    # 500 rows x 16 heads x (256 + 2) floats = 8.26 MB per segment, just under
+    # half the 16 MiB array (the largest per-segment size accepted): exactly
+    # two segments fit, and the split planner picks two for this batch.
+    # ALiBi and bf16 partials on.
+    w = W.random_small(32, num_seqs=1, hq=16, hk=2, d=256, b=64, sq=(500, 500), ctx=(900, 1000),
+                       alibi=True).to("cuda")
+    out = torch.full_like(w.q, float("nan"))
+    assert _noalloc(w, out, partials=ua.UA_PARTIALS_BF16) == 0
+    torch.cuda.synchronize()
+    _oracle_close(out, w)
+
+
+def test_noalloc_path_field_is_checked():
+    w = W.random_small(33, num_seqs=2, hq=8, hk=2, d=64, b=16, sq=(1, 1), ctx=(10, 50)).to("cuda")
+    out = torch.empty_like(w.q)
+    assert _noalloc(w, out, path=ua.UA_PATH_SPLIT_KV) == 0
+    assert _noalloc(w, out, path=ua.UA_PATH_TENSOR_CORE) == 2   # UA_ERR_UNSUPPORTED
+    assert _noalloc(w, out, path=ua.UA_PATH_DECODE_TC) == 2
+    assert _noalloc(w, out, path=7) == 1                        # UA_ERR_INVALID_ARG
     torch.cuda.synchronize()
