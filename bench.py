@@ -35,9 +35,10 @@ if ROOT not in sys.path:
 
 METRIC = "prefill TFLOPS and decode KV-read GB/s on 1×GB300, as % of roofline"
 HEADLINE = "decode"
-SECONDARY = ["chunked", "long_prefill", "wide_mha_alibi"]
-# HBM-bound secondary workloads, reported in GB/s of algorithmic bytes.
-SECONDARY_HBM = ["decode_fp8", "decode_topk"]
+SECONDARY = ["chunked", "long_prefill", "long_prefill_shuffled", "wide_mha_alibi"]
+# HBM-bound secondary workloads, reported in GB/s of algorithmic bytes
+# ("decode_cold": the headline batch with L2 flushed between steps).
+SECONDARY_HBM = ["decode_cold", "decode_fp8", "decode_topk"]
 L2_FLUSH_BYTES = 256 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
@@ -358,20 +359,29 @@ def run_ours(args):
                           torch=torch, ua=ua)
             ms = statistics.mean(r["step_ms"])
             km = statistics.mean(r["kernel_ms"])
+            # The kernel's own roofline: the larger of the tensor-core time
+            # of its flops and the HBM time of its bytes (burst peaks: the
+            # kernel is timed alone).
+            t_bound = max(f_s / (peaks["bf16_tflops"] * 1e12), b_s / (peaks["hbm_gbs"] * 1e9))
             per_config[name] = {
                 "ms_per_step": round(ms, 4), "tflops": round(f_s / (ms * 1e-3) / 1e12, 2),
                 "kernel_tflops": round(f_s / (km * 1e-3) / 1e12, 2),
                 "frac_of_bf16_peak": round(f_s / (km * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
+                "roofline_bound": "tensor" if f_s / peaks["bf16_tflops"] >= b_s / peaks["hbm_gbs"] * 1e3
+                                  else "hbm",
+                "roofline_us": round(t_bound * 1e6, 2),
+                "frac_of_roofline": round(t_bound / (km * 1e-3), 4),
                 "path": r["path"], "launches_per_step": r["launches"] // max(1, len(r["step_ms"])),
                 "flops": f_s, "bytes": b_s, "device_error": r["device_error"]}
             del ws
             torch.cuda.empty_cache()
         for name in SECONDARY_HBM:
-            ws = W.make(name, device=dev)
+            ws = w if name == "decode_cold" else W.make(name, device=dev)
             b_s, f_s = workload_units(ws)
-            # decode_topk touches 0.27 GB per step, only twice L2: flush between steps
+            # decode_topk touches 0.27 GB per step, only twice L2: flush between
+            # steps; decode_cold flushes too (the headline runs warm).
             r = time_ours(ws, max(3, min(args.steps, 20)), max(3, args.warmup),
-                          flush=ws.topk_len is not None, torch=torch, ua=ua)
+                          flush=ws.topk_len is not None or name == "decode_cold", torch=torch, ua=ua)
             ms = statistics.mean(r["step_ms"])
             km = statistics.mean(r["kernel_ms"])
             per_config[name] = {
@@ -381,8 +391,12 @@ def run_ours(args):
                 "kv_tokens_per_s": round((sum(ws.seqlens_k) if ws.topk_len is None else
                                           int(ws.topk_len.to("cpu").sum())) / (ms * 1e-3), 1),
                 "path": r["path"], "launches_per_step": r["launches"] // max(1, len(r["step_ms"])),
-                "bytes": b_s, "device_error": r["device_error"]}
-            del ws
+                "bytes": b_s, "device_error": r["device_error"],
+                "l2": "flushed (256 MiB write) between steps" if (ws.topk_len is not None or
+                                                                 name == "decode_cold") else
+                      "inputs larger than L2, no flush"}
+            if ws is not w:
+                del ws
             torch.cuda.empty_cache()
     sampler.stop()
 
@@ -510,7 +524,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default=None,
                     choices=["tiny", "decode", "chunked", "long_prefill", "long_prefill_shuffled",
-                             "wide_mha_alibi", "decode_fp8", "decode_topk"],
+                             "wide_mha_alibi", "decode_fp8", "decode_topk", "decode_d64",
+                             "decode_d256"],
                     help="time only this workload and print its own short JSON line "
                          "(for profiling); the default is the full headline run")
     ap.add_argument("--path", default="auto", choices=["auto", "split", "tensor", "decode"],

@@ -103,6 +103,8 @@ def load_library():
     lib.ua_forward_topk.restype = ctypes.c_int
     lib.ua_set_qq_bias.argtypes = [vp, vp, ctypes.c_int64, ctypes.c_int64]
     lib.ua_set_qq_bias.restype = ctypes.c_int
+    lib.ua_debug_stall_data_waits.argtypes = [vp, i32, i64]
+    lib.ua_debug_stall_data_waits.restype = ctypes.c_int
     lib.ua_set_profile_events.argtypes = [vp, vp, vp]
     lib.ua_set_profile_events.restype = ctypes.c_int
     lib.ua_destroy.argtypes = [vp]
@@ -227,6 +229,12 @@ def ua_set_qq_bias(problem, bias, n, row_stride):
     a * row_stride + c) to a problem; ``bias=None`` clears it.  Returns the
     status code without raising."""
     return load_library().ua_set_qq_bias(problem, _ptr(bias), n, row_stride)
+
+
+def ua_debug_stall_data_waits(problem, enable, limit_ns=2_000_000):
+    """Testing hook: make the next forward calls' first K/V data wait run out
+    after ``limit_ns`` (see include/ua.h).  Returns the status code."""
+    return load_library().ua_debug_stall_data_waits(problem, int(enable), int(limit_ns))
 
 
 def ua_check_device_error(problem, stream=None):

@@ -47,6 +47,10 @@ struct ua_problem {
     int32_t* d_err = nullptr;
     float* d_ws = nullptr;
     size_t ws_bytes = 0;
+    // work list of the persistent prefill kernel: entries, then the
+    // per-sequence prefix, then [entries, claim counter]
+    void* d_work = nullptr;
+    int32_t work_cap = 0;
     // staging buffers of ua_forward_host (allocated on first use)
     void* st_q = nullptr;
     void* st_out = nullptr;
@@ -72,6 +76,9 @@ struct ua_problem {
     const char* last_path = "none";
     cudaEvent_t prof_begin = nullptr;
     cudaEvent_t prof_end = nullptr;
+    // testing hook of ua_debug_stall_data_waits
+    int32_t stall = 0;
+    int64_t stall_ns = 0;
 };
 
 namespace {
@@ -143,10 +150,19 @@ ua_status ua_problem_create(const ua_problem_desc* d, ua_problem** out) {
     const size_t row_bytes = size_t(d->head_size + 2) * sizeof(float);
     const size_t want = size_t(d->max_total_q) * d->num_q_heads * row_bytes * 16;
     p->ws_bytes = std::min(want, kWorkspaceCap);
+    // Work-list entries: every call's (total_q / (2 ppt) + num_seqs) entries
+    // without a KV split, and room for the splits the planner makes when the
+    // grid is small (about 4 x 152 units per KV head x up to 64 segments).
+    const int64_t cap = std::min<int64_t>(d->max_total_q + d->max_num_seqs + 64 * 4 * 160,
+                                          int64_t(1) << 30);
+    p->work_cap = (int32_t)cap;
+    const size_t work_bytes = (size_t)cap * sizeof(int2) + (size_t)(d->max_num_seqs + 1) * 4 + 16;
     if (cudaMalloc(&p->d_err, sizeof(int32_t)) != cudaSuccess ||
-        cudaMalloc(&p->d_ws, p->ws_bytes) != cudaSuccess) {
+        cudaMalloc(&p->d_ws, p->ws_bytes) != cudaSuccess ||
+        cudaMalloc(&p->d_work, work_bytes) != cudaSuccess) {
         cudaGetLastError();
         cudaFree(p->d_err);
+        cudaFree(p->d_ws);
         delete p;
         return UA_ERR_OUT_OF_MEMORY;
     }
@@ -155,6 +171,7 @@ ua_status ua_problem_create(const ua_problem_desc* d, ua_problem** out) {
         note_cuda(e, "ua_problem_create");
         cudaFree(p->d_err);
         cudaFree(p->d_ws);
+        cudaFree(p->d_work);
         delete p;
         return UA_ERR_CUDA;
     }
@@ -166,6 +183,7 @@ void ua_destroy(ua_problem* p) {
     if (!p) return;
     cudaFree(p->d_err);
     cudaFree(p->d_ws);
+    cudaFree(p->d_work);
     cudaFree(p->st_q);
     cudaFree(p->st_out);
     cudaFree(p->st_bt);
@@ -192,6 +210,14 @@ ua_status ua_set_qq_bias(ua_problem* p, const float* bias, int64_t n, int64_t ro
     p->qq_bias = bias;
     p->qq_n = n;
     p->qq_stride = row_stride;
+    return UA_OK;
+}
+
+ua_status ua_debug_stall_data_waits(ua_problem* p, int32_t enable, int64_t limit_ns) {
+    if (!p) return UA_ERR_INVALID_ARG;
+    if (enable && (limit_ns < 1000 || limit_ns > 1000000000)) return UA_ERR_INVALID_ARG;
+    p->stall = enable ? 1 : 0;
+    p->stall_ns = enable ? limit_ns : 0;
     return UA_OK;
 }
 
@@ -277,6 +303,12 @@ ua_status prepare_call(ua_problem* p, const void* q, const void* k_cache, const 
     fp.k_scale = fp.kv_fp8 ? d.k_scale : 1.f;
     fp.v_scale = fp.kv_fp8 ? d.v_scale : 1.f;
     fp.part_bf16 = d.split_partials == UA_PARTIALS_BF16 ? 1 : 0;
+    fp.work_list = static_cast<int2*>(p->d_work);
+    fp.seq_prefix = reinterpret_cast<int32_t*>(fp.work_list + p->work_cap);
+    fp.work_info = fp.seq_prefix + (d.max_num_seqs + 1);
+    fp.work_cap = p->work_cap;
+    fp.stall = p->stall;
+    fp.stall_ns = p->stall_ns;
     if (flags & UA_FLAG_QQ_BIAS) {
         fp.qq_bias = p->qq_bias;
         fp.qq_stride = p->qq_stride;

@@ -46,6 +46,18 @@ struct FwdParams {
     const int32_t* topk_idx;       // [total_q, topk_stride] key positions per query token, or null
     const int32_t* topk_len;       // [total_q] list lengths (with topk_idx)
     int32_t topk_stride;
+    // Persistent prefill: the work list the planner kernel writes (entries
+    // (sequence, tile pair << 7 | KV segment), longest first), its length and
+    // claim counter, and the per-sequence exclusive prefix of entry counts.
+    int2* work_list;
+    int32_t* work_info;            // [0] entries, [1] claim counter
+    int32_t* seq_prefix;           // [num_seqs + 1]
+    int32_t work_cap;              // capacity of work_list in entries
+    // Testing hook (ua_debug_stall_data_waits): when set, each kernel's first
+    // consumer-side K/V data wait waits on a barrier that nothing completes,
+    // bounded by stall_ns, so the bounded-wait abort path runs.
+    int32_t stall;
+    int64_t stall_ns;
 };
 
 // Per-sequence metadata check.  Returns UA_DEVERR_* bits (0 = well formed) and

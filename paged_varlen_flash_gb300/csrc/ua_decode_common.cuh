@@ -12,14 +12,14 @@
 namespace ua {
 
 __device__ __forceinline__ bool dwait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                      int32_t* err) {
+                                      int32_t* err, uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t start = global_ns();
     for (;;) {
         for (int i = 0; i < 128; ++i)
             if (mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
-        if (global_ns() - start > kWaitLimitNs) {
+        if (global_ns() - start > limit_ns) {
             *abort_flag = 1;
             atomicOr(err, (int)UA_DEVERR_TIMEOUT);
             return false;

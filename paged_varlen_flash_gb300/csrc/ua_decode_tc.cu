@@ -74,8 +74,9 @@ struct DCfg {
     static constexpr int kOffP = kOffV16 + (F8 ? kKvBytes : 0);  // two P^T buffers
     static constexpr int kOffBar = kOffP + 2 * kPBuf;
     // q_full, k_full[NSK], v_full[NSV], k_empty[NSK], v_empty[NSV], s_full[2],
-    // p_full[2], o_done[2], drain[2]; F8: kc_full, kc_empty, vc_full, vc_empty
-    static constexpr int kNumBars = 1 + 2 * NSK + 2 * NSV + 8 + (F8 ? 4 : 0);
+    // p_full[2], o_done[2], drain[2]; F8: kc_full, kc_empty, vc_full, vc_empty;
+    // never (the testing hook's stall waits on it; nothing arrives)
+    static constexpr int kNumBars = 1 + 2 * NSK + 2 * NSV + 8 + (F8 ? 4 : 0) + 1;
     static constexpr int kOffRed = kOffBar + kNumBars * 8;    // maxima [2][4][16] fp32
     static constexpr int kOffSum = kOffRed + 2 * 4 * kN * 4;  // row sums [4][16] fp32
     static constexpr int kOffMisc = kOffSum + 4 * kN * 4;
@@ -170,6 +171,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     // and read by their MMA (kc_empty, vc_empty); single-buffered.
     const uint32_t kc_full = s_full0 + 64, kc_empty = s_full0 + 72;
     const uint32_t vc_full = s_full0 + 80, vc_empty = s_full0 + 88;
+    const uint32_t never = s_full0 + (F8 ? 96 : 64);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
     float* red = reinterpret_cast<float*>(smem + C::kOffRed);
@@ -200,6 +202,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         }
         mbar_init(drain, 1);
         mbar_init(drain + 8, 1);
+        mbar_init(never, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -317,6 +320,12 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             for (int j = 0; ok && j < n_tiles; ++j) {
                 if (j >= 2 && !wwait(p_full0 + 8 * (j & 1), ((j - 2) >> 1) & 1)) break;
                 const int stg = j % NSK;
+                if (p.stall && j == 0) {
+                    // Testing hook: the first K wait waits on a barrier that
+                    // nothing completes and gives up after stall_ns.
+                    if (!__all_sync(0xffffffffu, dwait(never, 0, abort_flag, p.err, (uint64_t)p.stall_ns)))
+                        break;
+                }
                 if constexpr (F8) {
                     if (!wwait(kc_full, j & 1)) break;
                 } else {

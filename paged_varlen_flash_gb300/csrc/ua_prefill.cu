@@ -645,13 +645,25 @@ void plan_prefill(const FwdParams& p, int num_sms, size_t workspace_bytes, Prefi
         splits = (int)std::min<size_t>((size_t)splits, per_split ? workspace_bytes / per_split : 1);
         if (splits < 1) splits = 1;
     }
+    const bool pair = prefill_pair_supported(p.d);
+    // The two-tile kernel's work list must hold every entry.
+    while (pair && splits > 1 && pair_work_entries_bound(p, splits) > p.work_cap) --splits;
     if (splits > 1) {
         const int per = (p.max_seqlen_k + splits - 1) / splits;
         plan->chunk = (per + bn - 1) / bn * bn;
         splits = (p.max_seqlen_k + plan->chunk - 1) / plan->chunk;
     }
     plan->splits = splits;
-    plan->launches = splits > 1 ? 2 : 1;
+    if (pair) {
+        // Persistent CTAs: one per SM, fewer when the call has fewer units
+        // (sequences x tile pairs x segments x KV heads, bounded from the
+        // host-side maxima).
+        const int64_t pairs = (int64_t)p.num_seqs * ctas * splits * p.hk;
+        plan->ctas = (int)std::max<int64_t>(1, std::min<int64_t>(num_sms, pairs));
+        plan->launches = splits > 1 ? 3 : 2;   // planner, kernel[, combine]
+    } else {
+        plan->launches = splits > 1 ? 2 : 1;
+    }
 }
 
 bool prefill_shape_ok(const FwdParams& p) {
@@ -670,8 +682,7 @@ cudaError_t launch_prefill(const PrefillPlan& plan, const CUtensorMap& tm_k, con
     cuuint32_t box[3] = {64, (cuuint32_t)p.g, (cuuint32_t)(kRows / p.g)};
     if (!encode_bf16_sw128(&tq, p.q, 3, dims, strides, box)) return cudaErrorInvalidValue;
     if (plan.num_tiles <= 0) return cudaSuccess;
-    if (prefill_pair_supported(p.d))
-        return launch_prefill_pair(tq, tm_k, tm_v, p, (plan.num_tiles + 1) / 2, stream);
+    if (prefill_pair_supported(p.d)) return launch_prefill_pair(tq, tm_k, tm_v, p, plan.ctas, stream);
     const bool qq = (p.flags & UA_FLAG_QQ_BIAS) != 0;
     const bool plain = !qq && (p.flags & (UA_FLAG_SOFTCAP | UA_FLAG_ALIBI)) == 0;
     if (p.d != 256) return cudaErrorInvalidValue;

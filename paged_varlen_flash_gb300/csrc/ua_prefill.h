@@ -10,6 +10,7 @@ struct PrefillPlan {
     int num_tiles = 0;     // query tiles per (sequence, kv head) (grid x / splits)
     int splits = 1;        // KV segments per tile (1 = the kernel writes O itself)
     int chunk = 0;         // keys per segment (a multiple of the KV tile)
+    int ctas = 0;          // persistent CTAs of the two-tile kernel (one per SM at most)
     int launches = 0;      // kernels enqueued per call
 };
 
@@ -28,10 +29,16 @@ void plan_prefill(const FwdParams& p, int num_sms, size_t workspace_bytes, Prefi
 // K/V tile); the others use one 128-row tile per CTA.
 bool prefill_pair_supported(int d);
 
-// Enqueue the two-tiles-per-CTA kernel over `pairs` tile pairs per (sequence,
-// kv head); tq is the Q tensor map (boxes of the tile's 128 packed rows).
+// Upper bound on the work-list entries (sequence, tile pair, KV segment) of
+// the two-tile kernel for a call with `splits` segments:
+// (total_q / (2 floor(128 / g)) + num_seqs) * splits.
+int64_t pair_work_entries_bound(const FwdParams& p, int splits);
+
+// Enqueue the planner (the longest-first work list in p.work_list) and the
+// persistent two-tile kernel on `ctas` CTAs; tq is the Q tensor map (boxes of
+// a tile's packed rows).
 cudaError_t launch_prefill_pair(const CUtensorMap& tq, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
-                                const FwdParams& p, int pairs, cudaStream_t stream);
+                                const FwdParams& p, int ctas, cudaStream_t stream);
 
 // Enqueue the prefill path (p.out receives the final bf16 rows).
 cudaError_t launch_prefill(const PrefillPlan& plan, const CUtensorMap& tm_k,

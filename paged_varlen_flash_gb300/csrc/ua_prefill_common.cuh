@@ -33,14 +33,15 @@ struct Bars {
 // Wait on an mbarrier phase; gives up (and raises the CTA's abort flag and the
 // device error bit) after about a second, or as soon as another role aborted.
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
-                                              volatile int* abort_flag, int32_t* err) {
+                                              volatile int* abort_flag, int32_t* err,
+                                              uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t start = global_ns();
     for (;;) {
         for (int i = 0; i < 128; ++i)
             if (mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
-        if (global_ns() - start > kWaitLimitNs) {
+        if (global_ns() - start > limit_ns) {
             *abort_flag = 1;
             atomicOr(err, (int)UA_DEVERR_TIMEOUT);
             return false;
@@ -60,6 +61,14 @@ __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
         : "=l"(d)
         : "l"(*reinterpret_cast<uint64_t*>(&a)), "l"(*reinterpret_cast<uint64_t*>(&b)),
           "l"(*reinterpret_cast<uint64_t*>(&c)));
+    return *reinterpret_cast<float2*>(&d);
+}
+
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;"
+        : "=l"(d)
+        : "l"(*reinterpret_cast<uint64_t*>(&a)), "l"(*reinterpret_cast<uint64_t*>(&b)));
     return *reinterpret_cast<float2*>(&d);
 }
 

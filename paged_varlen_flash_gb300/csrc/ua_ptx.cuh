@@ -70,13 +70,14 @@ __device__ __forceinline__ uint64_t global_ns() {
 // (checked every 256 polls).  Returns false if it gave up.
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t start = global_ns();
     for (;;) {
         for (int i = 0; i < 256; ++i)
             if (mbar_try_wait(bar, parity)) return true;
-        if (global_ns() - start > kWaitLimitNs) return false;
+        if (global_ns() - start > limit_ns) return false;
     }
 }
 
@@ -149,6 +150,28 @@ __device__ __forceinline__ float fast_exp2(float x) {
 }
 
 constexpr float kLog2e = 1.4426950408889634f;
+
+// tanh by the special-function unit's own approximation (tanh.approx.f32,
+// one instruction; relative error about 2^-11 over the whole range).  Used by
+// the compute-bound prefill kernel, where the softcap's two extra special-
+// function operations per score (an exponential and a reciprocal) would make
+// that unit, not the tensor cores, the bound.  A logit of magnitude |x| moves
+// by at most ~5e-4 |x|, the same order as rounding P to bf16 for the MMA.
+__device__ __forceinline__ float tanh_fast(float x) {
+    float y;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Programmatic dependent launch: a kernel launched with the programmatic
+// stream-serialization attribute may start while the kernel before it in the
+// stream still runs; griddep_wait() blocks the calling thread until that
+// kernel has completed and its memory is visible, and griddep_launch() lets
+// the dependent kernel start early.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 
 // tanh from its exponential form, tanh(x) = 1 - 2 / (e^{2x} + 1), with the
 // hardware base-2 exponential and a fast reciprocal: relative error a few

@@ -39,7 +39,7 @@ struct SplitLayout {
     static constexpr int kRingBytes = kWarps * kWarpBytes;
     static constexpr int kQBytes = ROWS * D * 4;         // q rows, fp32
     static constexpr int kPBytes = kWarps * kSub * ROWS * 4;
-    static constexpr int kBarBytes = kWarps * kStages * 8;
+    static constexpr int kBarBytes = kWarps * kStages * 8 + 8;   // + one barrier nothing completes
     static constexpr int kMergeBytes = kWarps * ROWS * (D + 2) * 4;
     static_assert(kMergeBytes <= kRingBytes, "merge area must fit in the ring");
     static constexpr int kQOff = kRingBytes;
@@ -147,8 +147,11 @@ split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
             for (int t = 0; t < 8; ++t) dst[t] = 0.f;
         }
     }
+    // The testing hook's stall waits on this barrier; nothing ever arrives.
+    const uint32_t never = smem_u32(&bars[kWarps * kStages]);
     if (lane == 0) {
         for (int stg = 0; stg < kStages; ++stg) mbar_init(smem_u32(&bars[warp * kStages + stg]), 1);
+        if (warp == 0) mbar_init(never, 1);
         fence_mbar_init();
     }
     if (threadIdx.x == 0) {
@@ -213,7 +216,8 @@ split_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ C
     for (int it = 0; it < my_n; ++it) {
         const int stg = it % kStages;
         const uint32_t bar = smem_u32(&bars[warp * kStages + stg]);
-        const bool ok = mbar_wait_bounded(bar, (it / kStages) & 1);
+        const bool ok = (p.stall && it == 0) ? mbar_wait_bounded(never, 0, (uint64_t)p.stall_ns)
+                                             : mbar_wait_bounded(bar, (it / kStages) & 1);
         if (__any_sync(0xffffffffu, !ok)) {
             timed_out = true;
             fail_it = it;

@@ -151,13 +151,24 @@ class Workload:
                 t += 1
         return total
 
-    def kv_bytes_read(self) -> int:
-        """K and V bytes of the used keys, counted once per (sequence, kv head);
-        with top-k lists, once per listed key of each query token."""
-        keys = int(sum(self.seqlens_k))
+    def kv_keys_read(self) -> int:
+        """Keys whose K and V rows the method needs, once per (sequence, kv
+        head): the union of the rows' visible ranges -- with a sliding window,
+        keys [max(0, ctx - W + 1), S_k) (row 0 reaches furthest back); else
+        all S_k keys.  With top-k lists, every listed entry of every token."""
         if self.topk_len is not None:
-            keys = int(self.topk_len.to(torch.int64).sum())
-        return keys * self.hk * self.d * (1 if self.kv_fp8 else 2) * 2
+            return int(self.topk_len.to(torch.int64).sum())
+        total = 0
+        for sq, sk in zip(self.seqlens_q, self.seqlens_k):
+            if sq <= 0:
+                continue
+            lo = max(0, sk - sq - self.window + 1) if self.window > 0 else 0
+            total += max(0, sk - lo)
+        return total
+
+    def kv_bytes_read(self) -> int:
+        """K and V bytes of the keys in ``kv_keys_read``."""
+        return self.kv_keys_read() * self.hk * self.d * (1 if self.kv_fp8 else 2) * 2
 
 
 def topk_lists(seqlens_q, seqlens_k, k: int, seed: int, *, causal: bool = True,

@@ -55,3 +55,27 @@ def test_decode_topk_workload_shape_and_counts():
     assert w.topk_idx.shape == (256, 2048) and int(w.topk_len.min()) == 2048
     assert w.visible_pairs() == 256 * 2048
     assert w.kv_bytes_read() == 256 * 2048 * 1 * 128 * 2 * 2
+
+
+def test_kv_keys_read_is_the_union_of_the_rows_visible_keys():
+    # Brute force: mark every key some row of the sequence can see (causal,
+    # window W keeps [i + ctx - W + 1, i + ctx]) and count the marks.
+    for window in (0, 1, 7, 100, 5000):
+        w = W.random_small(71 + window, num_seqs=5, sq=(1, 60), ctx=(0, 300), window=window,
+                           poison=False)
+        want = 0
+        for sq, sk in zip(w.seqlens_q, w.seqlens_k):
+            ctx = sk - sq
+            seen = set()
+            for i in range(sq):
+                lo = max(0, i + ctx - window + 1) if window else 0
+                seen.update(range(lo, i + ctx + 1))
+            want += len(seen)
+        assert w.kv_keys_read() == want, window
+        assert w.kv_bytes_read() == want * w.hk * w.d * 2 * 2
+
+
+def test_chunked_workload_reads_only_its_windows():
+    w = W.make("chunked", values=False)
+    full = sum(w.seqlens_k) * w.hk * w.d * 2 * 2
+    assert 70e6 <= w.kv_bytes_read() <= 76e6 < full
