@@ -38,7 +38,7 @@ HEADLINE = "decode"
 SECONDARY = ["chunked", "long_prefill", "long_prefill_shuffled", "wide_mha_alibi"]
 # HBM-bound secondary workloads, reported in GB/s of algorithmic bytes
 # ("decode_cold": the headline batch with L2 flushed between steps).
-SECONDARY_HBM = ["decode_cold", "decode_fp8", "decode_topk"]
+SECONDARY_HBM = ["decode_cold", "decode_d64", "decode_d256", "decode_fp8", "decode_topk"]
 L2_FLUSH_BYTES = 256 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")

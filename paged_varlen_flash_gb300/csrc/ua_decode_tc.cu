@@ -45,7 +45,6 @@ namespace {
 
 constexpr int kN = 16;          // packed rows per tile (MMA N)
 constexpr int kBN = 128;        // keys per KV tile (MMA M of S^T)
-constexpr int kD = 128;         // head size served by this kernel (MMA M of O^T)
 constexpr int kThreadsD = 224;  // 4 softmax warps, TMA warp, QK^T issuer, P.V issuer
 constexpr int kThreadsF8 = 352; // fp8 caches: + 4 warps turning e4m3 tiles into f16
 constexpr int kWarpTmaD = 4;
@@ -57,9 +56,16 @@ constexpr float kLazyD = 8.0f;
 // stage only once its P.V ran, so they may differ).  F8: the rings hold e4m3
 // tiles (128 keys x 128 one-byte dims); K is turned into f16 in tensor memory
 // (the QK^T A operand), V into an f16 tile in shared memory.
-template <int NSK, int NSV, bool F8>
+// D: head size (64, 128 or 256; the fp8 cache D = 128 only).  O^T has M = D
+// rows: one M = 128 MMA per 16 keys at D = 128, two (dims 0-127, 128-255 into
+// two 16-column blocks of tensor memory) at D = 256, and at D = 64 one M = 128
+// MMA whose descriptor reads the tile's single 64-dim panel for both halves
+// of M (lanes 64-127 receive a copy of lanes 0-63 that nobody reads).
+template <int D, int NSK, int NSV, bool F8>
 struct DCfg {
-    static constexpr int kPanels = kD / 64;
+    static_assert(D == 64 || D == 128 || D == 256, "head size");
+    static_assert(!F8 || D == 128, "fp8 caches at d = 128 only");
+    static constexpr int kPanels = D / 64;
     static constexpr int kQPanel = kN * 128;              // 16 rows x 64 dims
     static constexpr int kQBytes = kPanels * kQPanel;
     static constexpr int kKvPanel = kBN * 128;            // 128 keys x 64 dims (16-bit)
@@ -68,7 +74,7 @@ struct DCfg {
     static constexpr int kPPanel = kN * 128;              // 16 rows x 64 keys
     static constexpr int kPBuf = (kBN / 64) * kPPanel;    // one P^T tile
     static constexpr int kOffQ = 0;
-    static constexpr int kOffK = F8 ? 4096 : 8192;
+    static constexpr int kOffK = F8 ? 4096 : (D == 64 ? 4096 : 8192);
     static constexpr int kOffV = kOffK + NSK * kStage;
     static constexpr int kOffV16 = kOffV + NSV * kStage;  // F8: the f16 V tile
     static constexpr int kOffP = kOffV16 + (F8 ? kKvBytes : 0);  // two P^T buffers
@@ -82,7 +88,7 @@ struct DCfg {
     static constexpr int kOffMisc = kOffSum + 4 * kN * 4;
     static constexpr int kSmem = kOffMisc + 16 + 1024;
     static constexpr int kTmemS = 0;    // S^T buffers: columns [0, 16) and [16, 32)
-    static constexpr int kTmemO = 32;   // O^T: columns [32, 48)
+    static constexpr int kTmemO = 32;   // O^T: columns [32, 48) (D = 256: dims 128-255 in [48, 64))
     static constexpr int kTmemK = 64;   // F8: f16 K (lane = key, two dims per column)
     static constexpr uint32_t kTmemCols = F8 ? 128 : 64;
     static_assert(kQBytes <= kOffK, "Q tile");
@@ -103,11 +109,11 @@ __device__ __forceinline__ void e4m3x4_to_f16x2(uint32_t w, uint32_t& lo, uint32
 // F8: K and V caches hold e4m3 codes (gfx950 page, section 7.3): the MMAs run
 // in f16 (every e4m3 value is exact in f16, and so is a bf16 Q of moderate
 // magnitude), k_scale is folded into tau and v_scale into the output scale.
-template <int NSK, int NSV, int NR, bool PLAIN, bool F8>
+template <int D, int NSK, int NSV, int NR, bool PLAIN, bool F8>
 __global__ void __launch_bounds__(F8 ? kThreadsF8 : kThreadsD, F8 ? 2 : 1)   // two CTAs per SM
 decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
-    using C = DCfg<NSK, NSV, F8>;
+    using C = DCfg<D, NSK, NSV, F8>;
     constexpr int kThreads = F8 ? kThreadsF8 : kThreadsD;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -140,8 +146,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     if (st || k_beg >= k_end) {
         // Malformed lengths (rows written as zeros) or a segment no row sees
         // (an empty partial, m = -inf).
-        for (int e = threadIdx.x; e < nrows * kD; e += kThreads) {
-            const int r = e / kD, c = e % kD;
+        for (int e = threadIdx.x; e < nrows * D; e += kThreads) {
+            const int r = e / D, c = e % D;
             const int64_t row = (q0 + r / g) * p.hq + hkv * g + r % g;
             if (split) {
                 if (c == 0) {
@@ -149,7 +155,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     p.part_ml[(row * p.splits + seg) * 2 + 1] = 0.f;
                 }
             } else {
-                p.out[row * kD + c] = __float2bfloat16_rn(0.f);
+                p.out[row * D + c] = __float2bfloat16_rn(0.f);
             }
         }
         return;
@@ -297,8 +303,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         // O^T += V(j)^T P^T(j) once P(j) and V(j) are ready.
         constexpr uint32_t idesc_qk = F8 ? tc::idesc_f16_f32(kBN, kN, false, false)
                                          : tc::idesc_bf16_f32(kBN, kN, false, false);
-        constexpr uint32_t idesc_pv = F8 ? tc::idesc_f16_f32(kD, kN, true, false)
-                                         : tc::idesc_bf16_f32(kD, kN, true, false);
+        constexpr uint32_t idesc_pv = F8 ? tc::idesc_f16_f32(128, kN, true, false)
+                                         : tc::idesc_bf16_f32(128, kN, true, false);
         auto wwait = [&](uint32_t bar, uint32_t par) {
             return __all_sync(0xffffffffu, dwait(bar, par, abort_flag, p.err));
         };
@@ -336,7 +342,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     const uint32_t kst = sK + stg * C::kStage;
                     const uint32_t dS = tmem + C::kTmemS + (j & 1) * kN;
 #pragma unroll
-                    for (int k = 0; k < kD / 16; ++k) {
+                    for (int k = 0; k < D / 16; ++k) {
                         const int pn = k >> 2, off = (k & 3) * 32;
                         const uint64_t bq = tc::smem_desc_sw128(sQ + pn * C::kQPanel + off, 16, 1024);
                         if constexpr (F8) {
@@ -382,10 +388,18 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     const uint32_t pbuf = sP + (j & 1) * C::kPBuf;
 #pragma unroll
                     for (int kk = 0; kk < kBN / 16; ++kk) {
-                        const uint64_t a = tc::smem_desc_sw128(vst + kk * 16 * 128, C::kKvPanel, 1024);
                         const uint64_t bp =
                             tc::smem_desc_sw128(pbuf + (kk >> 2) * C::kPPanel + (kk & 3) * 32, 16, 1024);
-                        tc::mma_bf16(tmem + C::kTmemO, a, bp, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+                        // A = V^T, MN-major: the leading-dimension offset steps
+                        // from dims 0-63 to 64-127 of the M = 128 block (0 at
+                        // D = 64: both halves read the one panel).
+                        constexpr uint32_t lbo = D == 64 ? 0u : (uint32_t)C::kKvPanel;
+#pragma unroll
+                        for (int h = 0; h < (D == 256 ? 2 : 1); ++h) {
+                            const uint64_t a = tc::smem_desc_sw128(vst + h * 2 * C::kKvPanel + kk * 16 * 128,
+                                                                   lbo, 1024);
+                            tc::mma_bf16(tmem + C::kTmemO + h * kN, a, bp, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+                        }
                     }
                     tc::commit(o_done0 + 8 * (j & 1));
                     tc::commit(F8 ? vc_empty : v_empty0 + 8 * stg);
@@ -576,12 +590,15 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                                                    abort_flag, p.err));
                 if (go) {
                     tc::fence_after_sync();
-                    uint32_t o[kN];
-                    ld16(tl + C::kTmemO, o);
-                    tc::wait_ld();
 #pragma unroll
-                    for (int r = 0; r < NR; ++r) o[r] = __float_as_uint(__uint_as_float(o[r]) * alpha[r]);
-                    st16(tl + C::kTmemO, o);
+                    for (int h = 0; h < (D == 256 ? 2 : 1); ++h) {
+                        uint32_t o[kN];
+                        ld16(tl + C::kTmemO + h * kN, o);
+                        tc::wait_ld();
+#pragma unroll
+                        for (int r = 0; r < NR; ++r) o[r] = __float_as_uint(__uint_as_float(o[r]) * alpha[r]);
+                        st16(tl + C::kTmemO + h * kN, o);
+                    }
                     tc::wait_st();
                 }
             }
@@ -622,8 +639,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             }
             if (dbar_and(1, 128, done)) {
                 tc::fence_after_sync();
-                uint32_t o[kN];
+                // Thread t: output dim t (and t + 128 at D = 256); at D = 64
+                // threads 64-127 hold copies and store nothing.
+                uint32_t o[kN], o2[kN];
                 ld16(tl + C::kTmemO, o);
+                if constexpr (D == 256) ld16(tl + C::kTmemO + kN, o2);
                 tc::wait_ld();
 #pragma unroll
                 for (int r = 0; r < NR; ++r) {
@@ -631,8 +651,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     const float L0 = lsum[r] + lsum[kN + r] + lsum[2 * kN + r] + lsum[3 * kN + r];
                     const int64_t row = (q0 + r / g) * p.hq + hkv * g + r % g;
                     const float ov = __uint_as_float(o[r]) * (F8 ? p.v_scale : 1.f);
+                    const float ov2 = D == 256 ? __uint_as_float(o2[r]) : 0.f;
                     if (split) {
-                        part_store(p, (row * p.splits + seg) * kD + t, ov);
+                        if (D != 64 || t < 64) part_store(p, (row * p.splits + seg) * D + t, ov);
+                        if (D == 256) part_store(p, (row * p.splits + seg) * D + 128 + t, ov2);
                         if (t == 0) {
                             p.part_ml[(row * p.splits + seg) * 2 + 0] = m[r];
                             p.part_ml[(row * p.splits + seg) * 2 + 1] = L0;
@@ -653,7 +675,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                             }
                         }
                         const float inv = (!zero && L > 0.f) ? num * __frcp_rn(L) : 0.f;
-                        p.out[row * kD + t] = __float2bfloat16_rn(ov * inv);
+                        if (D != 64 || t < 64) p.out[row * D + t] = __float2bfloat16_rn(ov * inv);
+                        if (D == 256) p.out[row * D + 128 + t] = __float2bfloat16_rn(ov2 * inv);
                     }
                 }
             }
@@ -671,7 +694,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 }  // namespace
 
 bool decode_tc_shape_ok(const FwdParams& p) {
-    return p.d == kD && p.g >= 1 && p.g <= kN && (int64_t)p.g * p.max_seqlen_q <= kN;
+    const bool d_ok = p.kv_fp8 ? p.d == 128 : (p.d == 64 || p.d == 128 || p.d == 256);
+    return d_ok && p.g >= 1 && p.g <= kN && (int64_t)p.g * p.max_seqlen_q <= kN;
 }
 
 void plan_decode_tc(const FwdParams& p, int num_sms, size_t workspace_bytes, DecodePlan* plan) {
@@ -698,16 +722,18 @@ void plan_decode_tc(const FwdParams& p, int num_sms, size_t workspace_bytes, Dec
 
 namespace {
 
-template <int NSK, int NSV, bool F8>
+template <int D, int NSK, int NSV, bool F8>
 cudaError_t launch_decode_t(const CUtensorMap& tq, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                             const FwdParams& p, const DecodePlan& plan, cudaStream_t stream) {
-    using C = DCfg<NSK, NSV, F8>;
+    using C = DCfg<D, NSK, NSV, F8>;
     const bool plain = (p.flags & (UA_FLAG_SOFTCAP | UA_FLAG_ALIBI | UA_FLAG_QQ_BIAS)) == 0;
     const int rows = p.g * p.max_seqlen_q;
-    auto kern = rows <= 4 ? (plain ? decode_tc_kernel<NSK, NSV, 4, true, F8> : decode_tc_kernel<NSK, NSV, 4, false, F8>)
-              : rows <= 8 ? (plain ? decode_tc_kernel<NSK, NSV, 8, true, F8> : decode_tc_kernel<NSK, NSV, 8, false, F8>)
-                          : (plain ? decode_tc_kernel<NSK, NSV, 16, true, F8>
-                                   : decode_tc_kernel<NSK, NSV, 16, false, F8>);
+    auto kern = rows <= 4 ? (plain ? decode_tc_kernel<D, NSK, NSV, 4, true, F8>
+                                   : decode_tc_kernel<D, NSK, NSV, 4, false, F8>)
+              : rows <= 8 ? (plain ? decode_tc_kernel<D, NSK, NSV, 8, true, F8>
+                                   : decode_tc_kernel<D, NSK, NSV, 8, false, F8>)
+                          : (plain ? decode_tc_kernel<D, NSK, NSV, 16, true, F8>
+                                   : decode_tc_kernel<D, NSK, NSV, 16, false, F8>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)plan.splits, (unsigned)p.hk, (unsigned)p.num_seqs);
@@ -730,8 +756,15 @@ cudaError_t launch_decode_tc(const DecodePlan& plan, const CUtensorMap& tm_k, co
     // fp8 tiles carry half the bytes, so each CTA needs twice the tiles in
     // flight to keep the same HBM rate: two staging stages per operand (the
     // e4m3 stages are half the size, so two CTAs still share an SM).
-    return p.kv_fp8 ? launch_decode_t<2, 2, true>(tq, tm_k, tm_v, p, plan, stream)
-                    : launch_decode_t<NSK, NSV, false>(tq, tm_k, tm_v, p, plan, stream);
+    if (p.kv_fp8) return launch_decode_t<128, 2, 2, true>(tq, tm_k, tm_v, p, plan, stream);
+    switch (p.d) {
+        // d = 64: 16 KB K/V tiles, two stages each and still two CTAs per SM.
+        case 64: return launch_decode_t<64, 2, 2, false>(tq, tm_k, tm_v, p, plan, stream);
+        case 128: return launch_decode_t<128, NSK, NSV, false>(tq, tm_k, tm_v, p, plan, stream);
+        // d = 256: 64 KB K/V tiles, one stage each (one CTA per SM).
+        case 256: return launch_decode_t<256, 1, 1, false>(tq, tm_k, tm_v, p, plan, stream);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace ua

@@ -22,6 +22,8 @@ Named workloads (the sizes of the five benchmark configurations):
                       h = 1..32.
 * ``decode_fp8``      the ``decode`` lengths and tables with an fp8 e4m3 K/V cache
                       (one scale per tensor, 1/32; codes of N(0,1) / scale).
+* ``decode_d64`` / ``decode_d256``  the ``decode`` lengths and tables with
+                      head size 64 / 256 (the other decode head sizes).
 * ``decode_topk``     sparse top-k decode: 256 sequences, S_q = 1,
                       S_k ~ U{4096..16384}, H_q/H_k = 16/1, d = 128, b = 64,
                       pool 48,000 blocks, causal; each query token attends to
@@ -52,6 +54,7 @@ CONFIG_NAMES = ["tiny", "decode", "chunked", "long_prefill", "wide_mha_alibi"]
 _CONFIG_INDEX = {
     "tiny": 0, "decode": 1, "chunked": 2, "long_prefill": 3,
     "long_prefill_shuffled": 3, "wide_mha_alibi": 4, "decode_fp8": 1, "decode_topk": 5,
+    "decode_d64": 1, "decode_d256": 1,
 }
 
 
@@ -328,9 +331,10 @@ def make(name: str, device="cpu", poison: bool = False, values: bool = True) -> 
     common = dict(seed=seed, device=device, poison=poison, values=values)
     if name == "tiny":
         return build(name, 4, 1, 64, 16, [128], [128], 32, 1.0 / 8.0, **common)
-    if name in ("decode", "decode_fp8"):
+    if name in ("decode", "decode_fp8", "decode_d64", "decode_d256"):
         sk = _randint(g, 512, 8192, 64)
-        return build(name, 32, 8, 128, 16, [1] * 64, sk, 40000, 1.0 / math.sqrt(128),
+        d = {"decode_d64": 64, "decode_d256": 256}.get(name, 128)
+        return build(name, 32, 8, d, 16, [1] * 64, sk, 40000, 1.0 / math.sqrt(d),
                      kv_fp8=name == "decode_fp8", **common)
     if name == "chunked":
         ctx = _randint(g, 0, 4096, 16)

@@ -48,7 +48,7 @@ def serves(w, path):
     if path == TC:
         return g <= 128
     if path == DEC:
-        return w.d == 128 and g <= 16 and g * w.max_seqlen_q <= 16
+        return w.d in (64, 128, 256) and g <= 16 and g * w.max_seqlen_q <= 16
     return True
 
 

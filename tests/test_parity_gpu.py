@@ -39,7 +39,7 @@ def tc_ok(w):
 
 def dec_ok(w):
     g = w.hq // w.hk
-    return w.d == 128 and g <= 16 and g * w.max_seqlen_q <= 16
+    return w.d in (64, 128, 256) and g <= 16 and g * w.max_seqlen_q <= 16
 
 
 def run_gpu(w, problem=None, out=None, path=ua.UA_PATH_AUTO):
