@@ -40,7 +40,16 @@ SECONDARY = ["chunked", "long_prefill", "long_prefill_shuffled", "wide_mha_alibi
 # ("decode_cold": the headline batch with L2 flushed between steps).
 SECONDARY_HBM = ["decode_cold", "decode_d64", "decode_d256", "decode_fp8", "decode_topk"]
 L2_FLUSH_BYTES = 256 << 20
-FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# Special-function unit throughput per SM per clock on GB300, measured with a
+# dependency-free probe: ex2.approx.f32 32 results, tanh.approx.f32 16.  The
+# prefill kernels spend one exponential per (row, key) score, plus one tanh
+# with a softcap; on 152 SMs at the maximum SM clock this is a third bound
+# beside the tensor and HBM ones.
+SFU_EX2_PER_CLK = 32.0
+SFU_TANH_PER_CLK = 16.0
+NUM_SMS = 152
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                  "sm_max_mhz": 2070.0}
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 KERNEL_SOURCES = {
     "split_kernel": ["ua_split.cu", "ua_ptx.cuh", "ua_common.cuh"],
@@ -359,17 +368,24 @@ def run_ours(args):
                           torch=torch, ua=ua)
             ms = statistics.mean(r["step_ms"])
             km = statistics.mean(r["kernel_ms"])
-            # The kernel's own roofline: the larger of the tensor-core time
-            # of its flops and the HBM time of its bytes (burst peaks: the
-            # kernel is timed alone).
-            t_bound = max(f_s / (peaks["bf16_tflops"] * 1e12), b_s / (peaks["hbm_gbs"] * 1e9))
+            # The kernel's own roofline: the largest of the tensor-core time
+            # of its flops, the HBM time of its bytes (burst peaks: the kernel
+            # is timed alone) and the special-function time of its
+            # exponentials (and tanh with a softcap).
+            scores = f_s / (4.0 * ws.d)
+            sfu_clk = scores * (1.0 / SFU_EX2_PER_CLK + (1.0 / SFU_TANH_PER_CLK if ws.softcap else 0.0))
+            t_tensor = f_s / (peaks["bf16_tflops"] * 1e12)
+            t_hbm = b_s / (peaks["hbm_gbs"] * 1e9)
+            t_sfu = sfu_clk / (NUM_SMS * peaks["sm_max_mhz"] * 1e6)
+            t_bound = max(t_tensor, t_hbm, t_sfu)
             per_config[name] = {
                 "ms_per_step": round(ms, 4), "tflops": round(f_s / (ms * 1e-3) / 1e12, 2),
                 "kernel_tflops": round(f_s / (km * 1e-3) / 1e12, 2),
                 "frac_of_bf16_peak": round(f_s / (km * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
-                "roofline_bound": "tensor" if f_s / peaks["bf16_tflops"] >= b_s / peaks["hbm_gbs"] * 1e3
-                                  else "hbm",
+                "roofline_bound": ("tensor", "hbm", "sfu")[[t_tensor, t_hbm, t_sfu].index(t_bound)],
                 "roofline_us": round(t_bound * 1e6, 2),
+                "bounds_us": {"tensor": round(t_tensor * 1e6, 2), "hbm": round(t_hbm * 1e6, 2),
+                              "sfu": round(t_sfu * 1e6, 2)},
                 "frac_of_roofline": round(t_bound / (km * 1e-3), 4),
                 "path": r["path"], "launches_per_step": r["launches"] // max(1, len(r["step_ms"])),
                 "flops": f_s, "bytes": b_s, "device_error": r["device_error"]}

@@ -420,12 +420,15 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 mbar_arrive(u_full0 + 8 * slot);
             }
             __syncwarp();
-            // This warp reads the descriptor back from shared memory; the slot
-            // is rewritten only after every reader released it.
-            const PairUnit& un = units[slot];
+            // Every lane takes the fields it needs into registers (the copy
+            // asm statements clobber memory).
+            const PairUnit& ud = units[slot];
+            const int live = ud.live, zero = ud.zero, has_b = ud.has_b, hkv = ud.hkv;
+            const int q_row = ud.q0 + ud.p0, t_begin = ud.t_begin, useq = ud.s, sk = ud.sk;
+            const int n_tiles = max(ud.n_a, ud.n_b);
             ++n;
-            if (!un.live) break;
-            if (un.zero) continue;
+            if (!live) break;
+            if (zero) continue;
             // Q_A and Q_B of this unit, once both tiles' last QK^T of the
             // previous unit has read the old ones.
             if (qn >= 1 && !(ok = wwait(q_empty, (qn - 1) & 1))) break;
@@ -433,29 +436,28 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 // One box per panel and tile: g heads x ppt positions = g * ppt
                 // rows (128 when g divides 128; the rows past them are padding
                 // whose outputs are never stored).
-                mbar_arrive_expect_tx(q_full, (un.has_b ? 2u : 1u) * (uint32_t)(g * ppt) * 128u * C::kPanels);
+                mbar_arrive_expect_tx(q_full, (has_b ? 2u : 1u) * (uint32_t)(g * ppt) * 128u * C::kPanels);
 #pragma unroll
                 for (int pn = 0; pn < C::kPanels; ++pn) {
-                    tma_load_3d(sQ + pn * C::kQPanel, &tm_q, pn * 64, un.hkv * g, un.q0 + un.p0, q_full);
-                    if (un.has_b)
-                        tma_load_3d(sQ + C::kQTile + pn * C::kQPanel, &tm_q, pn * 64, un.hkv * g,
-                                    un.q0 + un.p0 + ppt, q_full);
+                    tma_load_3d(sQ + pn * C::kQPanel, &tm_q, pn * 64, hkv * g, q_row, q_full);
+                    if (has_b)
+                        tma_load_3d(sQ + C::kQTile + pn * C::kQPanel, &tm_q, pn * 64, hkv * g, q_row + ppt,
+                                    q_full);
                 }
             }
             ++qn;
-            const int n_tiles = max(un.n_a, un.n_b);
-            const int nblk_seq = (un.sk + b - 1) / b;
-            const int32_t* bt = p.block_table + (int64_t)un.s * p.bt_stride;
+            const int nblk_seq = (sk + b - 1) / b;
+            const int32_t* bt = p.block_table + (int64_t)useq * p.bt_stride;
             // Block ids are fetched one tile ahead so their load latency
             // overlaps the current tile's waits and copies.
             auto tile_id = [&](int j) -> int32_t {
-                const int blk0 = (un.t_begin + j) * kBN / b;
+                const int blk0 = (t_begin + j) * kBN / b;
                 return lane < min(kBN / b, nblk_seq - blk0) ? __ldg(bt + blk0 + lane) : 0;
             };
             int32_t id_next = tile_id(0);
             for (int j = 0; j < n_tiles; ++j, ++kt) {
                 const int stk = kt % NK, stv = kt % NV;
-                const int blk0 = (un.t_begin + j) * kBN / b;
+                const int blk0 = (t_begin + j) * kBN / b;
                 const int nb = min(kBN / b, nblk_seq - blk0);
                 const uint32_t bytes = (uint32_t)nb * b * 128 * C::kPanels;
                 const int32_t id = id_next;
@@ -469,7 +471,7 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
 #pragma unroll
                     for (int pn = 0; pn < C::kPanels; ++pn)
                         tma_load_4d(sK + stk * C::kKvBytes + pn * C::kKvPanel + lane * b * 128, &tm_k,
-                                    pn * 64, un.hkv, 0, id, k_full0 + 8 * stk);
+                                    pn * 64, hkv, 0, id, k_full0 + 8 * stk);
                 }
                 if (kt >= NV && !(ok = wwait(v_empty0 + 8 * stv, ((kt / NV) + 1) & 1))) {
                     k_extra = 1;   // this tile's K copy was issued, its V copy not
@@ -481,7 +483,7 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
 #pragma unroll
                     for (int pn = 0; pn < C::kPanels; ++pn)
                         tma_load_4d(sV + stv * C::kKvBytes + pn * C::kKvPanel + lane * b * 128, &tm_v,
-                                    pn * 64, un.hkv, 0, id, v_full0 + 8 * stv);
+                                    pn * 64, hkv, 0, id, v_full0 + 8 * stv);
                 }
             }
             if (!ok) break;
@@ -513,6 +515,15 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         const uint32_t dS = tmem + x * kBN;
         const uint32_t dO = tmem + C::kTmemO + x * D;
         const uint32_t qst = sQ + x * C::kQTile;
+        // Shared-memory descriptors as a base per operand buffer plus a
+        // compile-time offset per MMA: the start-address field holds the byte
+        // address >> 4 (below 2^14 for any shared-memory address), so adding
+        // an offset never carries into the next field, and the issue loop
+        // spends one add per descriptor instead of recomputing it.
+        const uint64_t q_desc = tc::smem_desc_sw128(qst, 16, 1024);
+        const uint64_t k_desc0 = tc::smem_desc_sw128(sK, 16, 1024);
+        const uint64_t v_desc0 = tc::smem_desc_sw128(sV, C::kKvPanel, 1024);
+        constexpr uint32_t kStageStep = (uint32_t)C::kKvBytes >> 4;   // one ring stage
         int n = 0, qn = 0;
         int sx = 0;   // S tiles of tile x issued before this unit
         int ux = 0;   // units with work for tile x before this one
@@ -520,33 +531,30 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         for (;;) {
             const int slot = n & 1;
             if (!(ok = wwait(u_full0 + 8 * slot, (n >> 1) & 1))) break;
-            // The descriptor is read from shared memory while the unit runs
-            // and the slot released at its end (the TMA warp may still run a
-            // unit ahead in the other slot).
-            const PairUnit& un = units[slot];
-            const uint32_t release = u_empty0 + 8 * slot;
+            // The fields this warp needs, in registers (the MMA asm statements
+            // clobber memory, so fields read from shared memory inside the
+            // issue loop would be reloaded after every MMA); the slot is
+            // released at once.
+            const PairUnit& ud = units[slot];
+            const int live = ud.live, zero = ud.zero;
+            const int nx = x ? ud.n_b : ud.n_a;
+            const int n_other = x ? ud.n_a : ud.n_b;
+            const int kv0 = ud.kv0, t_begin = ud.t_begin, sk = ud.sk;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(u_empty0 + 8 * slot);
             ++n;
-            if (!un.live) break;
-            if (un.zero) {
-                __syncwarp();
-                if (lane == 0) mbar_arrive(release);
-                continue;
-            }
-            const int nx = x ? un.n_b : un.n_a;
-            const int n_other = x ? un.n_a : un.n_b;
+            if (!live) break;
+            if (zero) continue;
             if (!(ok = wwait(q_full, qn & 1))) break;
             ++qn;
             if (nx == 0) {
                 // This tile reads neither Q nor any K/V stage in this unit.
+                if (lane == 0) mbar_arrive(q_empty);
                 __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(q_empty);
-                    mbar_arrive(release);
-                }
                 continue;
             }
             auto issue_qk = [&](int j) -> bool {
-                const int kt = un.kv0 + j;
+                const int kt = kv0 + j;
                 const int stg = kt % NK;
                 // Testing hook: the first K wait of the CTA waits on a barrier
                 // that nothing completes and gives up after stall_ns.
@@ -556,13 +564,12 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 if (!wwait(k_full0 + 8 * stg, (kt / NK) & 1)) return false;
                 tc::fence_after_sync();
                 if (lane == 0) {
-                    const uint32_t kst = sK + stg * C::kKvBytes;
+                    const uint64_t kd_s = k_desc0 + (uint64_t)((uint32_t)stg * kStageStep);
 #pragma unroll
                     for (int k = 0; k < D / 16; ++k) {
-                        const int pn = k >> 2, off = (k & 3) * 32;
-                        const uint64_t a = tc::smem_desc_sw128(qst + pn * C::kQPanel + off, 16, 1024);
-                        const uint64_t bd = tc::smem_desc_sw128(kst + pn * C::kKvPanel + off, 16, 1024);
-                        tc::mma_bf16(dS, a, bd, idesc_qk, k > 0 ? 1u : 0u);
+                        const uint32_t oq = ((k >> 2) * C::kQPanel + (k & 3) * 32) >> 4;
+                        const uint32_t ok_ = ((k >> 2) * C::kKvPanel + (k & 3) * 32) >> 4;
+                        tc::mma_bf16(dS, q_desc + oq, kd_s + ok_, idesc_qk, k > 0 ? 1u : 0u);
                     }
                     tc::commit(s_full0 + 8 * x);
                     tc::commit(k_empty0 + 8 * stg);
@@ -574,7 +581,7 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             };
             ok = issue_qk(0);
             for (int j = 0; ok && j < nx; ++j) {
-                const int kt = un.kv0 + j;
+                const int kt = kv0 + j;
                 const int stg = kt % NV;
                 if (!(ok = wwait(p_full0 + 8 * x, (sx + j) & 1))) break;
                 if (!(ok = wwait(v_full0 + 8 * stg, (kt / NV) & 1))) break;
@@ -582,9 +589,8 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 // epilogue must have read it.
                 if (j == 0 && ux > 0 && !(ok = wwait(o_free0 + 8 * x, (ux - 1) & 1))) break;
                 tc::fence_after_sync();
-                const uint32_t vst = sV + stg * C::kKvBytes;
-                const int key0 = (un.t_begin + j) * kBN;
-                const int nvalid = min(kBN, un.sk - key0);
+                const int key0 = (t_begin + j) * kBN;
+                const int nvalid = min(kBN, sk - key0);
                 if (nvalid < kBN) {
                     // Keys past S_k: whatever those slots hold must not reach O
                     // (0 * NaN is NaN), so their V rows become zeros.  (Both
@@ -601,11 +607,12 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                     __syncwarp();
                 }
                 if (lane == 0) {
+                    const uint64_t vd = v_desc0 + (uint64_t)((uint32_t)stg * kStageStep);
 #pragma unroll
                     for (int k = 0; k < kBN / 16; ++k) {
                         // A = P_x from tensor memory: 16 keys per MMA = 8 columns.
-                        const uint64_t bd = tc::smem_desc_sw128(vst + k * 16 * 128, C::kKvPanel, 1024);
-                        tc::mma_bf16_ts(dO, dS + k * 8, bd, idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
+                        tc::mma_bf16_ts(dO, dS + k * 8, vd + ((k * 16 * 128) >> 4), idesc_pv,
+                                        (j > 0 || k > 0) ? 1u : 0u);
                     }
                     tc::commit(v_empty0 + 8 * stg);
                     if (j >= n_other) tc::commit(v_empty0 + 8 * stg);
@@ -617,8 +624,6 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             if (!ok) break;
             sx += nx;
             ++ux;
-            __syncwarp();
-            if (lane == 0) mbar_arrive(release);
         }
         if (*abort_flag) {
             // No MMA this thread issued may still run when tensor memory is freed.
