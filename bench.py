@@ -56,6 +56,8 @@ KERNEL_SOURCES = {
     "prefill_kernel": ["ua_prefill.cu", "ua_prefill_common.cuh", "ua_ptx.cuh", "ua_common.cuh", "ua_tc.cuh"],
     "prefill_pair_kernel": ["ua_prefill_pair.cu", "ua_prefill_common.cuh", "ua_ptx.cuh", "ua_common.cuh",
                             "ua_tc.cuh"],
+    "prefill_grid_kernel": ["ua_prefill_grid.cu", "ua_prefill_common.cuh", "ua_ptx.cuh", "ua_common.cuh",
+                            "ua_tc.cuh"],
     "decode_tc_kernel": ["ua_decode_tc.cu", "ua_decode_common.cuh", "ua_ptx.cuh", "ua_common.cuh",
                          "ua_tc.cuh"],
     "topk_kernel": ["ua_topk.cu", "ua_decode_common.cuh", "ua_ptx.cuh", "ua_common.cuh", "ua_tc.cuh"],
@@ -196,6 +198,8 @@ def dominant_kernel(path):
         return "topk_kernel"
     if path.startswith("tensor_core_pair"):
         return "prefill_pair_kernel"
+    if path.startswith("tensor_core_grid"):
+        return "prefill_grid_kernel"
     if path.startswith("tensor_core"):
         return "prefill_kernel"
     return "split_kernel"

@@ -424,7 +424,9 @@ ua_status ua_forward(ua_problem* p, const void* q, const void* k_cache, const vo
             }
         }
         p->last_launches = plan.launches;
-        if (ua::prefill_pair_supported(fp.d))
+        if (ua::prefill_pair_supported(fp.d) && plan.dense)
+            p->last_path = plan.splits > 1 ? "tensor_core_grid+combine" : "tensor_core_grid";
+        else if (ua::prefill_pair_supported(fp.d))
             p->last_path = plan.splits > 1 ? "tensor_core_pair+combine" : "tensor_core_pair";
         else
             p->last_path = plan.splits > 1 ? "tensor_core+combine" : "tensor_core";

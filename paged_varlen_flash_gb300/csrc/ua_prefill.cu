@@ -655,12 +655,23 @@ void plan_prefill(const FwdParams& p, int num_sms, size_t workspace_bytes, Prefi
     }
     plan->splits = splits;
     if (pair) {
-        // Persistent CTAs: one per SM, fewer when the call has fewer units
-        // (sequences x tile pairs x segments x KV heads, bounded from the
-        // host-side maxima).
-        const int64_t pairs = (int64_t)p.num_seqs * ctas * splits * p.hk;
-        plan->ctas = (int)std::max<int64_t>(1, std::min<int64_t>(num_sms, pairs));
-        plan->launches = splits > 1 ? 3 : 2;   // planner, kernel[, combine]
+        // Dense batches -- the padded grid (num_seqs x max_seqlen_q rows)
+        // wastes at most a quarter on padding and fills every SM at least
+        // twice -- run one CTA per unit over that grid; ragged ones run
+        // persistent CTAs over the longest-first list (measured: the long
+        // prefill 1.87 ms dense vs 2.06 persistent, the chunked batch 0.171
+        // dense vs 0.137 persistent).
+        const int64_t grid = (int64_t)p.num_seqs * ctas * splits * p.hk;
+        plan->dense = (int64_t)p.num_seqs * p.max_seqlen_q * 4 <= (int64_t)p.total_q * 5 &&
+                      grid >= 2LL * num_sms && grid <= 0x7fffffffLL;
+        if (plan->dense) {
+            plan->launches = splits > 1 ? 2 : 1;
+        } else {
+            // Persistent CTAs: one per SM, fewer when the call has fewer
+            // units (bounded from the host-side maxima).
+            plan->ctas = (int)std::max<int64_t>(1, std::min<int64_t>(num_sms, grid));
+            plan->launches = splits > 1 ? 3 : 2;   // planner, kernel[, combine]
+        }
     } else {
         plan->launches = splits > 1 ? 2 : 1;
     }
@@ -682,7 +693,9 @@ cudaError_t launch_prefill(const PrefillPlan& plan, const CUtensorMap& tm_k, con
     cuuint32_t box[3] = {64, (cuuint32_t)p.g, (cuuint32_t)(kRows / p.g)};
     if (!encode_bf16_sw128(&tq, p.q, 3, dims, strides, box)) return cudaErrorInvalidValue;
     if (plan.num_tiles <= 0) return cudaSuccess;
-    if (prefill_pair_supported(p.d)) return launch_prefill_pair(tq, tm_k, tm_v, p, plan.ctas, stream);
+    if (prefill_pair_supported(p.d))
+        return plan.dense ? launch_prefill_grid(tq, tm_k, tm_v, p, (plan.num_tiles + 1) / 2, stream)
+                          : launch_prefill_pair(tq, tm_k, tm_v, p, plan.ctas, stream);
     const bool qq = (p.flags & UA_FLAG_QQ_BIAS) != 0;
     const bool plain = !qq && (p.flags & (UA_FLAG_SOFTCAP | UA_FLAG_ALIBI)) == 0;
     if (p.d != 256) return cudaErrorInvalidValue;

@@ -11,6 +11,7 @@ struct PrefillPlan {
     int splits = 1;        // KV segments per tile (1 = the kernel writes O itself)
     int chunk = 0;         // keys per segment (a multiple of the KV tile)
     int ctas = 0;          // persistent CTAs of the two-tile kernel (one per SM at most)
+    bool dense = false;    // two-tile kernel as one CTA per unit over the padded grid
     int launches = 0;      // kernels enqueued per call
 };
 
@@ -33,6 +34,12 @@ bool prefill_pair_supported(int d);
 // the two-tile kernel for a call with `splits` segments:
 // (total_q / (2 floor(128 / g)) + num_seqs) * splits.
 int64_t pair_work_entries_bound(const FwdParams& p, int splits);
+
+// Enqueue the two-tile kernel as one CTA per (tile pair, KV head, sequence[,
+// segment]) over the padded grid of `pairs` tile pairs per sequence: the form
+// for batches whose padded grid is nearly all real units (ua_prefill_grid.cu).
+cudaError_t launch_prefill_grid(const CUtensorMap& tq, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                                const FwdParams& p, int pairs, cudaStream_t stream);
 
 // Enqueue the planner (the longest-first work list in p.work_list) and the
 // persistent two-tile kernel on `ctas` CTAs; tq is the Q tensor map (boxes of

@@ -303,3 +303,66 @@ def test_host_buffer_entry_point_matches_device_entry_point():
     assert st == 0
     assert prob.check_device_error() == 0
     assert torch.equal(out_h, dev.cpu())
+
+
+# ---------------------------------------------------------------------------
+# The two forms of the d <= 128 tensor-core prefill: dense batches (the padded
+# grid is nearly all real units and fills the GPU twice) run one CTA per unit
+# over the grid; ragged ones run persistent CTAs over the planner's
+# longest-first list.  Both are checked against the oracle and bit-exactly
+# on position tags, and each test asserts which form ran.
+# ---------------------------------------------------------------------------
+DENSE = dict(num_seqs=1, hq=128, hk=16, d=64, b=32, sq=(640, 640), ctx=(0, 0))
+
+
+@pytest.mark.parametrize("fl", [{}, dict(softcap=30.0, window=200, sinks=True), dict(alibi=True)])
+def test_dense_grid_form_matches_oracle(fl):
+    w = W.random_small(710, **DENSE, **fl)
+    want = oracle.forward_workload(w)
+    got, err, prob = run_gpu(w, path=ua.UA_PATH_TENSOR_CORE)
+    assert prob.last_path() == "tensor_core_grid"
+    assert err == 0
+    check_close(got, want)
+
+
+def test_ragged_batch_takes_the_persistent_form():
+    w = W.random_small(711, num_seqs=6, hq=8, hk=2, d=128, b=16, sq=(1, 300), ctx=(0, 500),
+                       softcap=20.0)
+    want = oracle.forward_workload(w)
+    got, err, prob = run_gpu(w, path=ua.UA_PATH_TENSOR_CORE)
+    assert prob.last_path().startswith("tensor_core_pair")
+    assert err == 0
+    check_close(got, want)
+
+
+def test_dense_grid_form_position_tags_bit_exact():
+    sq = sk = [640]
+    d, b, hq, hk = 64, 32, 128, 16
+    need = sum((k + b - 1) // b for k in sk)
+    w = W.build("tags", hq, hk, d, b, sq, sk, need + 3, 1.0, seed=12, values=False, poison=True,
+                bt_pad=1)
+    q = torch.zeros(w.total_q, hq, d)
+    kl = [torch.zeros(k, hk, d) for k in sk]
+    g = torch.Generator().manual_seed(13)
+    # S_q > d: rows i and i + d share the query direction i mod d, so rows
+    # sharing a direction share one target key, drawn from the keys the first
+    # of them (position i mod d, ctx = 0) already sees.
+    target = [[int(torch.randint(0, a + 1, (1,), generator=g)) for a in range(d)] for _ in range(hk)]
+    for tok, (s, i, ctx) in enumerate(token_of_row(w)):
+        q[tok, :, i % d] = 1.0
+        for hkv in range(hk):
+            kl[s][target[hkv][i % d], hkv, i % d] = 64.0
+    w.q = q.to(torch.bfloat16)
+    scatter_logical(w, kl, [position_tags(k, hk, d) for k in sk])
+    got, err, prob = run_gpu(w, path=ua.UA_PATH_TENSOR_CORE)
+    assert prob.last_path() == "tensor_core_grid"
+    assert err == 0
+    want = oracle.forward_workload(w)
+    for tok in range(w.total_q):
+        for h in range(hq):
+            exp_tag = decode_tag(want[tok, h])
+            assert exp_tag == (target[h // (hq // hk)][tok % d], h // (hq // hk))
+            row = got[tok, h].numpy()
+            assert decode_tag(row) == exp_tag
+            assert tuple(float(x) for x in row[:4]) == tuple(float(x) for x in tag_values(*exp_tag))
+            assert np.all(row[4:] == 0)

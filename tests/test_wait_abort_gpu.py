@@ -37,6 +37,9 @@ CASES = {
                                              ctx=(100, 2000))),
     "prefill_pair": (ua.UA_PATH_TENSOR_CORE, dict(num_seqs=4, hq=16, hk=2, d=128, b=32, sq=(60, 300),
                                                   ctx=(0, 400), softcap=30.0)),
+    # one dense sequence: the one-CTA-per-unit grid form of the same kernel
+    "prefill_grid": (ua.UA_PATH_TENSOR_CORE, dict(num_seqs=1, hq=128, hk=16, d=64, b=32, sq=(640, 640),
+                                                  ctx=(0, 0))),
 }
 
 
