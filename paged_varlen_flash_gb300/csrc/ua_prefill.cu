@@ -627,14 +627,15 @@ bool prefill_supported(int d) { return d == 64 || d == 128 || d == 256; }
 void plan_prefill(const FwdParams& p, int num_sms, size_t workspace_bytes, PrefillPlan* plan) {
     *plan = PrefillPlan();
     plan->kv_box_rows = p.b;
-    const int bn = p.d == 256 ? 64 : 128;
+    const int bn = 128;   // keys per KV tile of every tensor-core prefill kernel
     const int ppt = kRows / p.g;
     plan->num_tiles = (p.max_seqlen_q + ppt - 1) / ppt;
     // Split the keys into segments only when the (tile, kv head, sequence)
     // grid is too small to give every SM about four CTAs; each segment keeps
     // at least eight KV tiles.
     // CTAs per (sequence, kv head): tile pairs where the pair kernel serves d.
-    const int ctas = prefill_pair_supported(p.d) ? (plan->num_tiles + 1) / 2 : plan->num_tiles;
+    // (the d = 256 kernel runs the tiles of a pair on two CTAs of a cluster)
+    const int ctas = prefill_pair_supported(p.d) ? (plan->num_tiles + 1) / 2 : 2 * ((plan->num_tiles + 1) / 2);
     const int64_t base = (int64_t)ctas * p.hk * p.num_seqs;
     int splits = 1;
     if (base < 4LL * num_sms) {
@@ -696,12 +697,8 @@ cudaError_t launch_prefill(const PrefillPlan& plan, const CUtensorMap& tm_k, con
     if (prefill_pair_supported(p.d))
         return plan.dense ? launch_prefill_grid(tq, tm_k, tm_v, p, (plan.num_tiles + 1) / 2, stream)
                           : launch_prefill_pair(tq, tm_k, tm_v, p, plan.ctas, stream);
-    const bool qq = (p.flags & UA_FLAG_QQ_BIAS) != 0;
-    const bool plain = !qq && (p.flags & (UA_FLAG_SOFTCAP | UA_FLAG_ALIBI)) == 0;
     if (p.d != 256) return cudaErrorInvalidValue;
-    if (qq) return launch_t<256, 64, 2, 2, 2, false, true>(tq, tm_k, tm_v, p, plan.num_tiles, stream);
-    return plain ? launch_t<256, 64, 2, 2, 2, true>(tq, tm_k, tm_v, p, plan.num_tiles, stream)
-                 : launch_t<256, 64, 2, 2, 2, false>(tq, tm_k, tm_v, p, plan.num_tiles, stream);
+    return launch_prefill_cta2(tq, tm_k, tm_v, p, (plan.num_tiles + 1) / 2, stream);
 }
 
 }  // namespace ua

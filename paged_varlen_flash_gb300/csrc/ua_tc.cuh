@@ -75,6 +75,59 @@ __device__ __forceinline__ void commit(uint32_t bar) {
         : "memory");
 }
 
+// ---- CTA pairs (cta_group::2) -------------------------------------------------
+// A kernel uses one cta_group throughout.  With two, one warp of each CTA of
+// the pair allocates (the same columns in both CTAs' tensor memory), and one
+// thread of the pair issues each MMA: M = 256 rows, rows 0-127 in the tensor
+// memory (and A rows in the shared memory) of CTA 0 and rows 128-255 in CTA
+// 1; the B operand's N columns are split the same way, N / 2 held by each CTA
+// at the same shared-memory offset.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t smem_result_addr, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_result_addr),
+                 "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish_pair() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// A from tensor memory: each CTA's lanes hold its 128 rows of A.
+__device__ __forceinline__ void mma_bf16_ts_pair(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                 uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive once on the mbarrier at `bar_cluster` (a shared::cluster address in
+// either CTA of the pair) when every MMA this thread issued has completed.
+__device__ __forceinline__ void commit_pair(uint32_t bar_cluster) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            bar_cluster)
+        : "memory");
+}
+
 // ---- tensor memory <-> registers (32 lanes x 32 consecutive columns) --------
 __device__ __forceinline__ void ld32(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile(
