@@ -29,13 +29,14 @@
 // Roles (11 warps per CTA):
 //   warps 0-7  softmax + epilogue: two warpgroups share each row's 128 key
 //              columns (64 each; one shared-memory max exchange per tile);
-//   warp 8     TMA producer: Q tile once, this CTA's 64 keys of each K tile
-//              and its 128 columns of d of each V tile through 2-stage rings
-//              (K completes on CTA 0's barrier directly; V on a local one);
+//   warp 8     TMA producer of Q (once) and of this CTA's 64 keys of each K
+//              tile, through a 2-stage ring; the copies complete on CTA 0's
+//              barrier directly;
 //   warp 9     tensor-memory allocation (both CTAs) and, in CTA 0, the MMA
 //              issuer;
-//   warp 10    V release: waits for this CTA's V copy, zeroes the rows past
-//              S_k of the sequence's last tile, then signals CTA 0.
+//   warp 10    TMA producer of this CTA's 128 columns of d of each V tile
+//              (2-stage ring, completing on a local barrier); zeroes the rows
+//              past S_k of the sequence's last tile, then signals CTA 0.
 #include <algorithm>
 #include <cstdint>
 
@@ -210,14 +211,16 @@ prefill_cta2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     };
     auto v_blocks = [&](int key0) { return max(0, min(kBN / b, nblk_seq - key0 / b)); };
 
+    const int32_t* bt = p.block_table + (int64_t)s * p.bt_stride;
     if (warp == kWarpTma2) {
-        // ------------------------------ TMA producer ------------------------------
-        // Lane i owns paged block i of this CTA's share of each tile (its id
-        // load and its boxes), so a tile's boxes go out in parallel.
+        // --------------------------- TMA producer: Q, K ---------------------------
+        // Lane i owns paged block i of this CTA's 64 keys of each K tile (its
+        // id load and its boxes), so a tile's boxes go out in parallel.  K runs
+        // ahead of V on its own warp: the next K tile is requested as soon as
+        // the QK^T two tiles back has read its stage.
         if (lane == 0) {
             tma_prefetch_desc(&tm_q);
             tma_prefetch_desc(&tm_k);
-            tma_prefetch_desc(&tm_v);
             // g heads x ppt positions per panel and tile, both tiles of the pair
             if (rank == 0)
                 mbar_arrive_expect_tx(q_full, 2u * (uint32_t)(g * ppt) * 128u * C::kPanels);
@@ -226,25 +229,18 @@ prefill_cta2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 tma_load_3d_pair(sQ + pn * C::kQPanel, &tm_q, pn * 64, hkv * g, (int)(q0 + p0),
                                  mapa_shared(q_full, 0));
         }
-        const int32_t* bt = p.block_table + (int64_t)s * p.bt_stride;
-        auto tile_id = [&](int j) -> int32_t {   // lane i: block i of V's 128 keys
-            const int blk0 = (t_last - j) * kBN / b;
-            return lane < min(kBN / b, nblk_seq - blk0) ? __ldg(bt + blk0 + lane) : 0;
+        auto tile_id = [&](int j) -> int32_t {   // lane i: block i of this CTA's K keys
+            const int blk0 = ((t_last - j) * kBN + (int)rank * kHalfKeys) / b;
+            return lane < min(kHalfKeys / b, nblk_seq - blk0) ? __ldg(bt + blk0 + lane) : 0;
         };
         const uint32_t k_full_lead0 = mapa_shared(k_full0, 0);
-        int issued = 0;
         int32_t id_next = tile_id(0);
         for (int j = 0; j < n_tiles; ++j) {
-            const int stk = j % NK, stv = j % NV;
+            const int stk = j % NK;
             const int key0 = (t_last - j) * kBN;
             const int nbk = k_blocks(key0, rank);
-            const int nbv = v_blocks(key0);
             const int32_t id = id_next;
             if (j + 1 < n_tiles) id_next = tile_id(j + 1);
-            if (lane < nbv && (id < 0 || (int64_t)id >= p.num_blocks))
-                atomicOr(p.err, (int)UA_DEVERR_BLOCK_ID);
-            // K: this CTA's 64 keys are V's blocks rank * 64 / b onwards.
-            const int32_t idk = __shfl_sync(0xffffffffu, id, min(31, (int)rank * (kHalfKeys / b) + lane));
             if (j >= NK && !__all_sync(0xffffffffu, wait_or_abort(k_empty0 + 8 * stk, ((j / NK) + 1) & 1,
                                                                    abort_flag, p.err)))
                 break;
@@ -257,11 +253,30 @@ prefill_cta2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
 #pragma unroll
                 for (int pn = 0; pn < C::kPanels; ++pn)
                     tma_load_4d_pair(sK + stk * C::kKBytes + pn * C::kKPanel + lane * b * 128, &tm_k,
-                                     pn * 64, hkv, 0, idk, k_full_lead0 + 8 * stk);
+                                     pn * 64, hkv, 0, id, k_full_lead0 + 8 * stk);
             }
+        }
+        __syncwarp();
+    } else if (warp == kWarpRel2) {
+        // ------------------- V producer, zero fill and release --------------------
+        // Lane i owns paged block i of each V tile's 128 keys (this CTA's 128
+        // columns of d).  Keys past S_k: whatever their V slots hold must not
+        // reach O (0 * NaN is NaN), so those rows become zeros before CTA 0 is
+        // told the tile is ready.  V(j + NV) is requested once the P.V of
+        // tile j has read its stage.
+        if (lane == 0) tma_prefetch_desc(&tm_v);
+        const uint32_t v_full_lead0 = mapa_shared(v_full0, 0);
+        auto issue_v = [&](int j) -> bool {
+            const int stv = j % NV;
+            const int key0 = (t_last - j) * kBN;
+            const int nbv = v_blocks(key0);
+            const int blk0 = key0 / b;
+            const int32_t id = lane < nbv ? __ldg(bt + blk0 + lane) : 0;
+            if (lane < nbv && (id < 0 || (int64_t)id >= p.num_blocks))
+                atomicOr(p.err, (int)UA_DEVERR_BLOCK_ID);
             if (j >= NV && !__all_sync(0xffffffffu, wait_or_abort(v_empty0 + 8 * stv, ((j / NV) + 1) & 1,
                                                                    abort_flag, p.err)))
-                break;
+                return false;
             if (lane == 0) mbar_arrive_expect_tx(v_land0 + 8 * stv, (uint32_t)nbv * b * 128 * 2);
             __syncwarp();
             if (lane < nbv) {
@@ -270,24 +285,14 @@ prefill_cta2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                     tma_load_4d(sV + stv * C::kVBytes + pn * C::kVPanel + lane * b * 128, &tm_v,
                                 ((int)rank * 2 + pn) * 64, hkv, 0, id, v_land0 + 8 * stv);
             }
-            issued = j + 1;
-        }
-        if (*abort_flag && lane == 0) {
-            // Let the V copies this warp issued land before the CTA ends (the
-            // K copies complete on CTA 0's barrier, which CTA 0 drains).
-            for (int j = max(0, issued - NV); j < issued; ++j)
-                mbar_wait_bounded(v_land0 + 8 * (j % NV), (j / NV) & 1);
-        }
-        __syncwarp();
-    } else if (warp == kWarpRel2) {
-        // ------------------------------- V release --------------------------------
-        // Keys past S_k: whatever their V slots hold must not reach O (0 * NaN
-        // is NaN), so those rows become zeros before CTA 0 is told the tile is
-        // ready.
-        const uint32_t v_full_lead0 = mapa_shared(v_full0, 0);
-        for (int j = 0; j < n_tiles; ++j) {
+            return true;
+        };
+        int issued = 0;
+        bool ok = true;
+        for (; ok && issued < min(NV, n_tiles); ++issued) ok = issue_v(issued);
+        for (int j = 0; ok && j < n_tiles; ++j) {
             const int stv = j % NV;
-            if (!__all_sync(0xffffffffu, wait_or_abort(v_land0 + 8 * stv, (j / NV) & 1, abort_flag, p.err)))
+            if (!(ok = __all_sync(0xffffffffu, wait_or_abort(v_land0 + 8 * stv, (j / NV) & 1, abort_flag, p.err))))
                 break;
             const int key0 = (t_last - j) * kBN;
             const int nvalid = min(kBN, sk - key0);
@@ -303,7 +308,17 @@ prefill_cta2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             }
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(v_full_lead0 + 8 * stv);
+            if (issued < n_tiles && (ok = issue_v(issued))) ++issued;
         }
+        if (*abort_flag && lane == 0) {
+            // Let the V copies this warp issued land before the CTA ends (the
+            // K copies complete on CTA 0's barrier and land within
+            // microseconds; the pair leaves only after the final cluster
+            // barrier, at least one wait limit later).
+            for (int j = max(0, issued - NV); j < issued; ++j)
+                mbar_wait_bounded(v_land0 + 8 * (j % NV), (j / NV) & 1);
+        }
+        __syncwarp();
     } else if (warp == kWarpMma2) {
         if (rank == 0) {
             // ------------------------ MMA issuer (CTA 0, one thread) ------------------------
