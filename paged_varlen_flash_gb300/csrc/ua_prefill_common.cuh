@@ -49,25 +49,6 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
     }
 }
 
-// The same for a barrier that the other CTA of a pair arrives on (acquire at
-// cluster scope).
-__device__ __forceinline__ bool wait_or_abort_cluster(uint32_t bar, uint32_t parity,
-                                                      volatile int* abort_flag, int32_t* err,
-                                                      uint64_t limit_ns = kWaitLimitNs) {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
-    const uint64_t start = global_ns();
-    for (;;) {
-        for (int i = 0; i < 128; ++i)
-            if (mbar_try_wait_cluster(bar, parity)) return true;
-        if (*abort_flag) return false;
-        if (global_ns() - start > limit_ns) {
-            *abort_flag = 1;
-            atomicOr(err, (int)UA_DEVERR_TIMEOUT);
-            return false;
-        }
-    }
-}
-
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
     float d;
     asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));

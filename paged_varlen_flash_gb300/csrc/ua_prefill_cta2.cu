@@ -326,7 +326,7 @@ prefill_cta2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             constexpr uint32_t idesc_pv = tc::idesc_bf16_f32(2 * kRows, kD, false, true);
             const uint32_t peer = 1;
             auto wwait = [&](uint32_t bar, uint32_t par) {
-                return __all_sync(0xffffffffu, wait_or_abort_cluster(bar, par, abort_flag, p.err));
+                return __all_sync(0xffffffffu, wait_or_abort(bar, par, abort_flag, p.err));
             };
             auto commit_both = [&](uint32_t bar) {
                 tc::commit_pair(bar);
@@ -421,8 +421,8 @@ prefill_cta2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         bool ok = true;
         for (int j = 0; j < n_tiles; ++j) {
             const uint32_t sbuf = (uint32_t)(j & 1) * kBN;
-            const bool got = __all_sync(0xffffffffu, wait_or_abort_cluster(s_full0 + 8 * (j & 1), (j >> 1) & 1,
-                                                                           abort_flag, p.err));
+            const bool got = __all_sync(0xffffffffu, wait_or_abort(s_full0 + 8 * (j & 1), (j >> 1) & 1,
+                                                                   abort_flag, p.err));
             uint32_t sr[kCPT / 32][32];
             const int key0 = (t_last - j) * kBN + half * kCPT;
             float pmax = -INFINITY;
@@ -533,8 +533,8 @@ prefill_cta2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             // Rescaling O needs the P.V of tile j - 1 to have finished.
             bool go = true;
             if (live && j > 0 && __any_sync(0xffffffffu, reanchor)) {
-                go = __all_sync(0xffffffffu, wait_or_abort_cluster(pv_done0 + 8 * ((j - 1) & 1),
-                                                                   ((j - 1) >> 1) & 1, abort_flag, p.err));
+                go = __all_sync(0xffffffffu, wait_or_abort(pv_done0 + 8 * ((j - 1) & 1),
+                                                           ((j - 1) >> 1) & 1, abort_flag, p.err));
                 if (go) {
                     tc::fence_after_sync();
 #pragma unroll 1
@@ -569,8 +569,8 @@ prefill_cta2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         // ------------------------------ epilogue ---------------------------------
         if (ok) {
             const bool done = __all_sync(0xffffffffu,
-                                         wait_or_abort_cluster(pv_done0 + 8 * ((n_tiles - 1) & 1),
-                                                               ((n_tiles - 1) >> 1) & 1, abort_flag, p.err));
+                                         wait_or_abort(pv_done0 + 8 * ((n_tiles - 1) & 1),
+                                                       ((n_tiles - 1) >> 1) & 1, abort_flag, p.err));
             red[half * kRows + r] = l;
             const bool all_done = bar_and_sync(1, kSmThreads2, done);
             if (all_done && live && split) {
