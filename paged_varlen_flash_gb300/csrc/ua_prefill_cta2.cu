@@ -325,6 +325,13 @@ prefill_cta2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(2 * kRows, kBN, false, false);
             constexpr uint32_t idesc_pv = tc::idesc_bf16_f32(2 * kRows, kD, false, true);
             const uint32_t peer = 1;
+            // Shared-memory descriptors as a base per operand buffer plus a
+            // compile-time offset per MMA: the start-address field holds the
+            // byte address >> 4 (below 2^14 for any shared-memory address), so
+            // adding an offset never carries into the next field.
+            const uint64_t q_desc = tc::smem_desc_sw128(sQ, 16, 1024);
+            const uint64_t k_desc0 = tc::smem_desc_sw128(sK, 16, 1024);
+            const uint64_t v_desc0 = tc::smem_desc_sw128(sV, C::kVPanel, 1024);
             auto wwait = [&](uint32_t bar, uint32_t par) {
                 return __all_sync(0xffffffffu, wait_or_abort(bar, par, abort_flag, p.err));
             };
@@ -343,13 +350,12 @@ prefill_cta2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 tc::fence_after_sync();
                 if (lane == 0) {
                     const uint32_t dS = tmem + (j & 1) * kBN;
-                    const uint32_t kst = sK + stg * C::kKBytes;
+                    const uint64_t kd_s = k_desc0 + (uint64_t)(((uint32_t)stg * C::kKBytes) >> 4);
 #pragma unroll
                     for (int k = 0; k < kD / 16; ++k) {
-                        const int pn = k >> 2, off = (k & 3) * 32;
-                        const uint64_t a = tc::smem_desc_sw128(sQ + pn * C::kQPanel + off, 16, 1024);
-                        const uint64_t bd = tc::smem_desc_sw128(kst + pn * C::kKPanel + off, 16, 1024);
-                        tc::mma_bf16_pair(dS, a, bd, idesc_qk, k > 0 ? 1u : 0u);
+                        const uint32_t oq = ((k >> 2) * C::kQPanel + (k & 3) * 32) >> 4;
+                        const uint32_t ok_ = ((k >> 2) * C::kKPanel + (k & 3) * 32) >> 4;
+                        tc::mma_bf16_pair(dS, q_desc + oq, kd_s + ok_, idesc_qk, k > 0 ? 1u : 0u);
                     }
                     commit_both(s_full0 + 8 * (j & 1));
                     commit_both(k_empty0 + 8 * stg);
@@ -366,13 +372,12 @@ prefill_cta2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 if (!(ok = wwait(v_full0 + 8 * stv, (j / NV) & 1))) break;
                 tc::fence_after_sync();
                 if (lane == 0) {
-                    const uint32_t vst = sV + stv * C::kVBytes;
+                    const uint64_t vd_s = v_desc0 + (uint64_t)(((uint32_t)stv * C::kVBytes) >> 4);
                     const uint32_t aP = tmem + (j & 1) * kBN;
 #pragma unroll
                     for (int k = 0; k < kBN / 16; ++k) {
                         // A = P from tensor memory: 16 keys per MMA = 8 columns.
-                        const uint64_t bd = tc::smem_desc_sw128(vst + k * 16 * 128, C::kVPanel, 1024);
-                        tc::mma_bf16_ts_pair(tmem + C::kTmemO, aP + k * 8, bd, idesc_pv,
+                        tc::mma_bf16_ts_pair(tmem + C::kTmemO, aP + k * 8, vd_s + ((k * 16 * 128) >> 4), idesc_pv,
                                              (j > 0 || k > 0) ? 1u : 0u);
                     }
                     commit_both(v_empty0 + 8 * stv);
