@@ -53,7 +53,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 KERNEL_SOURCES = {
     "split_kernel": ["ua_split.cu", "ua_ptx.cuh", "ua_common.cuh"],
-    "prefill_kernel": ["ua_prefill.cu", "ua_prefill_common.cuh", "ua_ptx.cuh", "ua_common.cuh", "ua_tc.cuh"],
+    "prefill_cta2_kernel": ["ua_prefill_cta2.cu", "ua_prefill_common.cuh", "ua_ptx.cuh", "ua_common.cuh",
+                            "ua_tc.cuh"],
     "prefill_pair_kernel": ["ua_prefill_pair.cu", "ua_prefill_common.cuh", "ua_ptx.cuh", "ua_common.cuh",
                             "ua_tc.cuh"],
     "prefill_grid_kernel": ["ua_prefill_grid.cu", "ua_prefill_common.cuh", "ua_ptx.cuh", "ua_common.cuh",
@@ -200,8 +201,8 @@ def dominant_kernel(path):
         return "prefill_pair_kernel"
     if path.startswith("tensor_core_grid"):
         return "prefill_grid_kernel"
-    if path.startswith("tensor_core"):
-        return "prefill_kernel"
+    if path.startswith("tensor_core_cta2"):
+        return "prefill_cta2_kernel"
     return "split_kernel"
 
 

@@ -429,7 +429,7 @@ ua_status ua_forward(ua_problem* p, const void* q, const void* k_cache, const vo
         else if (ua::prefill_pair_supported(fp.d))
             p->last_path = plan.splits > 1 ? "tensor_core_pair+combine" : "tensor_core_pair";
         else
-            p->last_path = plan.splits > 1 ? "tensor_core+combine" : "tensor_core";
+            p->last_path = plan.splits > 1 ? "tensor_core_cta2+combine" : "tensor_core_cta2";
         return UA_OK;
     }
 

@@ -85,7 +85,7 @@ def test_traffic_record_goes_stale_when_the_kernel_changes(tmp_path, monkeypatch
 def test_dominant_kernel_follows_the_reported_path():
     assert bench.dominant_kernel("decode_tc+combine") == "decode_tc_kernel"
     assert bench.dominant_kernel("topk_tc+combine") == "topk_kernel"
-    assert bench.dominant_kernel("tensor_core") == "prefill_kernel"
+    assert bench.dominant_kernel("tensor_core_cta2") == "prefill_cta2_kernel"
     assert bench.dominant_kernel("tensor_core_pair+combine") == "prefill_pair_kernel"
     assert bench.dominant_kernel("tensor_core_grid") == "prefill_grid_kernel"
     assert bench.dominant_kernel("split_kv+combine") == "split_kernel"

@@ -31,7 +31,7 @@ CASES = [
     (ua.UA_PATH_TENSOR_CORE, "tensor_core_pair+combine", 128, 32, 8, 2, [200], [3200], {}),
     (ua.UA_PATH_TENSOR_CORE, "tensor_core_pair+combine", 64, 16, 4, 4, [150], [2500],
      dict(alibi=True, sinks=True)),
-    (ua.UA_PATH_TENSOR_CORE, "tensor_core+combine", 256, 64, 4, 2, [150], [3000], {}),
+    (ua.UA_PATH_TENSOR_CORE, "tensor_core_cta2+combine", 256, 64, 4, 2, [150], [3000], {}),
     (ua.UA_PATH_SPLIT_KV, "split_kv+combine", 128, 16, 8, 2, [1, 3], [3000, 2000],
      dict(window=700)),
 ]

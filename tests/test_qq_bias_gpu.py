@@ -40,9 +40,9 @@ CASES = [
      dict(causal=False)),
     (ua.UA_PATH_TENSOR_CORE, "tensor_core_pair", 128, 64, 16, 2, (30, 200), (0, 400),
      dict(softcap=30.0, alibi=True, window=150, sinks=True)),
-    (ua.UA_PATH_TENSOR_CORE, "tensor_core", 256, 32, 4, 2, (50, 260), (0, 150),
+    (ua.UA_PATH_TENSOR_CORE, "tensor_core_cta2", 256, 32, 4, 2, (50, 260), (0, 150),
      dict(alibi=True)),
-    (ua.UA_PATH_TENSOR_CORE, "tensor_core", 256, 16, 2, 1, (100, 200), (0, 60),
+    (ua.UA_PATH_TENSOR_CORE, "tensor_core_cta2", 256, 16, 2, 1, (100, 200), (0, 60),
      dict(causal=False, softcap=20.0)),
     (ua.UA_PATH_SPLIT_KV, "split_kv", 128, 16, 8, 2, (1, 70), (0, 300), {}),
     (ua.UA_PATH_SPLIT_KV, "split_kv", 64, 32, 6, 3, (1, 40), (0, 500),
