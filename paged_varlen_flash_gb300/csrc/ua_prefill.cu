@@ -92,7 +92,9 @@ cudaError_t launch_prefill(const PrefillPlan& plan, const CUtensorMap& tm_k, con
         return plan.dense ? launch_prefill_grid(tq, tm_k, tm_v, p, (plan.num_tiles + 1) / 2, stream)
                           : launch_prefill_pair(tq, tm_k, tm_v, p, plan.ctas, stream);
     if (p.d != 256) return cudaErrorInvalidValue;
-    return launch_prefill_cta2(tq, tm_k, tm_v, p, (plan.num_tiles + 1) / 2, stream);
+    CUtensorMap to;   // the output, boxed like Q
+    if (!encode_bf16_sw128(&to, p.out, 3, dims, strides, box)) return cudaErrorInvalidValue;
+    return launch_prefill_cta2(tq, tm_k, tm_v, to, p, (plan.num_tiles + 1) / 2, stream);
 }
 
 }  // namespace ua

@@ -50,8 +50,9 @@ cudaError_t launch_prefill_pair(const CUtensorMap& tq, const CUtensorMap& tm_k, 
 // Enqueue the head-size-256 kernel on CTA pairs: one cluster of two CTAs per
 // (pair of adjacent query tiles, KV head, sequence[, segment]) over the padded
 // grid of `pairs` tile pairs per sequence (ua_prefill_cta2.cu).
+// `to` maps the output like tq maps Q (full tiles are stored through it).
 cudaError_t launch_prefill_cta2(const CUtensorMap& tq, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
-                                const FwdParams& p, int pairs, cudaStream_t stream);
+                                const CUtensorMap& to, const FwdParams& p, int pairs, cudaStream_t stream);
 
 // Enqueue the prefill path (p.out receives the final bf16 rows).
 cudaError_t launch_prefill(const PrefillPlan& plan, const CUtensorMap& tm_k,

@@ -89,7 +89,8 @@ struct C2Cfg {
 template <int NK, int NV, bool PLAIN, bool QQ>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads2, 1)
 prefill_cta2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                    const FwdParams p) {
     using C = C2Cfg<NK, NV>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -597,42 +598,72 @@ prefill_cta2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                     tc::wait_ld();
                     if (row_valid) part_store32(p, po + c * 32, o);
                 }
-            } else if (all_done && live && !split) {
-                tc::fence_after_sync();
-                float O_scale_num = 1.f;  // extra factor from the sink re-basing
-                float L = l;
+            } else if (all_done && !split) {
+                // A tile whose rows are all valid goes out through shared
+                // memory (the K stages, free once the last MMA has run) and
+                // one TMA store per 64-column panel: rows of a tile lie H_q * d
+                // elements apart in the output, so per-thread row stores
+                // would touch one sector per lane.  The last tile of a
+                // sequence, whose padding rows must not be written, keeps
+                // the per-thread stores.
+                const bool staged = p_last - p0 + 1 == ppt;
+                const uint32_t sO = smem_u32(smem + C::kOffK);
+                static_assert(NK * C::kKBytes >= C::kPanels * C::kQPanel, "output staging");
+                if (live) {
+                    tc::fence_after_sync();
+                    float O_scale_num = 1.f;  // extra factor from the sink re-basing
+                    float L = l;
 #pragma unroll
-                for (int o = 1; o < kSplit; ++o) L += red[((half + o) % kSplit) * kRows + r];
-                bool zero = false;
-                if (p.flags & UA_FLAG_SINKS) {
-                    const float s2 = __ldg(p.sinks + head) * kLog2e;
-                    if (s2 == INFINITY) {
-                        zero = true;
-                    } else if (s2 > m) {
-                        const float a = (m == -INFINITY) ? 0.f : fast_exp2(m - s2);
-                        O_scale_num = a;
-                        L = L * a + 1.0f;
-                    } else if (s2 != -INFINITY) {
-                        L += fast_exp2(s2 - m);
+                    for (int o = 1; o < kSplit; ++o) L += red[((half + o) % kSplit) * kRows + r];
+                    bool zero = false;
+                    if (p.flags & UA_FLAG_SINKS) {
+                        const float s2 = __ldg(p.sinks + head) * kLog2e;
+                        if (s2 == INFINITY) {
+                            zero = true;
+                        } else if (s2 > m) {
+                            const float a = (m == -INFINITY) ? 0.f : fast_exp2(m - s2);
+                            O_scale_num = a;
+                            L = L * a + 1.0f;
+                        } else if (s2 != -INFINITY) {
+                            L += fast_exp2(s2 - m);
+                        }
+                    }
+                    const float inv = (!zero && L > 0.f) ? O_scale_num * __frcp_rn(L) : 0.f;
+                    __nv_bfloat16* orow = p.out + ((q0 + i) * p.hq + head) * (int64_t)kD + half * kOPT;
+#pragma unroll 1
+                    for (int c = 0; c < kOPT / 32; ++c) {
+                        uint32_t o[32];
+                        tc::ld32(trow + C::kTmemO + half * kOPT + c * 32, o);
+                        tc::wait_ld();
+                        if (row_valid) {
+#pragma unroll
+                            for (int e = 0; e < 32; e += 8) {
+                                uint4 v;
+                                v.x = pack_bf16x2(__uint_as_float(o[e + 0]) * inv, __uint_as_float(o[e + 1]) * inv);
+                                v.y = pack_bf16x2(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
+                                v.z = pack_bf16x2(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv);
+                                v.w = pack_bf16x2(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv);
+                                if (staged) {
+                                    // panel half * 2 + c / 2, 16-byte chunk (c % 2) * 4 + e / 8
+                                    // of row r, 128-byte swizzled like the map's boxes
+                                    const int chunk = (c & 1) * 4 + e / 8;
+                                    *reinterpret_cast<uint4*>(smem + C::kOffK + (half * 2 + c / 2) * C::kQPanel +
+                                                              r * 128 + ((chunk ^ (r & 7)) * 16)) = v;
+                                } else {
+                                    *reinterpret_cast<uint4*>(orow + c * 32 + e) = v;
+                                }
+                            }
+                        }
                     }
                 }
-                const float inv = (!zero && L > 0.f) ? O_scale_num * __frcp_rn(L) : 0.f;
-                __nv_bfloat16* orow = p.out + ((q0 + i) * p.hq + head) * (int64_t)kD + half * kOPT;
-#pragma unroll 1
-                for (int c = 0; c < kOPT / 32; ++c) {
-                    uint32_t o[32];
-                    tc::ld32(trow + C::kTmemO + half * kOPT + c * 32, o);
-                    tc::wait_ld();
-                    if (row_valid) {
+                if (staged) {
+                    fence_proxy_async_smem();
+                    bar_and_sync(1, kSmThreads2, true);
+                    if (threadIdx.x == 0) {
 #pragma unroll
-                        for (int e = 0; e < 32; e += 8) {
-                            uint4 v;
-                            v.x = pack_bf16x2(__uint_as_float(o[e + 0]) * inv, __uint_as_float(o[e + 1]) * inv);
-                            v.y = pack_bf16x2(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
-                            v.z = pack_bf16x2(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv);
-                            v.w = pack_bf16x2(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv);
-                            *reinterpret_cast<uint4*>(orow + c * 32 + e) = v;
-                        }
+                        for (int pn = 0; pn < C::kPanels; ++pn)
+                            tma_store_3d(&tm_o, pn * 64, hkv * g, (int)(q0 + p0), sO + pn * C::kQPanel);
+                        bulk_commit_and_wait_read();
                     }
                 }
             }
@@ -652,26 +683,26 @@ prefill_cta2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
 
 template <int NK, int NV, bool PLAIN, bool QQ = false>
 cudaError_t launch_cta2_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                          const FwdParams& p, int pairs, cudaStream_t stream) {
+                          const CUtensorMap& to, const FwdParams& p, int pairs, cudaStream_t stream) {
     using C = C2Cfg<NK, NV>;
     auto kern = prefill_cta2_kernel<NK, NV, PLAIN, QQ>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)(2 * pairs * p.splits), (unsigned)p.hk, (unsigned)p.num_seqs);
-    kern<<<grid, kThreads2, C::kSmem, stream>>>(tq, tk, tv, p);
+    kern<<<grid, kThreads2, C::kSmem, stream>>>(tq, tk, tv, to, p);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_prefill_cta2(const CUtensorMap& tq, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
-                                const FwdParams& p, int pairs, cudaStream_t stream) {
+                                const CUtensorMap& to, const FwdParams& p, int pairs, cudaStream_t stream) {
     if (p.d != kD || (p.b != 16 && p.b != 32 && p.b != 64)) return cudaErrorInvalidValue;
     const bool qq = (p.flags & UA_FLAG_QQ_BIAS) != 0;
     const bool plain = !qq && (p.flags & (UA_FLAG_SOFTCAP | UA_FLAG_ALIBI)) == 0;
-    if (qq) return launch_cta2_t<2, 2, false, true>(tq, tm_k, tm_v, p, pairs, stream);
-    return plain ? launch_cta2_t<2, 2, true>(tq, tm_k, tm_v, p, pairs, stream)
-                 : launch_cta2_t<2, 2, false>(tq, tm_k, tm_v, p, pairs, stream);
+    if (qq) return launch_cta2_t<2, 2, false, true>(tq, tm_k, tm_v, to, p, pairs, stream);
+    return plain ? launch_cta2_t<2, 2, true>(tq, tm_k, tm_v, to, p, pairs, stream)
+                 : launch_cta2_t<2, 2, false>(tq, tm_k, tm_v, to, p, pairs, stream);
 }
 
 }  // namespace ua

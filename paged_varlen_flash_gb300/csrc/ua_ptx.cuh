@@ -158,6 +158,24 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const void* tmap,
         : "memory");
 }
 
+// 3-D tiled store from shared memory (the box at src, laid out with the
+// map's swizzle) to global memory, tracked by the bulk async-group of the
+// issuing thread.
+__device__ __forceinline__ void tma_store_3d(const void* tmap, int32_t c0, int32_t c1, int32_t c2,
+                                             uint32_t src) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+            reinterpret_cast<uint64_t>(tmap)),
+        "r"(c0), "r"(c1), "r"(c2), "r"(src)
+        : "memory");
+}
+
+// Close the thread's bulk async-group and wait until every store in it has
+// read its shared-memory source.
+__device__ __forceinline__ void bulk_commit_and_wait_read() {
+    asm volatile("cp.async.bulk.commit_group;\n\tcp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
 // Row gather from a 2-D tensor map whose box is {cols, 1}: rows r0..r3 (each
 // `cols` wide from column c0) land as four consecutive box rows at dst, with
 // the map's swizzle, completion signalled on `bar` (tx bytes).
