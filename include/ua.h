@@ -277,12 +277,14 @@ ua_status ua_set_profile_events(ua_problem *p, void *ev_begin, void *ev_end);
  * gives up, the kernel sets UA_DEVERR_TIMEOUT, raises a CTA-wide abort flag so
  * that every role leaves its loop, waits (bounded) for the copies and
  * tensor-core operations it issued, frees its tensor memory and returns.
- * While this hook is enabled, the split, decode tensor-core and two-tile
- * prefill kernels of later forward calls make their first consumer-side K/V
- * data wait wait on a barrier that nothing completes, bounded by limit_ns
- * instead: the wait gives up, the call returns, ua_check_device_error reports
- * UA_DEVERR_TIMEOUT, and the outputs of that call are unspecified.  The
- * waits that drain a CTA's own copies and MMAs keep their normal bound.
+ * While this hook is enabled, the split, decode tensor-core, two-tile and
+ * CTA-pair prefill kernels of later forward calls make their first
+ * consumer-side K/V data wait wait on a barrier that nothing completes,
+ * bounded by limit_ns instead: the wait gives up, the call returns,
+ * ua_check_device_error reports UA_DEVERR_TIMEOUT, and the outputs of that
+ * call are unspecified.  (In the CTA-pair kernel only the MMA-issuing CTA
+ * stalls; its partner's waits give up on their normal bound.)  The waits
+ * that drain a CTA's own copies and MMAs keep their normal bound.
  * enable = 0 restores normal calls.  limit_ns must lie in [1e3, 1e9] when
  * enabling (else UA_ERR_INVALID_ARG).
  */

@@ -6,7 +6,9 @@ MMAs it issued, frees its tensor memory and returns, so that the context stays
 usable.  The testing hook ua_debug_stall_data_waits makes a kernel's first K/V
 data wait wait on a barrier that nothing completes (with a 2 ms bound): the
 call must return promptly with the TIMEOUT bit set, and the next normal call
-on the same problem must match the fp64 oracle.  The drain waits keep their
+on the same problem must match the fp64 oracle.  (In the CTA-pair kernel
+only CTA 0 stalls; the other CTA's waits give up on their normal one-second
+bound.)  The drain waits keep their
 normal bound, so no CTA leaves with a copy or an MMA in flight."""
 import time
 
@@ -40,6 +42,10 @@ CASES = {
     # one dense sequence: the one-CTA-per-unit grid form of the same kernel
     "prefill_grid": (ua.UA_PATH_TENSOR_CORE, dict(num_seqs=1, hq=128, hk=16, d=64, b=32, sq=(640, 640),
                                                   ctx=(0, 0))),
+    # d = 256: the CTA-pair kernel (CTA 0 stalls; CTA 1's waits run out on
+    # their normal bound, so each stalled call takes about a second)
+    "prefill_cta2": (ua.UA_PATH_TENSOR_CORE, dict(num_seqs=2, hq=8, hk=4, d=256, b=32, sq=(200, 300),
+                                                  ctx=(0, 300))),
 }
 
 
