@@ -142,3 +142,37 @@ def test_noalloc_path_field_is_checked():
     assert _noalloc(w, out, path=ua.UA_PATH_DECODE_TC) == 2
     assert _noalloc(w, out, path=7) == 1                        # UA_ERR_INVALID_ARG
     torch.cuda.synchronize()
+
+
+def test_noalloc_captured_in_a_cuda_graph():
+    # The use the entry point exists for: one warm-up call, then the call
+    # inside a stream capture (no allocation may happen there), replayed;
+    # a second replay after Q changed in place reads the new values.
+    w = W.random_small(34, num_seqs=4, hq=16, hk=4, d=128, b=16, sq=(1, 2), ctx=(100, 2000),
+                       softcap=25.0, sinks=True).to("cuda")
+    prob = ua.Problem.for_workload(w)
+    ref = prob.forward_workload(w)
+    out = torch.full_like(w.q, float("nan"))
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        assert _noalloc(w, out, err) == 0
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    out.fill_(float("nan"))
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        assert _noalloc(w, out, err) == 0
+    graph.replay()
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    _close(out, ref)
+    g = torch.Generator(device="cpu").manual_seed(35)
+    w.q.copy_(torch.randn(w.q.shape, generator=g).to(w.q.dtype))
+    ref2 = prob.forward_workload(w)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    _close(out, ref2)
+    assert not torch.equal(ref, ref2)
