@@ -22,21 +22,21 @@
 // O [256, 512); P(j) bf16 is written over the first 64 columns of S(j & 1)):
 //   S(j) = Q K(j)^T    M = 256, N = 128 keys (64 held by each CTA), K = 256
 //   O += P(j) V(j)     M = 256, N = 256 (128 of d held by each CTA), K = 128
-// The issuing thread sends P.V(j) before S(j + 2) = Q K(j + 2)^T, and MMAs of
-// one thread run in issue order, so the QK^T that overwrites P(j) cannot
-// overtake the P.V reading it.
+// S(j + 2) = Q K(j + 2)^T overwrites the columns that hold P(j), so its
+// issuer waits for P.V(j) to complete first.
 //
-// Roles (11 warps per CTA):
+// Roles (12 warps per CTA):
 //   warps 0-7  softmax + epilogue: two warpgroups share each row's 128 key
 //              columns (64 each; one shared-memory max exchange per tile);
 //   warp 8     TMA producer of Q (once) and of this CTA's 64 keys of each K
 //              tile, through a 2-stage ring; the copies complete on CTA 0's
 //              barrier directly;
-//   warp 9     tensor-memory allocation (both CTAs) and, in CTA 0, the MMA
+//   warp 9     tensor-memory allocation (both CTAs) and, in CTA 0, the QK^T
 //              issuer;
 //   warp 10    TMA producer of this CTA's 128 columns of d of each V tile
 //              (2-stage ring, completing on a local barrier); zeroes the rows
-//              past S_k of the sequence's last tile, then signals CTA 0.
+//              past S_k of the sequence's last tile, then signals CTA 0;
+//   warp 11    in CTA 0, the P.V issuer.
 #include <algorithm>
 #include <cstdint>
 
@@ -57,9 +57,9 @@ constexpr int kHalfKeys = 64;     // keys of a K tile held by each CTA
 constexpr int kSplit = 2;         // softmax warpgroups sharing a row
 constexpr int kCPT = kBN / kSplit;    // key columns per softmax thread
 constexpr int kOPT = kD / kSplit;     // output columns per softmax thread
-constexpr int kThreads2 = 128 * kSplit + 96;
+constexpr int kThreads2 = 128 * kSplit + 128;
 constexpr int kSmThreads2 = 128 * kSplit;
-constexpr int kWarpTma2 = 8, kWarpMma2 = 9, kWarpRel2 = 10;
+constexpr int kWarpTma2 = 8, kWarpMma2 = 9, kWarpRel2 = 10, kWarpPv2 = 11;
 
 template <int NK, int NV>
 struct C2Cfg {
@@ -75,9 +75,9 @@ struct C2Cfg {
     static constexpr int kOffV = kOffK + NK * kKBytes;
     static constexpr int kOffBar = kOffV + NV * kVBytes;
     // q_full, k_full[NK], k_empty[NK], v_land[NV], v_full[NV], v_empty[NV],
-    // s_full[2], p_full[2], pv_done[2], drain, never (the testing hook's
+    // s_full[2], p_full[2], pv_done[2], drain[2], never (the testing hook's
     // stall waits on it; nothing arrives)
-    static constexpr int kNumBars = 1 + 2 * NK + 3 * NV + 6 + 2;
+    static constexpr int kNumBars = 1 + 2 * NK + 3 * NV + 6 + 3;
     static constexpr int kOffRed = (kOffBar + kNumBars * 8 + 15) / 16 * 16;   // [2][kSplit][128] fp32
     static constexpr int kOffMisc = kOffRed + 2 * kSplit * kRows * 4;
     static constexpr int kSmem = kOffMisc + 16 + 1024;
@@ -164,8 +164,8 @@ prefill_cta2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     const uint32_t s_full0 = smem_u32(&bar_mem[kBarS]);         // + 8 * (j & 1)
     const uint32_t p_full0 = smem_u32(&bar_mem[kBarS + 2]);     // CTA 0's: 8 warps x 2 CTAs
     const uint32_t pv_done0 = smem_u32(&bar_mem[kBarS + 4]);
-    const uint32_t drain = smem_u32(&bar_mem[kBarS + 6]);
-    const uint32_t never = smem_u32(&bar_mem[kBarS + 7]);
+    const uint32_t drain0 = smem_u32(&bar_mem[kBarS + 6]);     // + 8 * issuer
+    const uint32_t never = smem_u32(&bar_mem[kBarS + 8]);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
 
@@ -185,7 +185,8 @@ prefill_cta2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             mbar_init(p_full0 + 8 * x, 2 * kSmThreads2 / 32);
             mbar_init(pv_done0 + 8 * x, 1);
         }
-        mbar_init(drain, 1);
+        mbar_init(drain0, 1);
+        mbar_init(drain0 + 8, 1);
         mbar_init(never, 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -320,34 +321,47 @@ prefill_cta2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 mbar_wait_bounded(v_land0 + 8 * (j % NV), (j / NV) & 1);
         }
         __syncwarp();
-    } else if (warp == kWarpMma2) {
+    } else if (warp == kWarpMma2 || warp == kWarpPv2) {
+        // (CTA 1's warps 9 and 11 have no MMA work: they go straight to the end.)
         if (rank == 0) {
-            // ------------------------ MMA issuer (CTA 0, one thread) ------------------------
-            constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(2 * kRows, kBN, false, false);
-            constexpr uint32_t idesc_pv = tc::idesc_bf16_f32(2 * kRows, kD, false, true);
-            const uint32_t peer = 1;
-            // Shared-memory descriptors as a base per operand buffer plus a
-            // compile-time offset per MMA: the start-address field holds the
-            // byte address >> 4 (below 2^14 for any shared-memory address), so
-            // adding an offset never carries into the next field.
-            const uint64_t q_desc = tc::smem_desc_sw128(sQ, 16, 1024);
-            const uint64_t k_desc0 = tc::smem_desc_sw128(sK, 16, 1024);
-            const uint64_t v_desc0 = tc::smem_desc_sw128(sV, C::kVPanel, 1024);
-            auto wwait = [&](uint32_t bar, uint32_t par) {
-                return __all_sync(0xffffffffu, wait_or_abort(bar, par, abort_flag, p.err));
-            };
-            auto commit_both = [&](uint32_t bar) {
-                tc::commit_pair(bar);
-                tc::commit_pair(mapa_shared(bar, peer));
-            };
-            auto issue_qk = [&](int j) -> bool {
+        // --------------------- MMA issuers (CTA 0, two threads) ---------------------
+        // Warp 9 issues every S(j) = Q K(j)^T, warp 11 every O += P(j) V(j), so
+        // a P.V is queued as soon as its P is written instead of behind the
+        // issue of the next QK^T (with one issuing thread the pipe idled
+        // between them: an MMA issue returns only as the pipe drains).
+        // S(j + 2) overwrites the columns that hold P(j), so its issuer first
+        // waits for P.V(j) to complete.
+        constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(2 * kRows, kBN, false, false);
+        constexpr uint32_t idesc_pv = tc::idesc_bf16_f32(2 * kRows, kD, false, true);
+        const uint32_t peer = 1;
+        const bool qk_role = warp == kWarpMma2;
+        // Shared-memory descriptors as a base per operand buffer plus a
+        // compile-time offset per MMA: the start-address field holds the byte
+        // address >> 4 (below 2^14 for any shared-memory address), so adding
+        // an offset never carries into the next field.
+        const uint64_t q_desc = tc::smem_desc_sw128(sQ, 16, 1024);
+        const uint64_t k_desc0 = tc::smem_desc_sw128(sK, 16, 1024);
+        const uint64_t v_desc0 = tc::smem_desc_sw128(sV, C::kVPanel, 1024);
+        auto wwait = [&](uint32_t bar, uint32_t par) {
+            return __all_sync(0xffffffffu, wait_or_abort(bar, par, abort_flag, p.err));
+        };
+        auto commit_both = [&](uint32_t bar) {
+            tc::commit_pair(bar);
+            tc::commit_pair(mapa_shared(bar, peer));
+        };
+        bool ok = true;
+        if (qk_role) {
+            ok = wwait(q_full, 0);
+            for (int j = 0; ok && j < n_tiles; ++j) {
                 const int stg = j % NK;
-                // Testing hook: the first K wait waits on a barrier that nothing
-                // completes and gives up after stall_ns.
+                // Testing hook: the first K wait waits on a barrier that
+                // nothing completes and gives up after stall_ns.
                 if (p.stall && j == 0 &&
-                    !__all_sync(0xffffffffu, wait_or_abort(never, 0, abort_flag, p.err, (uint64_t)p.stall_ns)))
-                    return false;
-                if (!wwait(k_full0 + 8 * stg, (j / NK) & 1)) return false;
+                    !(ok = __all_sync(0xffffffffu, wait_or_abort(never, 0, abort_flag, p.err,
+                                                                 (uint64_t)p.stall_ns))))
+                    break;
+                if (j >= 2 && !(ok = wwait(pv_done0 + 8 * (j & 1), ((j - 2) >> 1) & 1))) break;
+                if (!(ok = wwait(k_full0 + 8 * stg, (j / NK) & 1))) break;
                 tc::fence_after_sync();
                 if (lane == 0) {
                     const uint32_t dS = tmem + (j & 1) * kBN;
@@ -362,11 +376,8 @@ prefill_cta2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                     commit_both(k_empty0 + 8 * stg);
                 }
                 __syncwarp();
-                return true;
-            };
-            bool ok = wwait(q_full, 0);
-            if (ok) ok = issue_qk(0);
-            if (ok && n_tiles > 1) ok = issue_qk(1);
+            }
+        } else {
             for (int j = 0; ok && j < n_tiles; ++j) {
                 const int stv = j % NV;
                 if (!(ok = wwait(p_full0 + 8 * (j & 1), (j >> 1) & 1))) break;
@@ -385,13 +396,14 @@ prefill_cta2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                     commit_both(pv_done0 + 8 * (j & 1));
                 }
                 __syncwarp();
-                if (j + 2 < n_tiles) ok = issue_qk(j + 2);
             }
-            // No MMA of the pair may still run when either CTA frees its
-            // tensor memory or leaves.
-            if (lane == 0) tc::commit_pair(drain);
-            __syncwarp();
-            mbar_wait_bounded(drain, 0);
+        }
+        // No MMA of the pair may still run when either CTA frees its tensor
+        // memory or leaves.
+        const uint32_t dr = drain0 + (qk_role ? 0 : 8);
+        if (lane == 0) tc::commit_pair(dr);
+        __syncwarp();
+        mbar_wait_bounded(dr, 0);
         }
     } else {
         // ------------------------- softmax + epilogue warps -----------------------
