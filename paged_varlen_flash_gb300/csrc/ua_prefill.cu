@@ -88,12 +88,12 @@ cudaError_t launch_prefill(const PrefillPlan& plan, const CUtensorMap& tm_k, con
     cuuint32_t box[3] = {64, (cuuint32_t)p.g, (cuuint32_t)(kRows / p.g)};
     if (!encode_bf16_sw128(&tq, p.q, 3, dims, strides, box)) return cudaErrorInvalidValue;
     if (plan.num_tiles <= 0) return cudaSuccess;
-    if (prefill_pair_supported(p.d))
-        return plan.dense ? launch_prefill_grid(tq, tm_k, tm_v, p, (plan.num_tiles + 1) / 2, stream)
-                          : launch_prefill_pair(tq, tm_k, tm_v, p, plan.ctas, stream);
-    if (p.d != 256) return cudaErrorInvalidValue;
     CUtensorMap to;   // the output, boxed like Q
     if (!encode_bf16_sw128(&to, p.out, 3, dims, strides, box)) return cudaErrorInvalidValue;
+    if (prefill_pair_supported(p.d))
+        return plan.dense ? launch_prefill_grid(tq, tm_k, tm_v, to, p, (plan.num_tiles + 1) / 2, stream)
+                          : launch_prefill_pair(tq, tm_k, tm_v, p, plan.ctas, stream);
+    if (p.d != 256) return cudaErrorInvalidValue;
     return launch_prefill_cta2(tq, tm_k, tm_v, to, p, (plan.num_tiles + 1) / 2, stream);
 }
 

@@ -38,8 +38,9 @@ int64_t pair_work_entries_bound(const FwdParams& p, int splits);
 // Enqueue the two-tile kernel as one CTA per (tile pair, KV head, sequence[,
 // segment]) over the padded grid of `pairs` tile pairs per sequence: the form
 // for batches whose padded grid is nearly all real units (ua_prefill_grid.cu).
+// `to` maps the output like tq maps Q (full tiles are stored through it).
 cudaError_t launch_prefill_grid(const CUtensorMap& tq, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
-                                const FwdParams& p, int pairs, cudaStream_t stream);
+                                const CUtensorMap& to, const FwdParams& p, int pairs, cudaStream_t stream);
 
 // Enqueue the planner (the longest-first work list in p.work_list) and the
 // persistent two-tile kernel on `ctas` CTAs; tq is the Q tensor map (boxes of

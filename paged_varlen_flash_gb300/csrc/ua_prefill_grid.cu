@@ -103,7 +103,8 @@ struct GR {
 template <int D, int NK, int NV, bool PLAIN, bool QQ>
 __global__ void __launch_bounds__(GR::kThreads, 1)
 prefill_grid_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                    const FwdParams p) {
     using C = GridCfg<D, NK, NV>;
     using R = GR;
     constexpr int kThreads = R::kThreads;
@@ -582,6 +583,14 @@ prefill_grid_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             p.part_ml[(row * p.splits + seg) * 2 + 0] = nx > 0 ? m : -INFINITY;
             p.part_ml[(row * p.splits + seg) * 2 + 1] = nx > 0 ? l : 0.f;
         }
+        // A tile whose rows are all valid goes out through shared memory --
+        // its own Q buffer, free once its last QK^T has run, in the layout of
+        // the map's boxes -- and one TMA store per 64-column panel: rows of a
+        // tile lie H_q * d elements apart in the output, so per-thread row
+        // stores touch one sector per lane.  A sequence's last tile, whose
+        // padding rows must not be written, keeps the per-thread stores.
+        const bool staged = !split && nx > 0 && (x == 0 || has_b) && last - first + 1 == ppt;
+        uint8_t* stage = smem + C::kOffQ + x * C::kQTile;
         if (ok && live && nx > 0) {
             // tcgen05.ld is warp-collective: every lane of a live warp loads.
             tc::fence_after_sync();
@@ -623,7 +632,15 @@ prefill_grid_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                         v.y = pack_bf16x2(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
                         v.z = pack_bf16x2(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv);
                         v.w = pack_bf16x2(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv);
-                        *reinterpret_cast<uint4*>(orow + e) = v;
+                        if (staged) {
+                            // panel c / 2, 16-byte chunk (c % 2) * 4 + e / 8 of
+                            // row r, 128-byte swizzled
+                            const int chunk = (c & 1) * 4 + e / 8;
+                            *reinterpret_cast<uint4*>(stage + (c / 2) * C::kQPanel + r * 128 +
+                                                      ((chunk ^ (r & 7)) * 16)) = v;
+                        } else {
+                            *reinterpret_cast<uint4*>(orow + e) = v;
+                        }
                     }
                 }
             }
@@ -632,6 +649,18 @@ prefill_grid_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             // the row is zero.
             __nv_bfloat16* orow = p.out + ((q0 + pos) * p.hq + head) * (int64_t)D;
             for (int c = 0; c < D; c += 8) *reinterpret_cast<uint4*>(orow + c) = make_uint4(0, 0, 0, 0);
+        }
+        if (staged) {
+            // Every thread of the warpgroup arrives (the vote carries whether
+            // all of them got their output), then one thread stores.
+            fence_proxy_async_smem();
+            if (bar_and_sync(2 + x, kRows, ok) && r == 0) {
+#pragma unroll
+                for (int pn = 0; pn < C::kPanels; ++pn)
+                    tma_store_3d(&tm_o, pn * 64, hkv * g, (int)(q0 + first),
+                                 smem_u32(stage + pn * C::kQPanel));
+                bulk_commit_and_wait_read();
+            }
         }
     }
 
@@ -645,32 +674,32 @@ prefill_grid_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
 
 template <int D, int NK, int NV, bool PLAIN, bool QQ = false>
 cudaError_t launch_grid_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                          const FwdParams& p, int pairs, cudaStream_t stream) {
+                          const CUtensorMap& to, const FwdParams& p, int pairs, cudaStream_t stream) {
     using C = GridCfg<D, NK, NV>;
     constexpr int kThreads = GR::kThreads;
     auto kern = prefill_grid_kernel<D, NK, NV, PLAIN, QQ>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)(pairs * p.splits), (unsigned)p.hk, (unsigned)p.num_seqs);
-    kern<<<grid, kThreads, C::kSmem, stream>>>(tq, tk, tv, p);
+    kern<<<grid, kThreads, C::kSmem, stream>>>(tq, tk, tv, to, p);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_prefill_grid(const CUtensorMap& tq, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
-                                const FwdParams& p, int pairs, cudaStream_t stream) {
+                                const CUtensorMap& to, const FwdParams& p, int pairs, cudaStream_t stream) {
     const bool qq = (p.flags & UA_FLAG_QQ_BIAS) != 0;
     const bool plain = !qq && (p.flags & (UA_FLAG_SOFTCAP | UA_FLAG_ALIBI)) == 0;
     switch (p.d) {
         case 64:
-            if (qq) return launch_grid_t<64, 4, 4, false, true>(tq, tm_k, tm_v, p, pairs, stream);
-            return plain ? launch_grid_t<64, 4, 4, true>(tq, tm_k, tm_v, p, pairs, stream)
-                         : launch_grid_t<64, 4, 4, false>(tq, tm_k, tm_v, p, pairs, stream);
+            if (qq) return launch_grid_t<64, 4, 4, false, true>(tq, tm_k, tm_v, to, p, pairs, stream);
+            return plain ? launch_grid_t<64, 4, 4, true>(tq, tm_k, tm_v, to, p, pairs, stream)
+                         : launch_grid_t<64, 4, 4, false>(tq, tm_k, tm_v, to, p, pairs, stream);
         case 128:
-            if (qq) return launch_grid_t<128, 2, 2, false, true>(tq, tm_k, tm_v, p, pairs, stream);
-            return plain ? launch_grid_t<128, 2, 2, true>(tq, tm_k, tm_v, p, pairs, stream)
-                         : launch_grid_t<128, 2, 2, false>(tq, tm_k, tm_v, p, pairs, stream);
+            if (qq) return launch_grid_t<128, 2, 2, false, true>(tq, tm_k, tm_v, to, p, pairs, stream);
+            return plain ? launch_grid_t<128, 2, 2, true>(tq, tm_k, tm_v, to, p, pairs, stream)
+                         : launch_grid_t<128, 2, 2, false>(tq, tm_k, tm_v, to, p, pairs, stream);
         default: return cudaErrorInvalidValue;
     }
 }
