@@ -1,5 +1,5 @@
 // ua_prefill_common.cuh -- device helpers shared by the tensor-core prefill
-// kernels: warp roles, bounded mbarrier waits that honour the CTA's abort
+// kernels: bounded mbarrier waits that honour the CTA's abort
 // flag, packed fp32 arithmetic, the base-2 exponential of a pair, a named
 // barrier with an AND vote.
 #pragma once
@@ -14,21 +14,7 @@ namespace pf {
 
 constexpr float kLazy = 8.0f;
 constexpr int kRows = 128;
-// SPLIT softmax warpgroups share each row's BN key columns (SPLIT parts of
-// BN / SPLIT); one more warp issues TMA copies, one issues QK^T and one P.V.
-template <int SPLIT>
-struct Roles {
-    static constexpr int kSmThreads = 128 * SPLIT;
-    static constexpr int kThreads = kSmThreads + 96;
-    static constexpr int kWarpTma = 4 * SPLIT;
-    static constexpr int kWarpMma = 4 * SPLIT + 1;   // QK^T issuer, tensor-memory owner
-    static constexpr int kWarpPv = 4 * SPLIT + 2;    // P.V issuer
-};
 constexpr uint32_t kTmemCols = 512;
-
-struct Bars {
-    uint32_t q_full, k_full0, v_full0, k_empty0, v_empty0, s_full0, p_full, o_done, drain;
-};
 
 // Wait on an mbarrier phase; gives up (and raises the CTA's abort flag and the
 // device error bit) after about a second, or as soon as another role aborted.
@@ -78,19 +64,6 @@ __device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
         : "=l"(d)
         : "l"(*reinterpret_cast<uint64_t*>(&a)), "l"(*reinterpret_cast<uint64_t*>(&b)));
     return *reinterpret_cast<float2*>(&d);
-}
-
-// 2^a for a pair: the argument rounded to fp16, the hardware fp16x2 base-2
-// exponential, and the two results widened back to fp32.  -inf maps to 0.
-__device__ __forceinline__ float2 exp2_pair_f16(float2 a) {
-    uint32_t h, e;
-    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(a.y), "f"(a.x));
-    asm("ex2.approx.f16x2 %0, %1;" : "=r"(e) : "r"(h));
-    float lo, hi;
-    asm("{\n\t.reg .f16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
-        : "=f"(lo), "=f"(hi)
-        : "r"(e));
-    return make_float2(lo, hi);
 }
 
 // 2^a for a pair on the fp32 special-function path.  -inf maps to 0.
