@@ -158,7 +158,11 @@ def test_long_prefill_shuffled_table_bit_identical():
 @pytest.mark.parametrize("d,b,hq,hk,sq,sk", [(64, 16, 8, 2, [7, 30, 1], [40, 30, 77]),
                                              (128, 16, 32, 8, [1, 1, 1], [300, 513, 17]),
                                              (128, 64, 16, 4, [60, 2], [60, 700]),
-                                             (256, 32, 4, 4, [33, 1], [90, 2000])])
+                                             (256, 32, 4, 4, [33, 1], [90, 2000]),
+                                             # full d = 256 tiles (the output goes out by
+                                             # TMA from shared memory): g = 1 and g = 2
+                                             (256, 64, 4, 4, [256], [300]),
+                                             (256, 16, 8, 4, [128, 3], [128, 40])])
 def test_position_tags_bit_exact(d, b, hq, hk, sq, sk, path):
     need = sum((k + b - 1) // b for k in sk)
     w = W.build("tags", hq, hk, d, b, sq, sk, need + 7, 1.0, seed=5, values=False, poison=True,
