@@ -95,13 +95,15 @@ enum { UA_DTYPE_BF16 = 0, UA_DTYPE_FP8_E4M3 = 1 };
 /* Execution path (gfx950 spec section 6: a path whose query-tile grid fills
  * the device versus split-KV segments plus a reduction).
  *   SPLIT_KV     CUDA-core split-KV kernel + combine, any shape.
- *   TENSOR_CORE  tcgen05 kernel over tiles of 128 packed (position, head)
+ *   TENSOR_CORE  tcgen05 kernels over tiles of 128 packed (position, head)
  *                rows (floor(128 / g) positions of the g heads of one KV
- *                head), KV-split + combine when the tile grid is small;
- *                needs g <= 128.
+ *                head): two tiles per CTA at d = 64 and 128, two tiles per
+ *                cluster of two CTAs at d = 256; KV-split + combine when the
+ *                tile grid is small; needs g <= 128.
  *   DECODE_TC    tcgen05 kernel with the keys on the MMA M dimension for
- *                calls with at most 16 packed rows per KV head; needs d = 128
- *                and g * max_seqlen_q <= 16.
+ *                calls with at most 16 packed rows per KV head: needs
+ *                g * max_seqlen_q <= 16 (d = 64, 128 or 256; an fp8 cache
+ *                needs d = 128).
  *   AUTO         DECODE_TC when it applies, else TENSOR_CORE when it applies
  *                and a KV head has more than 16 packed rows, else SPLIT_KV.
  * A forced path that does not apply returns UA_ERR_UNSUPPORTED. */
