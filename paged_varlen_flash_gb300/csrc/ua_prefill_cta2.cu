@@ -454,15 +454,28 @@ prefill_cta2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                     // ALiBi: one int -> float conversion per tile; the per-key
                     // offsets are compile-time constants.
                     const float abias = slope * (float)(key0 - ctx);
+                    if (softcap) {
 #pragma unroll
-                    for (int c = 0; c < kCPT / 32; ++c)
+                        for (int c = 0; c < kCPT / 32; ++c)
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) {
-                            float t = __uint_as_float(sr[c][e]) * p.scale;
-                            if (softcap) t = p.softcap * tanh_from_exp2(t * inv_cap);
-                            if (alibi) t += abias + slope * (float)(c * 32 + e);
-                            sr[c][e] = __float_as_uint(t * kLog2e);
-                        }
+                            for (int e = 0; e < 32; ++e) {
+                                float t = __uint_as_float(sr[c][e]) * p.scale;
+                                t = p.softcap * tanh_from_exp2(t * inv_cap);
+                                if (alibi) t += abias + slope * (float)(c * 32 + e);
+                                sr[c][e] = __float_as_uint(t * kLog2e);
+                            }
+                    } else {
+                        // No softcap: the score and the ALiBi term straight in
+                        // log2 units, two FMAs per score (slope = 0 without
+                        // ALiBi).
+                        const float sc2 = p.scale * kLog2e, sl2a = slope * kLog2e, ab2 = abias * kLog2e;
+#pragma unroll
+                        for (int c = 0; c < kCPT / 32; ++c)
+#pragma unroll
+                            for (int e = 0; e < 32; ++e)
+                                sr[c][e] = __float_as_uint(fmaf(__uint_as_float(sr[c][e]), sc2,
+                                                                fmaf(sl2a, (float)(c * 32 + e), ab2)));
+                    }
                     // Query-query bias, in its own pass: the query-section keys
                     // up to the row's last visible key (so j - ctx < S_q), in
                     // log2 units like the scores it joins.
